@@ -1,0 +1,82 @@
+"""Planted mistakes in a copy of the oracle must each fail at least one pin.
+
+The copy is made from the oracle's source text with one plausible error
+inserted (a dropped term, a wrong sign or index, a wrong operand); it runs on
+the CPU only.  The pins re-run here are the independent ones from
+test_oracle_pins: brute force, torch SDPA on single documents, and finite
+differences.
+"""
+import os
+import types
+
+import numpy as np
+import pytest
+
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                   "oracle", "blockdiag.py")
+
+MUTATIONS = {
+    "causal_off_by_one": ("keys[None, :] <= np.arange(r0, r1)[:, None]",
+                          "keys[None, :] <= np.arange(r0, r1)[:, None] + 1"),
+    "cross_document": ("if ids[p] != ids[p - 1]]", "if ids[p] != ids[p - 1] and ids[p] == 0]"),
+    "gqa_modulo": ("g = h // G", "g = h % Hkv"),
+    "pad_not_masked": ("if sid == PAD_DOC_ID:\n                continue",
+                       "if False:\n                continue"),
+    "lse_without_log": ("row_lse = m + np.log(np.exp(s - m).sum(axis=1, keepdims=True))",
+                        "row_lse = m + np.exp(s - m).sum(axis=1, keepdims=True) - 1.0"),
+    "dq_missing_scale": ("dq[b, h, i0:i1] = scale * (ds @ kk)", "dq[b, h, i0:i1] = ds @ kk"),
+    "ds_sign": ("ds = p * (dp - delta[b, h, i0:i1, None])",
+                "ds = p * (dp + delta[b, h, i0:i1, None])"),
+    "dv_into_dk": ("dv[b, g, start:r1] += p.T @ dout[b, h, i0:i1]",
+                   "dk[b, g, start:r1] += p.T @ dout[b, h, i0:i1]"),
+    "dk_uses_k": ("dk[b, g, start:r1] += scale * (ds.T @ q[b, h, i0:i1])",
+                  "dk[b, g, start:r1] += scale * (ds.T @ q[b, h, i0:i1][:, ::-1])"),
+    "interval_offset": ("q[b, h, r0 - seq_start:r1 - seq_start] @ k[b, g, start:r1].T",
+                        "q[b, h, r0:r1] @ k[b, g, start:r1].T"),
+}
+
+
+def _mutant(name):
+    src = open(SRC).read()
+    old, new = MUTATIONS[name]
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mod = types.ModuleType(f"oracle_mutant_{name}")
+    exec(compile(src.replace(old, new), SRC, "exec"), mod.__dict__)
+    return mod
+
+
+def _pins(orc, monkeypatch):
+    monkeypatch.setattr(pins, "orc", orc)
+    checks = [
+        lambda: pins.test_golden_tiny_segments(),
+        lambda: pins.test_golden_padded_small(),
+        lambda: pins.test_forward_matches_brute_force(
+            ([[4, 4, 4, 4, 4, 7, 7, 7, 0, 0, 9, 9]], 3, 6, 4, 2, 2)),
+        lambda: pins.test_forward_matches_brute_force(
+            ([[1, 1, 2, 2, 1, 1, 0, 0]], 0, 8, 2, 2, 4)),
+        lambda: pins.test_single_document_is_torch_causal_sdpa(8),
+        lambda: pins.test_packed_equals_documents_run_separately(),
+        lambda: pins.test_backward_matches_finite_differences(),
+    ]
+    failed = 0
+    for c in checks:
+        try:
+            c()
+        except (AssertionError, IndexError, ValueError, FloatingPointError):
+            failed += 1
+    return failed
+
+
+def test_unmutated_oracle_passes_all(monkeypatch):
+    src = open(SRC).read()
+    mod = types.ModuleType("oracle_copy")
+    exec(compile(src, SRC, "exec"), mod.__dict__)
+    assert _pins(mod, monkeypatch) == 0
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, monkeypatch):
+    with np.errstate(all="ignore"):
+        assert _pins(_mutant(name), monkeypatch) >= 1
