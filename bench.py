@@ -1,0 +1,432 @@
+#!/usr/bin/env python
+"""Benchmark of the block-diagonal causal attention hot path on GB300.
+
+One step = the whole path on one synthetic packed batch, every call through
+the C ABI: doc ids from cu_seqlens -> segments -> plan (tile classifier and
+longest-first lists) -> forward -> backward (per-row terms, main kernel, dq
+conversion).  Default workload: 1 row x 8192 tokens, Hq=32, Hkv=8, D=128,
+lognormal(1024, 1.0) document lengths (seed 0).
+
+Metric: useful TFLOP/s = 14 * D * (unmasked query/key pairs) * Hq per step
+(4*D forward + 10*D backward per pair and query head) over the step time;
+tokens/s (non-padding query tokens) is reported beside it.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 run under torch.distributed.run: every rank runs its own replica of
+the workload (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from packed_sequence_block_gb300.workloads import make_qkv_do, make_workload  # noqa: E402
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="lognormal8k")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the CPU baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    return ap.parse_args()
+
+
+def useful_pairs(wl):
+    total = 0
+    for cu in wl.cu:
+        cu = [int(x) for x in cu]
+        for s0 in wl.seq_starts:
+            for a, b in zip(cu[:-1], cu[1:]):
+                lo, hi = max(a, s0), min(b, s0 + wl.L)
+                if lo < hi:
+                    n1, n2 = lo - a + 1, hi - a
+                    total += (n1 + n2) * (n2 - n1 + 1) // 2
+    return total
+
+
+def describe(wl):
+    docs = sum(len(c) - 1 for c in wl.cu)
+    pad = sum(wl.S - int(c[-1]) for c in wl.cu)
+    return (f"{wl.name}: {wl.B} row(s) x {wl.S} tokens, Hq={wl.Hq}, Hkv={wl.Hkv}, D={wl.D}, "
+            f"{docs} docs, {pad} padding tokens, {len(wl.seq_starts)} query interval(s) of "
+            f"{wl.L}, seed {wl.seed}")
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    def __init__(self, path):
+        self.path = path
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self, gpu_index):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    if int(parts[0]) != gpu_index:
+                        continue
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, val in zip(names[1:], parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+class HotPath:
+    """Device buffers and the per-step call sequence through the C ABI."""
+
+    def __init__(self, wl, device):
+        from packed_sequence_block_gb300 import _native as N
+        from packed_sequence_block_gb300.attention import device_status_word
+        self.N, self.wl, self.dev = N, wl, device
+        B, S, L, Hq, Hkv, D = wl.B, wl.S, wl.L, wl.Hq, wl.Hkv, wl.D
+        flat, rp = wl.cu_csr()
+        self.cu_h = torch.from_numpy(flat).pin_memory()
+        self.rp_h = torch.from_numpy(rp).pin_memory()
+        self.cu = self.cu_h.to(device)
+        self.rp = self.rp_h.to(device)
+        q, k, v, do = make_qkv_do(wl, device=device, generator_device=device)
+        self.k, self.v = k, v
+        self.q_iv = [q[:, :, s:s + L].contiguous() for s in wl.seq_starts]
+        self.do_iv = [do[:, :, s:s + L].contiguous() for s in wl.seq_starts]
+        del q, do
+        self.ids = torch.empty((B, S), dtype=torch.int32, device=device)
+        self.seg = torch.empty((B, S + 1), dtype=torch.int32, device=device)
+        self.sid = torch.empty((B, S), dtype=torch.int32, device=device)
+        self.nseg = torch.empty((B,), dtype=torch.int32, device=device)
+        self.plans = [torch.empty(N.bd_attn_plan_size(B, Hq, Hkv, L, S), dtype=torch.uint8,
+                                  device=device) for _ in wl.seq_starts]
+        self.out = [torch.empty_like(x) for x in self.q_iv]
+        self.lse = [torch.empty((B, Hq, L), dtype=torch.float32, device=device)
+                    for _ in wl.seq_starts]
+        self.dq = [torch.empty_like(x) for x in self.q_iv]
+        self.dk = torch.empty_like(k)
+        self.dv = torch.empty_like(v)
+        self.ws = torch.empty(N.bd_attn_bwd_workspace_size(B, Hq, Hkv, L, S, D),
+                              dtype=torch.uint8, device=device)
+        self.status = device_status_word(device)
+        self.scale = D ** -0.5
+        self.gqa = Hq != Hkv
+        self.main_events = []
+
+    def launches_per_step(self):
+        return 2 + len(self.wl.seq_starts) * 7
+
+    def step(self, time_main=False):
+        N, wl = self.N, self.wl
+        B, S, L, Hq, Hkv, D = wl.B, wl.S, wl.L, wl.Hq, wl.Hkv, wl.D
+        N.bd_doc_ids_from_cu_seqlens(self.cu, self.rp, B, S, self.ids, self.status)
+        N.bd_segment_cu_seqlens(self.ids, B, S, self.seg, self.sid, self.nseg)
+        for i, s0 in enumerate(wl.seq_starts):
+            N.bd_attn_plan(self.seg, self.sid, self.nseg, B, Hq, Hkv, L, S, s0, self.plans[i])
+            N.bd_attn_fwd(self.q_iv[i], self.k, self.v, B, Hq, Hkv, L, S, D, s0, self.scale,
+                          self.gqa, self.plans[i], self.out[i], self.lse[i], self.status)
+            args = (self.q_iv[i], self.k, self.v, self.out[i], self.lse[i], self.do_iv[i], B, Hq,
+                    Hkv, L, S, D, s0, self.scale, self.gqa, self.plans[i], self.dq[i], self.dk,
+                    self.dv, self.ws, self.status)
+            N.bd_attn_bwd_stages(*args, stages=1)
+            if time_main:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+            N.bd_attn_bwd_stages(*args, stages=2)
+            if time_main:
+                e1.record()
+                self.main_events.append((e0, e1))
+            N.bd_attn_bwd_stages(*args, stages=4)
+
+    def e2e_buffers(self):
+        """Pinned host copies of the inputs and room for the results."""
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)  # noqa: E731
+        self.h_in = []
+        for dev_t in [self.k, self.v, *self.q_iv, *self.do_iv]:
+            h = pin(dev_t)
+            h.copy_(dev_t)
+            self.h_in.append((h, dev_t))
+        self.h_out = [(pin(t), t) for t in [*self.out, *self.lse, *self.dq, self.dk, self.dv]]
+        h2d = sum(h.numel() * h.element_size() for h, _ in self.h_in)
+        h2d += self.cu_h.numel() * 4 + self.rp_h.numel() * 4
+        d2h = sum(h.numel() * h.element_size() for h, _ in self.h_out)
+        return h2d, d2h
+
+    def e2e_step(self):
+        self.cu.copy_(self.cu_h, non_blocking=True)
+        self.rp.copy_(self.rp_h, non_blocking=True)
+        for h, d in self.h_in:
+            d.copy_(h, non_blocking=True)
+        self.step()
+        for h, d in self.h_out:
+            h.copy_(d, non_blocking=True)
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def oracle_inputs(wl, seed):
+    from oracle import blockdiag as orc
+    q, k, v, do = make_qkv_do(wl, seed=seed, device="cpu")
+    ids = np.stack([orc.doc_ids_from_cu_seqlens(c, wl.S) for c in wl.cu])
+    return q, k, v, do, ids
+
+
+def cpu_oracle_sample(wl, budget_s, inputs):
+    """Time the fp64 oracle (fwd + bwd) on whole kv-head groups until the budget is used."""
+    from oracle import blockdiag as orc
+    q, k, v, do, ids = inputs
+    G = wl.G
+    s0 = wl.seq_starts[0]
+    pairs_all = useful_pairs_interval(wl, s0)
+    done_heads, elapsed = 0, 0.0
+    t_start = time.perf_counter()
+    for g in range(wl.Hkv):
+        hs = slice(g * G, (g + 1) * G)
+        qi = q[:, hs, s0:s0 + wl.L]
+        di = do[:, hs, s0:s0 + wl.L]
+        kg, vg = k[:, g:g + 1], v[:, g:g + 1]
+        o, l = orc.blockdiag_sdpa_forward(qi, kg, vg, ids, s0, None, G > 1)
+        orc.blockdiag_sdpa_backward(qi, kg, vg, di, ids, s0, None, G > 1, out=o, lse=l)
+        done_heads += G
+        elapsed = time.perf_counter() - t_start
+        if elapsed >= budget_s:
+            break
+    flops = 14.0 * wl.D * pairs_all * done_heads
+    return {
+        "value": flops / elapsed / 1e12, "unit": "TFLOP/s", "kind": "oracle",
+        "cores": len(os.sched_getaffinity(0)),
+        "sample": (f"{done_heads} of {wl.Hq} query heads ({done_heads // G} kv-head groups), "
+                   f"query interval at {s0}, forward+backward in numpy fp64, "
+                   f"{elapsed:.1f} s"),
+        "seconds": elapsed,
+    }
+
+
+def useful_pairs_interval(wl, s0):
+    total = 0
+    for cu in wl.cu:
+        cu = [int(x) for x in cu]
+        for a, b in zip(cu[:-1], cu[1:]):
+            lo, hi = max(a, s0), min(b, s0 + wl.L)
+            if lo < hi:
+                n1, n2 = lo - a + 1, hi - a
+                total += (n1 + n2) * (n2 - n1 + 1) // 2
+    return total
+
+
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return
+    pairs = useful_pairs(wl)
+    inputs = oracle_inputs(wl, args.seed)
+    for _ in range(args.warmup):
+        cpu_oracle_sample(wl, 0.0, inputs)
+    vals, secs = [], []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r = cpu_oracle_sample(wl, 0.0, inputs)
+        vals.append(r["value"])
+        secs.append(r["seconds"])
+    total = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": "useful TFLOP/s, block-causal varlen attention fwd+bwd",
+        "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": describe(wl), "useful_pairs": pairs},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "kind": "oracle",
+                         "cores": len(os.sched_getaffinity(0)),
+                         "sample": f"one kv-head group ({wl.G} of {wl.Hq} query heads) per "
+                                   f"step, forward+backward in numpy fp64"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = make_workload(args.workload, args.seed)
+    if args.impl == "reference":
+        run_reference(args, wl, rank, world)
+        return
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    from packed_sequence_block_gb300.attention import check_device_status
+
+    hp = HotPath(wl, device)
+    pairs = useful_pairs(wl)
+    D, Hq = wl.D, wl.Hq
+    flops_step = 14.0 * D * pairs * Hq
+    flops_bwd_main_step = 10.0 * D * pairs * Hq  # all intervals of one step
+    tokens_step = wl.non_pad_tokens()
+    l2_buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+
+    for _ in range(max(3, args.warmup)):
+        hp.step()
+    torch.cuda.synchronize()
+    check_device_status(device)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    peaks, peak_src = read_peaks()
+    sampler = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
+                           if os.path.isdir(os.path.join(ROOT, "gpurun_out"))
+                           else f"/tmp/bd_clocks_{os.getpid()}.csv")
+    step_ms = []
+    barrier()
+    with sampler:
+        for _ in range(args.steps):
+            flush_l2(l2_buf)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            hp.step(time_main=True)
+            e1.record()
+            step_ms.append((e0, e1))
+        barrier()
+    check_device_status(device)
+    times = [a.elapsed_time(b) for a, b in step_ms]
+    main_ms = [a.elapsed_time(b) for a, b in hp.main_events]
+    total_ms = sum(times)
+
+    # end to end through the public API with host buffers (copies inside the timed region)
+    h2d, d2h = hp.e2e_buffers()
+    for _ in range(2):
+        hp.e2e_step()
+    barrier()
+    e_ms = []
+    for _ in range(args.e2e_steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        hp.e2e_step()
+        e1.record()
+        e_ms.append((e0, e1))
+    barrier()
+    e2e_total = sum(a.elapsed_time(b) for a, b in e_ms)
+
+    t = torch.tensor([total_ms, e2e_total], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    total_ms, e2e_total = float(t[0]), float(t[1])
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    e2e_value = world * flops_step * args.e2e_steps / (e2e_total * 1e-3) / 1e12
+    tok_s = world * tokens_step * args.steps / (total_ms * 1e-3)
+
+    main_avg = statistics.mean(main_ms)
+    achieved = flops_bwd_main_step * args.steps / (sum(main_ms) * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    clocks = sampler.summary(local)
+
+    if rank == 0:
+        line = {
+            "metric": "useful TFLOP/s, block-causal varlen attention fwd+bwd",
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": describe(wl), "B": wl.B, "S": wl.S, "L": wl.L, "Hq": Hq,
+                       "Hkv": wl.Hkv, "D": D, "useful_pairs": pairs,
+                       "useful_tflop_per_step": flops_step / 1e12,
+                       "strict_12D_tflops": value * 12.0 / 14.0,
+                       "l2": "flushed between timed steps (256 MiB write, outside the events)",
+                       "parallelism": f"{world} independent replica(s)"},
+            "tokens_per_s": tok_s,
+            "frac_of_bf16_peak": value / peak,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": hp.launches_per_step() * args.steps,
+            "roofline": {"kernel": "bd_bwd_kernel (backward main)", "bound": "tensor",
+                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_source": f"{peak_src} bf16_tflops (burst)",
+                         "avg_launch_ms": main_avg},
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_oracle_sample(wl, args.cpu_budget,
+                                                     oracle_inputs(wl, args.seed))
+            line["cpu_baseline"].pop("seconds", None)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,179 @@
+/*
+ * bd_attn.h -- C ABI of the GB300 (sm_103a) block-diagonal causal attention
+ * library for packed sequences (libbd_attn.so).
+ *
+ * The operation is the one described on the NeMo Automodel API reference page
+ * "nemo_automodel.components.distributed.blockdiag_cp", function
+ * cp_blockdiag_sdpa: local queries [B, Hq, L, D] attend the delivered keys and
+ * values [B, Hkv, S, D] under a per-document causal mask rebuilt from document
+ * ids, so documents packed into one row never attend across a boundary.  The
+ * document ids and their segments follow the page
+ * "nemo_automodel.components.models.glm5_next.cp" (doc_ids_from_cu_seqlens,
+ * segment_cu_seqlens, _PAD_DOC_ID = 0).  Queries may be a contiguous
+ * interval [seq_start, seq_start + L) of the row (Glm5NextPackedContext
+ * .seq_start on the same page), as a context-parallel rank sees them.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    never allocates, frees or synchronises; every call only enqueues work on
+ *    `stream` (a cudaStream_t; NULL = the legacy default stream) and returns.
+ *  - Tensors are dense, row-major, with the shapes given below; bf16 data is
+ *    passed as `const void*` / `void*` (IEEE bfloat16, 2 bytes).  q, k, v,
+ *    out, dout, dq, dk, dv must be 16-byte aligned.
+ *  - The return value is a bd_status_t.  Host-side argument errors return
+ *    BD_ERR_INVALID_ARG / BD_ERR_UNSUPPORTED / BD_ERR_WORKSPACE before any
+ *    work is enqueued.  A failed launch returns BD_ERR_CUDA.  Errors found on
+ *    the device (invalid cu_seqlens, a wait that timed out) are written to the
+ *    caller's `dev_status` word (int32, device memory, may be NULL); the
+ *    first error of a call is kept.  bd_get_device_status() reads it back.
+ *  - Document id 0 marks padding.  A query in a padding segment attends
+ *    nothing: its output row is 0, its log-sum-exp -inf, its dq row 0.  Keys
+ *    that no query of the call attends get dk = dv = 0.
+ */
+#ifndef BD_ATTN_H
+#define BD_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* bd_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  BD_OK = 0,
+  BD_ERR_INVALID_ARG = 1, /* bad shape, pointer, alignment or cu_seqlens */
+  BD_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. head dim not 64/128) */
+  BD_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+  BD_ERR_TIMEOUT = 4,     /* a device-side wait gave up (reported via dev_status) */
+  BD_ERR_WORKSPACE = 5    /* plan or workspace buffer too small */
+} bd_status_t;
+
+/* Human-readable text for a status code (static storage, never NULL). */
+const char* bd_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int bd_version(void);
+
+/*
+ * Document ids from cumulative boundaries (page
+ * "nemo_automodel.components.models.glm5_next.cp", doc_ids_from_cu_seqlens,
+ * and _PAD_DOC_ID = 0).
+ *   cu       int32, the B rows' boundary lists concatenated.  Row b's list is
+ *            cu[row_ptr[b] .. row_ptr[b+1]-1]: n_b + 1 entries, starting at 0,
+ *            non-decreasing, last entry <= S.  Zero-length documents allowed.
+ *   row_ptr  int32 [B+1], row_ptr[0] = 0, row_ptr[b+1] - row_ptr[b] >= 1.
+ *   doc_ids  int32 [B, S] output: position p of row b gets d + 1 when
+ *            cu_b[d] <= p < cu_b[d+1], and 0 (padding) when p >= cu_b[n_b].
+ * A row whose list breaks the rules above gets all ids 0 and
+ * BD_ERR_INVALID_ARG in *dev_status.
+ */
+int bd_doc_ids_from_cu_seqlens(const int32_t* cu, const int32_t* row_ptr, int B, int S,
+                               int32_t* doc_ids, int32_t* dev_status, bd_stream_t stream);
+
+/*
+ * Segment boundaries of each row (page
+ * "nemo_automodel.components.models.glm5_next.cp", segment_cu_seqlens):
+ * the maximal runs of equal ids, padding runs included, covering the row.
+ *   doc_ids  int32 [B, S].
+ *   seg      int32 [B, S+1] output: row b's boundaries are
+ *            seg[b*(S+1) + 0 .. nseg[b]], seg[..0] = 0, seg[..nseg[b]] = S.
+ *   seg_ids  int32 [B, S] output: seg_ids[b*S + k] = id carried by run k.
+ *   nseg     int32 [B] output: number of runs of row b.
+ * Entries past a row's count are left untouched.
+ */
+int bd_segment_cu_seqlens(const int32_t* doc_ids, int B, int S, int32_t* seg, int32_t* seg_ids,
+                          int32_t* nseg, bd_stream_t stream);
+
+/*
+ * Attention plan: per-row mask bounds, the non-empty tile ranges of every
+ * query block (forward) and key tile (backward), and both work lists sorted
+ * longest-first.  This is the "varlen metadata precompute" that the page
+ * "nemo_automodel.components.distributed.blockdiag_cp" names as an internal
+ * detail.  Built on the device from the output of bd_segment_cu_seqlens,
+ * with no host synchronisation.
+ *   seg, seg_ids, nseg  as written by bd_segment_cu_seqlens for [B, S].
+ *   Hq, Hkv             head counts (the plan's forward blocks depend on
+ *                       whether Hq / Hkv is even).
+ *   L, seq_start        query rows are global positions seq_start .. +L-1.
+ *   plan                device buffer of bd_attn_plan_size() bytes, 256-byte
+ *                       aligned; read by bd_attn_fwd / bd_attn_bwd, which must
+ *                       be given the same B, Hq, Hkv, L, S, seq_start.
+ * Returns BD_ERR_UNSUPPORTED when B * ceil(L/128) or B * ceil(S/128)
+ * exceeds 16384.
+ */
+size_t bd_attn_plan_size(int B, int Hq, int Hkv, int L, int S);
+int bd_attn_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg, int B, int Hq,
+                 int Hkv, int L, int S, int seq_start, void* plan, size_t plan_bytes,
+                 bd_stream_t stream);
+
+/*
+ * Forward pass (page "nemo_automodel.components.distributed.blockdiag_cp",
+ * cp_blockdiag_sdpa: output [B, Hq, L, D] for the local rows).
+ *   q            bf16 [B, Hq, L, D]; query i sits at global position seq_start+i.
+ *   k, v         bf16 [B, Hkv, S, D], the full key/value row.
+ *   D            64 or 128 (else BD_ERR_UNSUPPORTED).
+ *   scale        softmax scale; a value <= 0 or not finite means D^-0.5
+ *                ("None -> D**-0.5" on the page).
+ *   enable_gqa   must be non-zero when Hq != Hkv (Hq a multiple of Hkv);
+ *                query head h reads key/value head h / (Hq / Hkv).
+ *   plan         from bd_attn_plan with the same sizes.
+ *   out          bf16 [B, Hq, L, D] output.
+ *   lse          fp32 [B, Hq, L] output: natural-log log-sum-exp of the
+ *                scaled scores of each row (-inf for padding rows).
+ */
+int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L, int S,
+                int D, int seq_start, float scale, int enable_gqa, const void* plan,
+                size_t plan_bytes, void* out, float* lse, int32_t* dev_status,
+                bd_stream_t stream);
+
+/*
+ * Backward pass: gradients of sum(out * dout) (the autograd backward of the
+ * forward above).  Same arguments as bd_attn_fwd plus
+ *   out, lse     the forward's outputs for these inputs.
+ *   dout         bf16 [B, Hq, L, D].
+ *   dq           bf16 [B, Hq, L, D] output.
+ *   dk, dv       bf16 [B, Hkv, S, D] outputs, summed over the query heads of
+ *                each group; fully overwritten (rows no query attends are 0).
+ *   workspace    device scratch of bd_attn_bwd_workspace_size() bytes,
+ *                256-byte aligned (fp32 dq accumulator and per-row terms).
+ * The dq accumulation uses floating-point atomics, so dq may differ in the
+ * last bits between runs; dk and dv are deterministic.
+ */
+size_t bd_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int S, int D);
+int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                const void* dout, int B, int Hq, int Hkv, int L, int S, int D, int seq_start,
+                float scale, int enable_gqa, const void* plan, size_t plan_bytes, void* dq,
+                void* dk, void* dv, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                bd_stream_t stream);
+
+/*
+ * The backward pass in separately launchable stages (same arguments as
+ * bd_attn_bwd plus a bit mask).  Bit 1: per-row terms Delta_i = <dO_i, o_i>
+ * and lse in log2 units, and zeroing of the fp32 dq accumulator (both in
+ * `workspace`).  Bit 2: the main kernel (dk, dv written; dq accumulated into
+ * the workspace).  Bit 4: dq = bf16(scale * accumulator).  The stages must
+ * run in this order on the same workspace; bd_attn_bwd is stages = 7.  Meant
+ * for timing one stage at a time.
+ */
+int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* out,
+                       const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S,
+                       int D, int seq_start, float scale, int enable_gqa, const void* plan,
+                       size_t plan_bytes, void* dq, void* dk, void* dv, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, int stages,
+                       bd_stream_t stream);
+
+/*
+ * Copy the device status word to *host_status after the work already queued
+ * on `stream` finishes (this call synchronises `stream`; no other entry point
+ * does).  Returns BD_OK or BD_ERR_CUDA.
+ */
+int bd_get_device_status(const int32_t* dev_status, int32_t* host_status, bd_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BD_ATTN_H */

@@ -1,0 +1,188 @@
+"""ctypes binding of libbd_attn.so: the C ABI entry points under the same names.
+
+Each wrapper only marshals arguments: torch tensors become device pointers
+(``data_ptr()``), the stream defaults to torch's current CUDA stream, and a
+non-zero status becomes an exception (ValueError for argument errors,
+RuntimeError otherwise).  All computation happens in the library's kernels;
+there is no CPU fallback, and loading fails loudly when the library has not
+been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbd_attn.so")
+
+BD_OK = 0
+BD_ERR_INVALID_ARG = 1
+BD_ERR_UNSUPPORTED = 2
+BD_ERR_CUDA = 3
+BD_ERR_TIMEOUT = 4
+BD_ERR_WORKSPACE = 5
+
+_c_int, _c_size, _c_float, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p
+
+# name -> (restype, argtypes); mirrors include/bd_attn.h
+SIGNATURES = {
+    "bd_status_string": (ctypes.c_char_p, [_c_int]),
+    "bd_version": (_c_int, []),
+    "bd_doc_ids_from_cu_seqlens": (_c_int, [_vp, _vp, _c_int, _c_int, _vp, _vp, _vp]),
+    "bd_segment_cu_seqlens": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp, _vp]),
+    "bd_attn_plan_size": (_c_size, [_c_int] * 5),
+    "bd_attn_plan": (_c_int, [_vp, _vp, _vp] + [_c_int] * 6 + [_vp, _c_size, _vp]),
+    "bd_attn_fwd": (_c_int, [_vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size,
+                                                               _vp, _vp, _vp, _vp]),
+    "bd_attn_bwd_workspace_size": (_c_size, [_c_int] * 6),
+    "bd_attn_bwd": (_c_int, [_vp] * 6 + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size, _vp,
+                                                         _vp, _vp, _vp, _c_size, _vp, _vp]),
+    "bd_attn_bwd_stages": (_c_int, [_vp] * 6 + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size,
+                                                                _vp, _vp, _vp, _vp, _c_size, _vp,
+                                                                _c_int, _vp]),
+    "bd_get_device_status": (_c_int, [_vp, _vp, _vp]),
+}
+
+_lib = None
+
+
+def lib():
+    """Load (once) and return the ctypes handle of the built library."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is not built; run `python -m packed_sequence_block_gb300.build` "
+                "(the CUDA library is required: there is no CPU fallback)")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().bd_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str):
+    if code == BD_OK:
+        return
+    msg = f"{what}: {status_string(code)} (status {code})"
+    if code in (BD_ERR_INVALID_ARG, BD_ERR_UNSUPPORTED, BD_ERR_WORKSPACE):
+        raise ValueError(msg)
+    raise RuntimeError(msg)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _want(t, dtype, name):
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+# ------------------------------------------------------------------ entry points
+
+def bd_version() -> int:
+    return int(lib().bd_version())
+
+
+def bd_doc_ids_from_cu_seqlens(cu, row_ptr, B: int, S: int, doc_ids, dev_status=None,
+                               stream=None) -> None:
+    for t, n in ((cu, "cu"), (row_ptr, "row_ptr"), (doc_ids, "doc_ids")):
+        _want(t, torch.int32, n)
+    _check(lib().bd_doc_ids_from_cu_seqlens(_ptr(cu), _ptr(row_ptr), B, S, _ptr(doc_ids),
+                                            _ptr(dev_status), _stream(stream)),
+           "bd_doc_ids_from_cu_seqlens")
+
+
+def bd_segment_cu_seqlens(doc_ids, B: int, S: int, seg, seg_ids, nseg, stream=None) -> None:
+    for t, n in ((doc_ids, "doc_ids"), (seg, "seg"), (seg_ids, "seg_ids"), (nseg, "nseg")):
+        _want(t, torch.int32, n)
+    _check(lib().bd_segment_cu_seqlens(_ptr(doc_ids), B, S, _ptr(seg), _ptr(seg_ids), _ptr(nseg),
+                                       _stream(stream)), "bd_segment_cu_seqlens")
+
+
+def bd_attn_plan_size(B: int, Hq: int, Hkv: int, L: int, S: int) -> int:
+    return int(lib().bd_attn_plan_size(B, Hq, Hkv, L, S))
+
+
+def bd_attn_plan(seg, seg_ids, nseg, B: int, Hq: int, Hkv: int, L: int, S: int, seq_start: int,
+                 plan, stream=None) -> None:
+    _check(lib().bd_attn_plan(_ptr(seg), _ptr(seg_ids), _ptr(nseg), B, Hq, Hkv, L, S, seq_start,
+                              _ptr(plan), plan.numel() * plan.element_size(), _stream(stream)),
+           "bd_attn_plan")
+
+
+def bd_attn_fwd(q, k, v, B: int, Hq: int, Hkv: int, L: int, S: int, D: int, seq_start: int,
+                scale: float, enable_gqa: bool, plan, out, lse, dev_status=None,
+                stream=None) -> None:
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _want(t, torch.bfloat16, n)
+    _want(lse, torch.float32, "lse")
+    _check(lib().bd_attn_fwd(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, L, S, D, seq_start,
+                             float(scale), int(bool(enable_gqa)), _ptr(plan),
+                             plan.numel() * plan.element_size(), _ptr(out), _ptr(lse),
+                             _ptr(dev_status), _stream(stream)), "bd_attn_fwd")
+
+
+def bd_attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, L: int, S: int, D: int) -> int:
+    return int(lib().bd_attn_bwd_workspace_size(B, Hq, Hkv, L, S, D))
+
+
+def bd_attn_bwd(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: int, D: int,
+                seq_start: int, scale: float, enable_gqa: bool, plan, dq, dk, dv, workspace,
+                dev_status=None, stream=None) -> None:
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"),
+                 (dk, "dk"), (dv, "dv")):
+        _want(t, torch.bfloat16, n)
+    _want(lse, torch.float32, "lse")
+    _check(lib().bd_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), B, Hq,
+                             Hkv, L, S, D, seq_start, float(scale), int(bool(enable_gqa)),
+                             _ptr(plan), plan.numel() * plan.element_size(), _ptr(dq), _ptr(dk),
+                             _ptr(dv), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                             _stream(stream)), "bd_attn_bwd")
+
+
+def bd_attn_bwd_stages(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: int,
+                       D: int, seq_start: int, scale: float, enable_gqa: bool, plan, dq, dk, dv,
+                       workspace, dev_status=None, stages: int = 7, stream=None) -> None:
+    _check(lib().bd_attn_bwd_stages(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                    B, Hq, Hkv, L, S, D, seq_start, float(scale),
+                                    int(bool(enable_gqa)), _ptr(plan),
+                                    plan.numel() * plan.element_size(), _ptr(dq), _ptr(dk),
+                                    _ptr(dv), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(),
+                                    _ptr(dev_status), int(stages), _stream(stream)),
+           "bd_attn_bwd_stages")
+
+
+def bd_get_device_status(dev_status, stream=None) -> int:
+    """Synchronise the stream and return the device status word."""
+    host = ctypes.c_int32(0)
+    _check(lib().bd_get_device_status(_ptr(dev_status), ctypes.addressof(host), _stream(stream)),
+           "bd_get_device_status")
+    return int(host.value)

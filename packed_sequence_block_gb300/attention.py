@@ -1,0 +1,203 @@
+"""Tensor-level API over the C ABI: doc ids, segments, plan, and autograd attention.
+
+Everything here allocates torch tensors and forwards pointers to
+``libbd_attn.so`` through ``_native``; every computation runs in the
+library's CUDA kernels.
+
+Names follow the NeMo Automodel API reference pages:
+``doc_ids_from_cu_seqlens`` / ``segment_cu_seqlens`` ("nemo_automodel
+.components.models.glm5_next.cp") and ``cp_blockdiag_sdpa``
+("nemo_automodel.components.distributed.blockdiag_cp").
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _native as N
+
+_status_words: dict[int, torch.Tensor] = {}
+
+
+def device_status_word(device=None) -> torch.Tensor:
+    """The per-device int32 status word the kernels report device-side errors into."""
+    dev = torch.device(device if device is not None else "cuda")
+    idx = dev.index if dev.index is not None else torch.cuda.current_device()
+    w = _status_words.get(idx)
+    if w is None:
+        w = torch.zeros(1, dtype=torch.int32, device=torch.device("cuda", idx))
+        _status_words[idx] = w
+    return w
+
+
+def check_device_status(device=None, reset: bool = True) -> None:
+    """Synchronise and raise if a kernel reported an error since the last check."""
+    w = device_status_word(device)
+    code = N.bd_get_device_status(w)
+    if reset:
+        w.zero_()
+    if code != N.BD_OK:
+        exc = ValueError if code == N.BD_ERR_INVALID_ARG else RuntimeError
+        raise exc(f"device reported: {N.status_string(code)} (status {code})")
+
+
+def _csr(cu_seqlens, device):
+    """(flat boundaries, row_ptr) int32 device tensors from one row or a list of rows."""
+    if isinstance(cu_seqlens, (list, tuple)) and len(cu_seqlens) > 0 and (
+            isinstance(cu_seqlens[0], torch.Tensor) or hasattr(cu_seqlens[0], "__len__")):
+        rows = [torch.as_tensor(c, dtype=torch.int32).reshape(-1) for c in cu_seqlens]
+    else:
+        rows = [torch.as_tensor(cu_seqlens, dtype=torch.int32).reshape(-1)]
+    lens = torch.tensor([0] + [r.numel() for r in rows], dtype=torch.int64).cumsum(0)
+    flat = torch.cat([r.to("cpu") for r in rows]).to(device)
+    return flat, lens.to(torch.int32).to(device), len(rows)
+
+
+def doc_ids_from_cu_seqlens(cu_seqlens, seq_len: int, device=None, row_ptr=None) -> torch.Tensor:
+    """Document ids [B, S] (int32, 0 == padding) from cumulative boundaries.
+
+    ``cu_seqlens`` is one row's boundaries, a list of rows, or (with
+    ``row_ptr``) the concatenated rows as a CUDA int32 tensor.
+    """
+    if row_ptr is not None:
+        flat, rp, B = cu_seqlens, row_ptr, row_ptr.numel() - 1
+    else:
+        dev = device if device is not None else (
+            cu_seqlens.device if isinstance(cu_seqlens, torch.Tensor) and cu_seqlens.is_cuda
+            else "cuda")
+        flat, rp, B = _csr(cu_seqlens, dev)
+    ids = torch.empty((B, seq_len), dtype=torch.int32, device=flat.device)
+    N.bd_doc_ids_from_cu_seqlens(flat, rp, B, seq_len, ids, device_status_word(flat.device))
+    return ids
+
+
+def segment_cu_seqlens(doc_ids: torch.Tensor):
+    """(seg [B, S+1], seg_ids [B, S], nseg [B]) for ids [B, S] or [S]."""
+    ids = doc_ids.reshape(-1, doc_ids.shape[-1]).to(torch.int32).contiguous()
+    B, S = ids.shape
+    seg = torch.empty((B, S + 1), dtype=torch.int32, device=ids.device)
+    seg_ids = torch.empty((B, S), dtype=torch.int32, device=ids.device)
+    nseg = torch.empty((B,), dtype=torch.int32, device=ids.device)
+    N.bd_segment_cu_seqlens(ids, B, S, seg, seg_ids, nseg)
+    return seg, seg_ids, nseg
+
+
+def make_plan(seg, seg_ids, nseg, Hq: int, Hkv: int, L: int, seq_start: int = 0) -> torch.Tensor:
+    """Plan buffer (uint8, device) for attention of L local queries against S keys."""
+    B, S = seg_ids.shape
+    plan = torch.empty(N.bd_attn_plan_size(B, Hq, Hkv, L, S), dtype=torch.uint8,
+                       device=seg.device)
+    N.bd_attn_plan(seg, seg_ids, nseg, B, Hq, Hkv, L, S, seq_start, plan)
+    return plan
+
+
+def _resolve_scale(scale, D):
+    return float(D) ** -0.5 if scale is None else float(scale)
+
+
+def attn_forward(q, k, v, plan, seq_start=0, scale=None, enable_gqa=False):
+    """out [B,Hq,L,D] bf16 and lse [B,Hq,L] fp32 (no autograd)."""
+    B, Hq, L, D = q.shape
+    Hkv, S = k.shape[1], k.shape[2]
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device)
+    N.bd_attn_fwd(q, k, v, B, Hq, Hkv, L, S, D, seq_start, _resolve_scale(scale, D), enable_gqa,
+                  plan, out, lse, device_status_word(q.device))
+    return out, lse
+
+
+def attn_backward(q, k, v, out, lse, dout, plan, seq_start=0, scale=None, enable_gqa=False,
+                  workspace=None):
+    """dq, dk, dv (bf16) for the forward above (no autograd)."""
+    B, Hq, L, D = q.shape
+    Hkv, S = k.shape[1], k.shape[2]
+    if workspace is None:
+        workspace = torch.empty(N.bd_attn_bwd_workspace_size(B, Hq, Hkv, L, S, D),
+                                dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    N.bd_attn_bwd(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, seq_start,
+                  _resolve_scale(scale, D), enable_gqa, plan, dq, dk, dv, workspace,
+                  device_status_word(q.device))
+    return dq, dk, dv
+
+
+class BlockdiagAttention(torch.autograd.Function):
+    """Autograd wrapper: forward and backward both run the library's kernels."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, plan, seq_start, scale, enable_gqa):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        out, lse = attn_forward(q, k, v, plan, seq_start, scale, enable_gqa)
+        ctx.save_for_backward(q, k, v, out, lse, plan)
+        ctx.args = (seq_start, scale, enable_gqa)
+        ctx.mark_non_differentiable(lse)
+        return out, lse
+
+    @staticmethod
+    def backward(ctx, dout, _dlse):
+        q, k, v, out, lse, plan = ctx.saved_tensors
+        seq_start, scale, enable_gqa = ctx.args
+        dq, dk, dv = attn_backward(q, k, v, out, lse, dout.contiguous(), plan, seq_start, scale,
+                                   enable_gqa)
+        return dq, dk, dv, None, None, None, None
+
+
+def blockdiag_attention(q, k, v, *, cu_seqlens=None, doc_ids=None, seq_start: int = 0,
+                        scale=None, enable_gqa: bool = False, return_lse: bool = False):
+    """Block-diagonal causal attention of q [B,Hq,L,D] against k, v [B,Hkv,S,D].
+
+    The mask comes from ``doc_ids`` [B, S] (0 == padding) or, when those are
+    not given, from ``cu_seqlens`` (one row's boundaries or a list of rows).
+    """
+    S = k.shape[2]
+    if doc_ids is None:
+        if cu_seqlens is None:
+            raise ValueError("cu_seqlens or doc_ids is required")
+        doc_ids = doc_ids_from_cu_seqlens(cu_seqlens, S, device=q.device)
+    seg, seg_ids, nseg = segment_cu_seqlens(doc_ids)
+    if seg_ids.shape[0] != q.shape[0]:
+        raise ValueError("document ids must have one row per batch row")
+    plan = make_plan(seg, seg_ids, nseg, q.shape[1], k.shape[1], q.shape[2], seq_start)
+    out, lse = BlockdiagAttention.apply(q, k, v, plan, seq_start, scale, enable_gqa)
+    return (out, lse) if return_lse else out
+
+
+def cp_blockdiag_sdpa(query, key, value, attn_mask=None, dropout_p: float = 0.0,
+                      is_causal: bool = False, scale=None, enable_gqa: bool = False, *,
+                      doc_ids=None, cu_seqlens=None, seq_start: int = 0, **kwargs):
+    """SDPA-shaped entry: local queries against delivered K/V, per-document causal mask.
+
+    As on the page "nemo_automodel.components.distributed.blockdiag_cp",
+    ``attn_mask`` and ``is_causal`` are ignored (the mask is rebuilt from the
+    document ids), ``scale`` None means D**-0.5, and extra keyword arguments
+    are accepted and ignored.  Dropout is not implemented: ``dropout_p`` must be 0.
+    """
+    del attn_mask, is_causal, kwargs
+    if dropout_p != 0.0:
+        raise ValueError("dropout_p > 0 is not supported")
+    return blockdiag_attention(query, key, value, cu_seqlens=cu_seqlens, doc_ids=doc_ids,
+                               seq_start=seq_start, scale=scale, enable_gqa=enable_gqa)
+
+
+def useful_pairs(cu_rows, seq_start: int, L: int) -> int:
+    """Number of (query, key) pairs the mask allows, from host boundary lists (for FLOP counts)."""
+    total = 0
+    for cu in cu_rows:
+        cu = [int(x) for x in cu]
+        for a, b in zip(cu[:-1], cu[1:]):
+            lo, hi = max(a, seq_start), min(b, seq_start + L)
+            for_rows = 0
+            if lo < hi:
+                # rows t in [lo, hi) attend t - a + 1 keys each
+                n1, n2 = lo - a + 1, hi - a
+                for_rows = (n1 + n2) * (n2 - n1 + 1) // 2
+            total += for_rows
+    return total
+
+
+__all__ = [
+    "BlockdiagAttention", "attn_backward", "attn_forward", "blockdiag_attention",
+    "check_device_status", "cp_blockdiag_sdpa", "device_status_word", "doc_ids_from_cu_seqlens",
+    "make_plan", "segment_cu_seqlens", "useful_pairs",
+]

@@ -1,0 +1,237 @@
+// The library's C ABI (declared in include/bd_attn.h): argument checks,
+// TMA tensor maps and launches.  No call allocates, frees or synchronises
+// except bd_get_device_status, which exists to read the status word back.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "bd_internal.h"
+
+namespace bd {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int num_sms_current() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shapes shared by the attention entry points.
+int check_dims(int B, int Hq, int Hkv, int L, int S, int D, int seq_start, int enable_gqa) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || S < 1 || D < 1 || seq_start < 0)
+    return BD_ERR_INVALID_ARG;
+  if (static_cast<long long>(seq_start) + L > S) return BD_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return BD_ERR_INVALID_ARG;
+  if (Hq != Hkv && !enable_gqa) return BD_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return BD_ERR_UNSUPPORTED;
+  // TMA planes/rows and the int offsets used on the device
+  if (static_cast<long long>(B) * Hq * L * D >= (1ll << 40)) return BD_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq > (1ll << 30) || S > (1 << 30)) return BD_ERR_UNSUPPORTED;
+  return BD_OK;
+}
+
+int check_plan_lists(int B, int Hq, int Hkv, int L, int S) {
+  const PlanLayout pl = plan_layout(B, Hq, Hkv, L, S);
+  if (static_cast<long long>(B) * pl.NQB > kMaxListLen ||
+      static_cast<long long>(B) * pl.NKT > kMaxListLen)
+    return BD_ERR_UNSUPPORTED;
+  return BD_OK;
+}
+
+AttnDims resolve(int B, int Hq, int Hkv, int L, int S, int D, int seq_start, float scale) {
+  AttnDims d{B, Hq, Hkv, L, S, D, seq_start, scale, 0.f};
+  if (!(scale > 0.f) || !std::isfinite(scale)) d.scale = 1.0f / std::sqrt(static_cast<float>(D));
+  d.scale_log2 = d.scale * 1.4426950408889634f;
+  return d;
+}
+
+}  // namespace
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int planes, int rows, int D) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                           static_cast<cuuint64_t>(rows) * D * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace bd
+
+using namespace bd;
+
+extern "C" {
+
+const char* bd_status_string(int status) {
+  switch (status) {
+    case BD_OK: return "ok";
+    case BD_ERR_INVALID_ARG: return "invalid argument";
+    case BD_ERR_UNSUPPORTED: return "unsupported configuration";
+    case BD_ERR_CUDA: return "CUDA error";
+    case BD_ERR_TIMEOUT: return "device wait timed out";
+    case BD_ERR_WORKSPACE: return "plan or workspace buffer too small";
+    default: return "unknown status";
+  }
+}
+
+int bd_version(void) { return 100; }
+
+int bd_doc_ids_from_cu_seqlens(const int32_t* cu, const int32_t* row_ptr, int B, int S,
+                               int32_t* doc_ids, int32_t* dev_status, bd_stream_t stream) {
+  if (cu == nullptr || row_ptr == nullptr || doc_ids == nullptr || B < 1 || S < 1)
+    return BD_ERR_INVALID_ARG;
+  if (B > 65535) return BD_ERR_UNSUPPORTED;
+  return launch_doc_ids(cu, row_ptr, B, S, doc_ids, dev_status, stream) == cudaSuccess
+             ? BD_OK
+             : BD_ERR_CUDA;
+}
+
+int bd_segment_cu_seqlens(const int32_t* doc_ids, int B, int S, int32_t* seg, int32_t* seg_ids,
+                          int32_t* nseg, bd_stream_t stream) {
+  if (doc_ids == nullptr || seg == nullptr || seg_ids == nullptr || nseg == nullptr || B < 1 ||
+      S < 1)
+    return BD_ERR_INVALID_ARG;
+  if (S >= (1 << 30)) return BD_ERR_UNSUPPORTED;
+  return launch_segments(doc_ids, B, S, seg, seg_ids, nseg, stream) == cudaSuccess ? BD_OK
+                                                                                  : BD_ERR_CUDA;
+}
+
+size_t bd_attn_plan_size(int B, int Hq, int Hkv, int L, int S) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || S < 1) return 0;
+  return plan_layout(B, Hq, Hkv, L, S).total;
+}
+
+int bd_attn_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg, int B, int Hq,
+                 int Hkv, int L, int S, int seq_start, void* plan, size_t plan_bytes,
+                 bd_stream_t stream) {
+  if (seg == nullptr || seg_ids == nullptr || nseg == nullptr || plan == nullptr)
+    return BD_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || S < 1 || seq_start < 0 ||
+      static_cast<long long>(seq_start) + L > S || Hq % Hkv != 0)
+    return BD_ERR_INVALID_ARG;
+  if (!aligned(plan, 256)) return BD_ERR_INVALID_ARG;
+  if (S >= (1 << 30) || B > 65535) return BD_ERR_UNSUPPORTED;
+  int st = check_plan_lists(B, Hq, Hkv, L, S);
+  if (st != BD_OK) return st;
+  if (plan_bytes < plan_layout(B, Hq, Hkv, L, S).total) return BD_ERR_WORKSPACE;
+  return launch_plan(seg, seg_ids, nseg, B, Hq, Hkv, L, S, seq_start, plan, stream) == cudaSuccess
+             ? BD_OK
+             : BD_ERR_CUDA;
+}
+
+int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L, int S,
+                int D, int seq_start, float scale, int enable_gqa, const void* plan,
+                size_t plan_bytes, void* out, float* lse, int32_t* dev_status,
+                bd_stream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || plan == nullptr || out == nullptr ||
+      lse == nullptr)
+    return BD_ERR_INVALID_ARG;
+  int st = check_dims(B, Hq, Hkv, L, S, D, seq_start, enable_gqa);
+  if (st != BD_OK) return st;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(plan, 256))
+    return BD_ERR_INVALID_ARG;
+  st = check_plan_lists(B, Hq, Hkv, L, S);
+  if (st != BD_OK) return st;
+  if (plan_bytes < plan_layout(B, Hq, Hkv, L, S).total) return BD_ERR_WORKSPACE;
+  const AttnDims d = resolve(B, Hq, Hkv, L, S, D, seq_start, scale);
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_bf16(&tq, q, B * Hq, L, D) || !make_tmap_bf16(&tk, k, B * Hkv, S, D) ||
+      !make_tmap_bf16(&tv, v, B * Hkv, S, D))
+    return BD_ERR_CUDA;
+  const int sms = num_sms_current();
+  if (sms <= 0) return BD_ERR_CUDA;
+  return launch_fwd(tq, tk, tv, d, plan, out, lse, dev_status, sms, stream) == cudaSuccess
+             ? BD_OK
+             : BD_ERR_CUDA;
+}
+
+size_t bd_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int S, int D) {
+  (void)Hkv;
+  (void)S;
+  if (B < 1 || Hq < 1 || L < 1 || D < 1) return 0;
+  return bwd_layout(B, Hq, L, D).total;
+}
+
+int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* out,
+                       const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S,
+                       int D, int seq_start, float scale, int enable_gqa, const void* plan,
+                       size_t plan_bytes, void* dq, void* dk, void* dv, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, int stages,
+                       bd_stream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || lse == nullptr ||
+      dout == nullptr || plan == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
+      workspace == nullptr)
+    return BD_ERR_INVALID_ARG;
+  if (stages <= 0 || stages > (kBwdPrepare | kBwdMain | kBwdFinish)) return BD_ERR_INVALID_ARG;
+  int st = check_dims(B, Hq, Hkv, L, S, D, seq_start, enable_gqa);
+  if (st != BD_OK) return st;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(plan, 256) || !aligned(workspace, 256))
+    return BD_ERR_INVALID_ARG;
+  st = check_plan_lists(B, Hq, Hkv, L, S);
+  if (st != BD_OK) return st;
+  if (plan_bytes < plan_layout(B, Hq, Hkv, L, S).total) return BD_ERR_WORKSPACE;
+  if (workspace_bytes < bwd_layout(B, Hq, L, D).total) return BD_ERR_WORKSPACE;
+  const AttnDims d = resolve(B, Hq, Hkv, L, S, D, seq_start, scale);
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tmap_bf16(&tq, q, B * Hq, L, D) || !make_tmap_bf16(&tk, k, B * Hkv, S, D) ||
+      !make_tmap_bf16(&tv, v, B * Hkv, S, D) || !make_tmap_bf16(&tdo, dout, B * Hq, L, D))
+    return BD_ERR_CUDA;
+  const int sms = num_sms_current();
+  if (sms <= 0) return BD_ERR_CUDA;
+  return launch_bwd(tq, tk, tv, tdo, d, plan, out, lse, dout, dq, dk, dv, workspace, dev_status,
+                    stages, sms, stream) == cudaSuccess
+             ? BD_OK
+             : BD_ERR_CUDA;
+}
+
+int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                const void* dout, int B, int Hq, int Hkv, int L, int S, int D, int seq_start,
+                float scale, int enable_gqa, const void* plan, size_t plan_bytes, void* dq,
+                void* dk, void* dv, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                bd_stream_t stream) {
+  return bd_attn_bwd_stages(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
+                            enable_gqa, plan, plan_bytes, dq, dk, dv, workspace, workspace_bytes,
+                            dev_status, kBwdPrepare | kBwdMain | kBwdFinish, stream);
+}
+
+int bd_get_device_status(const int32_t* dev_status, int32_t* host_status, bd_stream_t stream) {
+  if (dev_status == nullptr || host_status == nullptr) return BD_ERR_INVALID_ARG;
+  if (cudaMemcpyAsync(host_status, dev_status, sizeof(int32_t), cudaMemcpyDeviceToHost, stream) !=
+      cudaSuccess)
+    return BD_ERR_CUDA;
+  return cudaStreamSynchronize(stream) == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,583 @@
+// Backward pass of block-diagonal causal attention: gradients of
+// sum(out * dout) for cp_blockdiag_sdpa (page
+// "nemo_automodel.components.distributed.blockdiag_cp"), written from the
+// softmax derivative: Delta_i = <dO_i, o_i>, P = exp(S - lse),
+// dS = P * (dP - Delta), dq = scale dS K, dk = scale dS^T Q, dv = P^T dO.
+//
+// Kernels:
+//  bwd_pre    Delta per row, lse in log2 units, zero the fp32 dq accumulator
+//  bd_bwd     persistent; one work unit = one 128-key tile of one K/V head,
+//             looping over the G query heads of the group and the query tiles
+//             the plan marks non-empty.  Per iteration (tcgen05, TMEM):
+//               S^T = K Q^T, dP^T = V dO^T          (cols 256, 384)
+//               P^T, dS^T -> bf16 into TMEM; dS -> smem
+//               dV += P^T dO, dK += dS^T Q          (cols 128, 0)
+//               dQ = dS K                           (cols 256, after dV)
+//             warpgroup 2 reads dQ out of TMEM and adds it into the fp32
+//             accumulator with vector reductions; dK, dV leave once per unit.
+//  bwd_dq     dq = bf16(scale * accumulator)
+#include "bd_ptx.cuh"
+
+namespace bd {
+
+namespace {
+
+constexpr int kThreads = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int TILE = 128 * D * 2;  // bytes of a 128-row bf16 tile
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = TILE;
+  static constexpr int OFF_Q = 2 * TILE;              // [2 stages]
+  static constexpr int OFF_DO = OFF_Q + 2 * TILE;     // [2 stages]
+  static constexpr int OFF_DS = OFF_DO + 2 * TILE;    // 128 keys x 128 queries bf16
+  static constexpr int OFF_LSED = OFF_DS + 32768;     // [2 stages] 128 x float2
+  static constexpr int OFF_BAR = OFF_LSED + 2048;
+  static constexpr int SMEM = OFF_BAR + 256;
+  static constexpr uint32_t IDESC_S = make_idesc_bf16(128, 128, 0, 0);   // S^T, dP^T
+  static constexpr uint32_t IDESC_KV = make_idesc_bf16(128, D, 0, 1);    // dV, dK (A in TMEM)
+  static constexpr uint32_t IDESC_DQ = make_idesc_bf16(128, D, 1, 1);    // dQ = dS K
+};
+
+struct BwdParams {
+  int B, Hq, Hkv, L, S, seq_start, G, NKT, Spad, Lq, n_units;
+  float scale_log2, scale;
+  const int32_t* kend;
+  const int32_t* bwd_range;
+  const int32_t* bwd_order;
+  const float2* lsed;
+  float* dqacc;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int32_t* status;
+};
+
+struct BUnit {
+  int b, g, kt, qt_lo, nq, n_it;
+};
+
+__device__ __forceinline__ BUnit decode_bunit(const BwdParams& p, int w) {
+  BUnit u;
+  const int e = w / p.Hkv;
+  u.g = w % p.Hkv;
+  const int ktl = p.bwd_order[e];
+  u.b = ktl / p.NKT;
+  u.kt = ktl % p.NKT;
+  u.qt_lo = p.bwd_range[2 * ktl];
+  u.nq = p.bwd_range[2 * ktl + 1] - u.qt_lo + 1;
+  u.n_it = u.nq > 0 ? u.nq * p.G : 0;
+  return u;
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      set_status(status, BD_ERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ preprocess
+
+// One thread per 8 elements of a row; rows [0, Lq) of every (b, h) plane.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
+                                                      const __nv_bfloat16* __restrict__ dout,
+                                                      const float* __restrict__ lse, int planes,
+                                                      int L, int Lq, float2* __restrict__ lsed,
+                                                      float* __restrict__ dqacc) {
+  constexpr int TPR = D / 8;  // threads per row (a power of two dividing 32)
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long rowg = tid / TPR;
+  const int part = static_cast<int>(tid % TPR);
+  const bool active = rowg < (long long)planes * Lq;
+  const int plane = active ? static_cast<int>(rowg / Lq) : 0;
+  const int i = active ? static_cast<int>(rowg % Lq) : 0;
+  float acc = 0.f;
+  if (active && i < L) {
+    const size_t off = ((size_t)plane * L + i) * D + part * 8;
+    const uint4 o4 = *reinterpret_cast<const uint4*>(out + off);
+    const uint4 d4 = *reinterpret_cast<const uint4*>(dout + off);
+    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o4);
+    const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&d4);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 a = __bfloat1622float2(o2[j]);
+      const float2 b = __bfloat1622float2(d2[j]);
+      acc = fmaf(a.x, b.x, acc);
+      acc = fmaf(a.y, b.y, acc);
+    }
+    float4* z = reinterpret_cast<float4*>(dqacc + off);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // every lane of the warp takes part in the shuffles (inactive lanes add 0)
+#pragma unroll
+  for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, TPR);
+  if (active && part == 0) {
+    float l2 = INFINITY, dl = 0.f;
+    if (i < L) {
+      const float x = lse[(size_t)plane * L + i];
+      if (x != -INFINITY) {
+        l2 = x * kLog2e;
+        dl = acc;
+      }
+    }
+    lsed[(size_t)plane * Lq + i] = make_float2(l2, dl);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ dqacc,
+                                                     __nv_bfloat16* __restrict__ dq,
+                                                     long long n8, float scale) {
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= n8) return;
+  const float4* src = reinterpret_cast<const float4*>(dqacc) + 2 * t;
+  const float4 a = src[0], b = src[1];
+  uint4 o;
+  o.x = pack_bf16x2(a.x * scale, a.y * scale);
+  o.y = pack_bf16x2(a.z * scale, a.w * scale);
+  o.z = pack_bf16x2(b.x * scale, b.y * scale);
+  o.w = pack_bf16x2(b.z * scale, b.w * scale);
+  reinterpret_cast<uint4*>(dq)[t] = o;
+}
+
+// ------------------------------------------------------------------ main kernel
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bd_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                  const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v,
+                  const __grid_constant__ CUtensorMap tmap_do, const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* kv_empty = bars + 1;
+  uint64_t* st_full = bars + 2;   // [2]
+  uint64_t* st_empty = bars + 4;  // [2]
+  uint64_t* s_full = bars + 6;
+  uint64_t* pds_full = bars + 7;
+  uint64_t* dq_full = bars + 8;
+  uint64_t* dq_empty = bars + 9;
+  uint64_t* dkdv_full = bars + 10;
+  uint64_t* drain = bars + 11;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    if ((smem_u32(smem) & 1023u) != 0) {
+      set_status(p.status, BD_ERR_CUDA);
+      *abort_flag = 1;
+    }
+    mbar_init(kv_full, 1);
+    mbar_init(kv_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(st_full + s, 1);
+      mbar_init(st_empty + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(pds_full, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 128);
+    mbar_init(dkdv_full, 1);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tmap_q);
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_v);
+    prefetch_tmap(&tmap_do);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool aborted_at_start = *abort_flag != 0;
+
+  if (warp == 0 && !aborted_at_start) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t kv_u = 0, st_it = 0;
+      for (int w = blockIdx.x; w < p.n_units; w += gridDim.x) {
+        const BUnit u = decode_bunit(p, w);
+        if (u.n_it <= 0) continue;
+        if (!mbar_wait(kv_empty, (kv_u & 1) ^ 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
+        const int kvplane = u.b * p.Hkv + u.g;
+        for (int j = 0; j < D / 64; ++j) {
+          tma_load_3d(smem + C::OFF_K + j * 16384, &tmap_k, kv_full, 64 * j, u.kt * kBN, kvplane);
+          tma_load_3d(smem + C::OFF_V + j * 16384, &tmap_v, kv_full, 64 * j, u.kt * kBN, kvplane);
+        }
+        ++kv_u;
+        bool ok = true;
+        for (int i = 0; i < u.n_it; ++i) {
+          const int h = u.g * p.G + i / u.nq;
+          const int qt = u.qt_lo + i % u.nq;
+          const int st = st_it & 1;
+          ok = mbar_wait(st_empty + st, ((st_it >> 1) & 1) ^ 1, abort_flag, p.status);
+          if (!ok) break;
+          mbar_arrive_expect_tx(st_full + st, 2 * C::TILE + 1024);
+          const int qplane = u.b * p.Hq + h;
+          for (int j = 0; j < D / 64; ++j) {
+            tma_load_3d(smem + C::OFF_Q + st * C::TILE + j * 16384, &tmap_q, st_full + st, 64 * j,
+                        qt * kBM, qplane);
+            tma_load_3d(smem + C::OFF_DO + st * C::TILE + j * 16384, &tmap_do, st_full + st,
+                        64 * j, qt * kBM, qplane);
+          }
+          bulk_load(smem + C::OFF_LSED + st * 1024, p.lsed + (size_t)qplane * p.Lq + qt * kBM,
+                    1024, st_full + st);
+          ++st_it;
+        }
+        if (!ok) break;
+      }
+      if (kv_u > 0) drain_wait(kv_full, (kv_u - 1) & 1, p.status);
+      for (int st = 0; st < 2; ++st) {
+        if (st_it > static_cast<uint32_t>(st)) {
+          const uint32_t last = st_it - 1 - ((st_it - 1 - st) & 1);
+          drain_wait(st_full + st, (last >> 1) & 1, p.status);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1 && !aborted_at_start) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sk = smem_u32(smem + C::OFF_K);
+      const uint32_t sv = smem_u32(smem + C::OFF_V);
+      const uint32_t sq0 = smem_u32(smem + C::OFF_Q);
+      const uint32_t sdo0 = smem_u32(smem + C::OFF_DO);
+      const uint32_t sds = smem_u32(smem + C::OFF_DS);
+      const uint32_t tDK = tmem, tDV = tmem + 128, tS = tmem + 256, tDP = tmem + 384;
+      // A (K-major, M=128 keys) x B (K-major, N=128 queries), K-dim = D
+      auto issue_kmajor = [&](uint32_t d, uint32_t a, uint32_t b) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(d, make_sdesc_sw128(a + off, 16, 1024), make_sdesc_sw128(b + off, 16, 1024),
+                 C::IDESC_S, kk > 0);
+        }
+      };
+      // D[keys, D] (+)= A[tmem, keys x 128 q] * B[q, D] (MN-major smem)
+      auto issue_ts = [&](uint32_t d, uint32_t a_tmem, uint32_t b, bool acc) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ts(d, a_tmem + ks * 8, make_sdesc_sw128(b + ks * 2048, 16384, 1024), C::IDESC_KV,
+                 (acc || ks > 0));
+      };
+      // dQ[q, D] = dS[q, keys] (MN-major smem) * K[keys, D] (MN-major smem)
+      auto issue_dq = [&]() {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ss(tS, make_sdesc_sw128(sds + ks * 2048, 16384, 1024),
+                 make_sdesc_sw128(sk + ks * 2048, 16384, 1024), C::IDESC_DQ, ks > 0);
+      };
+      uint32_t kv_u = 0, st_it = 0, it_g = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < p.n_units && ok; w += gridDim.x) {
+        const BUnit u = decode_bunit(p, w);
+        if (u.n_it <= 0) continue;
+        ok = mbar_wait(kv_full, kv_u & 1, abort_flag, p.status);
+        if (!ok) break;
+        int st = st_it & 1;
+        ok = mbar_wait(st_full + st, (st_it >> 1) & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        issue_kmajor(tDP, sv, sdo0 + st * C::TILE);
+        if (it_g > 0) {
+          ok = mbar_wait(dq_empty, (it_g - 1) & 1, abort_flag, p.status);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        issue_kmajor(tS, sk, sq0 + st * C::TILE);
+        mma_commit(s_full);
+        for (int i = 0; i < u.n_it && ok; ++i) {
+          const uint32_t si = st_it + i;
+          st = si & 1;
+          ok = mbar_wait(pds_full, it_g & 1, abort_flag, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_ts(tDV, tS, sdo0 + st * C::TILE, i > 0);
+          issue_ts(tDK, tDP, sq0 + st * C::TILE, i > 0);
+          mma_commit(st_empty + st);
+          issue_dq();
+          mma_commit(dq_full);
+          if (i + 1 < u.n_it) {
+            const int sn = (si + 1) & 1;
+            ok = mbar_wait(st_full + sn, ((si + 1) >> 1) & 1, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_kmajor(tDP, sv, sdo0 + sn * C::TILE);
+            ok = mbar_wait(dq_empty, it_g & 1, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_kmajor(tS, sk, sq0 + sn * C::TILE);
+            mma_commit(s_full);
+          }
+          ++it_g;
+        }
+        st_it += u.n_it;
+        mma_commit(kv_empty);
+        mma_commit(dkdv_full);
+        ++kv_u;
+      }
+      mma_commit(drain);
+      drain_wait(drain, 0, p.status);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 8 && !aborted_at_start) {
+    // ------------------------------------------------------------ P / dS warpgroup
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;  // key row of the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t tS = tmem + lane_off + 256, tDP = tmem + lane_off + 384;
+    const uint32_t sds_row = smem_u32(smem + C::OFF_DS) + (r >> 3) * 1024 + (r & 7) * 128;
+    uint32_t st_it = 0, it_g = 0, kv_u = 0;
+    for (int w = blockIdx.x; w < p.n_units; w += gridDim.x) {
+      const BUnit u = decode_bunit(p, w);
+      const int key = u.kt * kBN + r;
+      const size_t krow = ((size_t)(u.b * p.Hkv + u.g) * p.S + key) * D;
+      if (u.n_it <= 0) {
+        if (key < p.S) {
+          uint4* a = reinterpret_cast<uint4*>(p.dk + krow);
+          uint4* b = reinterpret_cast<uint4*>(p.dv + krow);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) {
+            a[c] = make_uint4(0, 0, 0, 0);
+            b[c] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        continue;
+      }
+      const int kend = p.kend[(size_t)u.b * p.Spad + key];
+      bool ok = true;
+      for (int i = 0; i < u.n_it; ++i) {
+        const int qt = u.qt_lo + i % u.nq;
+        const int st = st_it & 1;
+        ok = mbar_wait_warp(s_full, it_g & 1, abort_flag, p.status);
+        if (!ok) break;
+        ok = mbar_wait_warp(st_full + st, (st_it >> 1) & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        // columns c (query q0 + c) attending this key: key <= q0 + c < min(kend, end of interval)
+        const int q0 = p.seq_start + qt * kBM;
+        int ca = 1, cb = 0;
+        if (kend > key) {
+          ca = key - q0;
+          cb = min(kend, p.seq_start + p.L) - q0 - 1;
+        }
+        const bool full = __all_sync(0xffffffffu, ca <= 0 && cb >= kBM - 1);
+        const float2* ld = reinterpret_cast<const float2*>(smem + C::OFF_LSED + st * 1024);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sv[32], dv[32];
+          tmem_ld32x2(tS + c * 32, tDP + c * 32, sv, dv);
+          float pr[32], ds[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float2 x = ld[c * 32 + e];
+            float pe = fast_exp2(fmaf(__uint_as_float(sv[e]), p.scale_log2, -x.x));
+            if (!full) {
+              const int col = c * 32 + e;
+              pe = (col >= ca && col <= cb) ? pe : 0.f;
+            }
+            pr[e] = pe;
+            ds[e] = pe * (__uint_as_float(dv[e]) - x.y);
+          }
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            pk[e] = pack_bf16x2(pr[2 * e], pr[2 * e + 1]);
+            dk[e] = pack_bf16x2(ds[2 * e], ds[2 * e + 1]);
+          }
+          tmem_st16(tS + c * 16, pk);
+          tmem_st16(tDP + c * 16, dk);
+          // dS (queries contiguous) into the MN-major, 128-byte-swizzled A tile of dQ = dS K
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq) {
+            const int cq = c * 4 + gq;  // 16-byte chunk index along the queries
+            const uint32_t addr = sds_row + (cq >> 3) * 16384 + (((cq & 7) ^ (r & 7)) << 4);
+            st_shared_v4(addr, dk[4 * gq], dk[4 * gq + 1], dk[4 * gq + 2], dk[4 * gq + 3]);
+          }
+        }
+        tmem_wait_st();
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(pds_full);
+        ++st_it;
+        ++it_g;
+      }
+      if (!ok) break;
+      // epilogue: dK (scaled) and dV of this key tile
+      ok = mbar_wait_warp(dkdv_full, kv_u & 1, abort_flag, p.status);
+      if (!ok) break;
+      ++kv_u;
+      tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t tsrc = tmem + lane_off + half * 128;
+        __nv_bfloat16* dst = (half == 0 ? p.dk : p.dv) + krow;
+        const float mul = half == 0 ? p.scale : 1.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tsrc + c * 32, v);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul,
+                                __uint_as_float(v[2 * e + 1]) * mul);
+          if (key < p.S) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+            d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            d4[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+            d4[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+          }
+        }
+      }
+      tc_fence_before();
+    }
+  } else if (warp >= 8 && !aborted_at_start) {
+    // ------------------------------------------------------------ dQ warpgroup
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;  // query row of the tile = TMEM lane
+    const uint32_t tQ = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + 256;
+    uint32_t it_g = 0;
+    for (int w = blockIdx.x; w < p.n_units; w += gridDim.x) {
+      const BUnit u = decode_bunit(p, w);
+      bool ok = true;
+      for (int i = 0; i < u.n_it; ++i) {
+        const int h = u.g * p.G + i / u.nq;
+        const int row = (u.qt_lo + i % u.nq) * kBM + r;
+        ok = mbar_wait_warp(dq_full, it_g & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t v[D];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t t[32];
+          tmem_ld32(tQ + c * 32, t);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[c * 32 + e] = t[e];
+        }
+        tc_fence_before();
+        mbar_arrive(dq_empty);  // TMEM columns free again; the adds below run from registers
+        ++it_g;
+        if (row < p.L) {
+          float* dst = p.dqacc + ((size_t)(u.b * p.Hq + h) * p.L + row) * D;
+#pragma unroll
+          for (int j = 0; j < D / 4; ++j)
+            red_add_v4(dst + 4 * j, __uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                       __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        }
+      }
+      if (!ok) break;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const CUtensorMap& tdo,
+                                const BwdParams& p, const void* out, const float* lse,
+                                const void* dout, void* dq, int stages, int num_sms,
+                                cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(bd_bwd_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int planes = p.B * p.Hq;
+  if (stages & kBwdPrepare) {
+    const long long threads = (long long)planes * p.Lq * (D / 8);
+    bwd_pre_kernel<D><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse,
+        planes, p.L, p.Lq, const_cast<float2*>(p.lsed), p.dqacc);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int grid = p.n_units < num_sms ? p.n_units : num_sms;
+  if ((stages & kBwdMain) && grid > 0) {
+    bd_bwd_kernel<D><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (stages & kBwdFinish) {
+    const long long n8 = (long long)planes * p.L * D / 8;
+    bwd_dq_kernel<D><<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
+        p.dqacc, static_cast<__nv_bfloat16*>(dq), n8, p.scale);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const AttnDims& d, const void* plan,
+                       const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                       void* dv, void* workspace, int32_t* status, int stages, int num_sms,
+                       cudaStream_t stream) {
+  const PlanLayout pl = plan_layout(d.B, d.Hq, d.Hkv, d.L, d.S);
+  const BwdLayout wl = bwd_layout(d.B, d.Hq, d.L, d.D);
+  const char* base = static_cast<const char*>(plan);
+  char* ws = static_cast<char*>(workspace);
+  BwdParams p{};
+  p.B = d.B;
+  p.Hq = d.Hq;
+  p.Hkv = d.Hkv;
+  p.L = d.L;
+  p.S = d.S;
+  p.seq_start = d.seq_start;
+  p.G = d.Hq / d.Hkv;
+  p.NKT = pl.NKT;
+  p.Spad = pl.Spad;
+  p.Lq = wl.Lq;
+  p.n_units = d.B * pl.NKT * d.Hkv;
+  p.scale_log2 = d.scale_log2;
+  p.scale = d.scale;
+  p.kend = reinterpret_cast<const int32_t*>(base + pl.kend);
+  p.bwd_range = reinterpret_cast<const int32_t*>(base + pl.bwd_range);
+  p.bwd_order = reinterpret_cast<const int32_t*>(base + pl.bwd_order);
+  p.lsed = reinterpret_cast<const float2*>(ws + wl.lsed);
+  p.dqacc = reinterpret_cast<float*>(ws + wl.dqacc);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.status = status;
+  if (d.D == 64) return launch_bwd_t<64>(tq, tk, tv, tdo, p, out, lse, dout, dq, stages, num_sms,
+                                          stream);
+  return launch_bwd_t<128>(tq, tk, tv, tdo, p, out, lse, dout, dq, stages, num_sms, stream);
+}
+
+}  // namespace bd

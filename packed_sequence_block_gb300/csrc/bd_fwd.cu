@@ -1,0 +1,483 @@
+// Forward pass of block-diagonal causal attention (cp_blockdiag_sdpa on the
+// page "nemo_automodel.components.distributed.blockdiag_cp": local queries
+// against the full key/value row under a per-document causal mask).
+//
+// Design (sm_103a):
+//  * persistent CTAs (one per SM) walk a longest-first list of work units;
+//    a unit is one query block = two 128-row sub-tiles that share every
+//    key/value tile: two query heads of one GQA group (Hq/Hkv even) or two
+//    consecutive row tiles of one head (Hq/Hkv odd);
+//  * warp 0 streams Q and K/V tiles with TMA (128-byte swizzle) into shared
+//    memory; only the key tiles the plan marks non-empty are loaded;
+//  * warp 1 (one thread) issues tcgen05 MMAs: S_s = Q_s K^T into TMEM, then
+//    O_s += P_s V with P_s read back from TMEM;
+//  * warpgroups 1 and 2 run the softmax of sub-tile 0 and 1 (one thread per
+//    query row = one TMEM lane): mask, running max, exp2, bf16 P into TMEM,
+//    lazy rescaling of O, and the epilogue O / l -> bf16 plus the fp32 LSE.
+// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
+#include "bd_ptx.cuh"
+
+namespace bd {
+
+namespace {
+
+constexpr int kThreads = 384;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int QTILE = kBM * D * 2;  // bytes of one 128-row bf16 tile
+  static constexpr int KTILE = kBN * D * 2;
+  static constexpr int STAGES = (D == 64) ? 3 : 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * QTILE;
+  static constexpr int OFF_V = OFF_K + STAGES * KTILE;
+  static constexpr int OFF_BAR = OFF_V + STAGES * KTILE;
+  static constexpr int SMEM = OFF_BAR + 512;
+  static constexpr uint32_t IDESC_S = make_idesc_bf16(128, 128, 0, 0);
+  static constexpr uint32_t IDESC_PV = make_idesc_bf16(128, D, 0, 1);
+};
+
+struct FwdParams {
+  int B, Hq, Hkv, L, S, seq_start, G, HP, NQB, Lpad, n_units, g_odd;
+  float scale_log2;
+  const int32_t* qlo;
+  const int32_t* fwd_range;
+  const int32_t* fwd_order;
+  __nv_bfloat16* out;
+  float* lse;
+  int32_t* status;
+};
+
+struct Unit {
+  int b, h0, h1, qt0, qt1, kt_lo, n, g;
+};
+
+__device__ __forceinline__ Unit decode_unit(const FwdParams& p, int w) {
+  const int per = p.Hkv * p.HP;
+  const int e = w / per, r = w % per;
+  const int qbl = p.fwd_order[e];
+  Unit u;
+  u.b = qbl / p.NQB;
+  const int qb = qbl % p.NQB;
+  u.g = r / p.HP;
+  const int slot = r % p.HP;
+  if (!p.g_odd) {
+    u.h0 = u.g * p.G + 2 * slot;
+    u.h1 = u.h0 + 1;
+    u.qt0 = u.qt1 = qb;
+  } else {
+    u.h0 = u.h1 = u.g * p.G + slot;
+    u.qt0 = 2 * qb;
+    u.qt1 = 2 * qb + 1;
+  }
+  u.kt_lo = p.fwd_range[2 * qbl];
+  u.n = p.fwd_range[2 * qbl + 1] - u.kt_lo + 1;
+  return u;
+}
+
+// Bounded wait used at teardown for copies/MMAs already in flight: ignores
+// the abort flag (the operation completes on its own) but never spins forever.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      set_status(status, BD_ERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bd_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                  const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;                      // [STAGES]
+  uint64_t* k_empty = k_full + C::STAGES;           // [STAGES]
+  uint64_t* v_full = k_empty + C::STAGES;           // [STAGES]
+  uint64_t* v_empty = v_full + C::STAGES;           // [STAGES]
+  uint64_t* s_full = v_empty + C::STAGES;           // [2]
+  uint64_t* p_full = s_full + 2;                    // [2]
+  uint64_t* o_full = p_full + 2;                    // [2]
+  uint64_t* drain = o_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    if ((smem_u32(smem) & 1023u) != 0) {  // swizzled tiles need 1024-byte alignment
+      set_status(p.status, BD_ERR_CUDA);
+      *abort_flag = 1;
+    }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(k_full + s, 1);
+      mbar_init(k_empty + s, 1);
+      mbar_init(v_full + s, 1);
+      mbar_init(v_empty + s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(s_full + s, 1);
+      mbar_init(p_full + s, 128);
+      mbar_init(o_full + s, 1);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tmap_q);
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool aborted_at_start = *abort_flag != 0;
+
+  if (warp == 0 && !aborted_at_start) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t k_it = 0, v_it = 0, u_it = 0;
+      bool q_issued = false;
+      for (int w = blockIdx.x; w < p.n_units; w += gridDim.x) {
+        const Unit u = decode_unit(p, w);
+        if (u.n <= 0) continue;
+        if (!mbar_wait(q_empty, (u_it & 1) ^ 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(q_full, 2 * C::QTILE);
+        q_issued = true;
+        for (int j = 0; j < D / 64; ++j) {
+          tma_load_3d(smem + C::OFF_Q + j * 16384, &tmap_q, q_full, 64 * j, u.qt0 * kBM,
+                      u.b * p.Hq + u.h0);
+          tma_load_3d(smem + C::OFF_Q + C::QTILE + j * 16384, &tmap_q, q_full, 64 * j,
+                      u.qt1 * kBM, u.b * p.Hq + u.h1);
+        }
+        ++u_it;
+        const int plane = u.b * p.Hkv + u.g;
+        bool ok = true;
+        for (int jj = 0; jj < u.n; ++jj) {
+          const int row = (u.kt_lo + jj) * kBN;
+          const int st = k_it % C::STAGES;
+          ok = mbar_wait(k_empty + st, ((k_it / C::STAGES) & 1) ^ 1, abort_flag, p.status);
+          if (!ok) break;
+          mbar_arrive_expect_tx(k_full + st, C::KTILE);
+          for (int j = 0; j < D / 64; ++j)
+            tma_load_3d(smem + C::OFF_K + st * C::KTILE + j * 16384, &tmap_k, k_full + st, 64 * j,
+                        row, plane);
+          ++k_it;
+          ok = mbar_wait(v_empty + st, ((v_it / C::STAGES) & 1) ^ 1, abort_flag, p.status);
+          if (!ok) break;
+          mbar_arrive_expect_tx(v_full + st, C::KTILE);
+          for (int j = 0; j < D / 64; ++j)
+            tma_load_3d(smem + C::OFF_V + st * C::KTILE + j * 16384, &tmap_v, v_full + st, 64 * j,
+                        row, plane);
+          ++v_it;
+        }
+        if (!ok) break;
+      }
+      // teardown: every issued copy must land before the CTA's memory is released
+      if (q_issued) drain_wait(q_full, (u_it - 1) & 1, p.status);
+      for (int st = 0; st < C::STAGES; ++st) {
+        if (k_it > static_cast<uint32_t>(st)) {
+          const uint32_t last = k_it - 1 - ((k_it - 1 - st) % C::STAGES);
+          drain_wait(k_full + st, (last / C::STAGES) & 1, p.status);
+        }
+        if (v_it > static_cast<uint32_t>(st)) {
+          const uint32_t last = v_it - 1 - ((v_it - 1 - st) % C::STAGES);
+          drain_wait(v_full + st, (last / C::STAGES) & 1, p.status);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1 && !aborted_at_start) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sq0 = smem_u32(smem + C::OFF_Q);
+      const uint32_t sk0 = smem_u32(smem + C::OFF_K);
+      const uint32_t sv0 = smem_u32(smem + C::OFF_V);
+      auto issue_s = [&](int s, int st) {
+        const uint32_t qa = sq0 + s * C::QTILE, ka = sk0 + st * C::KTILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + s * 128, make_sdesc_sw128(qa + off, 16, 1024),
+                 make_sdesc_sw128(ka + off, 16, 1024), C::IDESC_S, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int s, int st, bool acc) {
+        const uint32_t va = sv0 + st * C::KTILE;
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          mma_ts(tmem + 256 + s * 128, tmem + s * 128 + ks * 8,
+                 make_sdesc_sw128(va + ks * 2048, 16384, 1024), C::IDESC_PV, (acc || ks > 0));
+        }
+      };
+      uint32_t kv_it = 0, u_it = 0, t_it = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < p.n_units && ok; w += gridDim.x) {
+        const Unit u = decode_unit(p, w);
+        if (u.n <= 0) continue;
+        ok = mbar_wait(q_full, u_it & 1, abort_flag, p.status);
+        if (!ok) break;
+        int st = kv_it % C::STAGES;
+        ok = mbar_wait(k_full + st, (kv_it / C::STAGES) & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(0, st);
+        mma_commit(s_full + 0);
+        issue_s(1, st);
+        mma_commit(s_full + 1);
+        for (int jj = 0; jj < u.n && ok; ++jj) {
+          const uint32_t it = kv_it + jj;
+          const int stj = it % C::STAGES;
+          mma_commit(k_empty + stj);  // the S MMAs reading K_jj are all issued
+          ok = mbar_wait(v_full + stj, (it / C::STAGES) & 1, abort_flag, p.status);
+          if (!ok) break;
+          const bool last = (jj + 1 == u.n);
+          const int stn = (it + 1) % C::STAGES;
+          for (int s = 0; s < 2 && ok; ++s) {
+            ok = mbar_wait(p_full + s, t_it & 1, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(s, stj, jj > 0);
+            if (!last) {
+              if (s == 0) {
+                ok = mbar_wait(k_full + stn, ((it + 1) / C::STAGES) & 1, abort_flag, p.status);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              issue_s(s, stn);
+              mma_commit(s_full + s);
+            } else {
+              mma_commit(o_full + s);
+            }
+          }
+          mma_commit(v_empty + stj);
+          ++t_it;
+        }
+        kv_it += u.n;
+        mma_commit(q_empty);
+        ++u_it;
+      }
+      // teardown: wait for every MMA issued so far
+      mma_commit(drain);
+      drain_wait(drain, 0, p.status);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && !aborted_at_start) {
+    // ------------------------------------------------------------ softmax
+    const int wg = (warp - 4) >> 2;  // sub-tile
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;     // row of the sub-tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t tS = tmem + lane_off + wg * 128;
+    const uint32_t tO = tmem + lane_off + 256 + wg * 128;
+    uint32_t t_it = 0, o_it = 0;
+    for (int w = blockIdx.x; w < p.n_units; w += gridDim.x) {
+      const Unit u = decode_unit(p, w);
+      const int h = wg ? u.h1 : u.h0;
+      const int qt = wg ? u.qt1 : u.qt0;
+      const int i = qt * kBM + r;  // local query row
+      const bool in_range = i < p.L;
+      const int t = p.seq_start + i;
+      const int32_t lo = in_range ? p.qlo[(size_t)u.b * p.Lpad + i] : kPadLo;
+      const size_t row = static_cast<size_t>(u.b * p.Hq + h) * p.L + i;
+      if (u.n <= 0) {
+        if (in_range) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + row * D);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+          p.lse[row] = -INFINITY;
+        }
+        continue;
+      }
+      float m_used = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int jj = 0; jj < u.n; ++jj) {
+        const int k0 = (u.kt_lo + jj) * kBN;
+        ok = mbar_wait_warp(s_full + wg, t_it & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        // allowed columns of this tile for this row: [ca, cb]
+        int ca = 1, cb = 0;
+        if (lo != kPadLo) {
+          ca = lo - k0;
+          cb = t - k0;
+        }
+        const bool full = __all_sync(0xffffffffu, ca <= 0 && cb >= kBN - 1);
+        // pass 1: row max of the allowed scores
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tS + c * 32, v);
+          if (full) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int col = c * 32 + e;
+              const float x = (col >= ca && col <= cb) ? __uint_as_float(v[e]) : -INFINITY;
+              mx = fmaxf(mx, x);
+            }
+          }
+        }
+        const float m_tile = mx * p.scale_log2;
+        const float m_new = fmaxf(m_used, m_tile);
+        float factor = 1.f;
+        bool rescale = false;
+        if (m_new != -INFINITY) {
+          if (m_used == -INFINITY) {
+            m_used = m_new;  // nothing accumulated yet for this row (O row is 0)
+          } else if (m_new > m_used + kRescaleThreshold) {
+            factor = fast_exp2(m_used - m_new);
+            l *= factor;
+            m_used = m_new;
+            rescale = true;
+          }
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O holds P_0..P_{jj-1} times V: the S_full wait covered those MMAs
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tO + c * 32, v);
+            uint32_t a[16], b2[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              a[e] = __float_as_uint(__uint_as_float(v[e]) * factor);
+              b2[e] = __float_as_uint(__uint_as_float(v[16 + e]) * factor);
+            }
+            tmem_st16(tO + c * 32, a);
+            tmem_st16(tO + c * 32 + 16, b2);
+          }
+        }
+        // pass 2: P = exp2(s * scale * log2 e - m), row sum, bf16 P into TMEM
+        const float m_use = (m_used == -INFINITY) ? 0.f : m_used;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tS + c * 32, v);
+          float pr[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float x = fast_exp2(fmaf(__uint_as_float(v[e]), p.scale_log2, -m_use));
+            if (!full) {
+              const int col = c * 32 + e;
+              x = (col >= ca && col <= cb) ? x : 0.f;
+            }
+            pr[e] = x;
+            l += x;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pr[2 * e], pr[2 * e + 1]);
+          tmem_st16(tS + c * 16, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full + wg);
+        ++t_it;
+      }
+      if (!ok) break;
+      // epilogue: O / l -> bf16, LSE
+      ok = mbar_wait_warp(o_full + wg, o_it & 1, abort_flag, p.status);
+      if (!ok) break;
+      ++o_it;
+      tc_fence_after();
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tO + c * 32, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
+        if (in_range) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + row * D + c * 32);
+          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+          dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+        }
+      }
+      if (in_range) p.lse[row] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      tc_fence_before();
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const FwdParams& p, int num_sms,
+                                cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(bd_fwd_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int grid = p.n_units < num_sms ? p.n_units : num_sms;
+  if (grid <= 0) return cudaSuccess;
+  bd_fwd_kernel<D><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const AttnDims& d, const void* plan, void* out, float* lse,
+                       int32_t* status, int num_sms, cudaStream_t stream) {
+  const PlanLayout pl = plan_layout(d.B, d.Hq, d.Hkv, d.L, d.S);
+  const char* base = static_cast<const char*>(plan);
+  FwdParams p{};
+  p.B = d.B;
+  p.Hq = d.Hq;
+  p.Hkv = d.Hkv;
+  p.L = d.L;
+  p.S = d.S;
+  p.seq_start = d.seq_start;
+  p.G = d.Hq / d.Hkv;
+  p.g_odd = p.G % 2;
+  p.HP = p.g_odd ? p.G : p.G / 2;
+  p.NQB = pl.NQB;
+  p.Lpad = pl.Lpad;
+  p.n_units = d.B * pl.NQB * d.Hkv * p.HP;
+  p.scale_log2 = d.scale_log2;
+  p.qlo = reinterpret_cast<const int32_t*>(base + pl.qlo);
+  p.fwd_range = reinterpret_cast<const int32_t*>(base + pl.fwd_range);
+  p.fwd_order = reinterpret_cast<const int32_t*>(base + pl.fwd_order);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.status = status;
+  if (d.D == 64) return launch_fwd_t<64>(tq, tk, tv, p, num_sms, stream);
+  return launch_fwd_t<128>(tq, tk, tv, p, num_sms, stream);
+}
+
+}  // namespace bd

@@ -1,0 +1,117 @@
+// Internal declarations shared by the library's translation units: constants,
+// the plan buffer layout and the kernel launchers called by the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/bd_attn.h"
+
+namespace bd {
+
+// Tile sizes: 128 query rows x 128 keys per MMA tile.
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+
+// Device-side waits give up after this long (a healthy wait lasts microseconds).
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+
+// Mask lower bound of a query row that attends nothing (padding / past L).
+constexpr int32_t kPadLo = 0x7fffffff;
+
+// Largest work list the single-CTA sorter handles.
+constexpr int kMaxListLen = 16384;
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Plan buffer layout (byte offsets from the plan base, each 256-aligned).
+//   qlo       int32 [B, Lpad]  segment start of query row i (global position),
+//                              kPadLo when the row attends nothing
+//   kend      int32 [B, Spad]  end of the segment holding key p, or p itself
+//                              for a padding key (no query attends it)
+//   fwd_range int32 [B*NQB, 2] non-empty key-tile range [lo, hi] of each
+//                              query block (hi < lo when empty)
+//   bwd_range int32 [B*NKT, 2] query-tile range [lo, hi] of each key tile
+//   fwd_order int32 [B*NQB]    query blocks sorted by cost, longest first
+//   bwd_order int32 [B*NKT]    key tiles sorted by cost, longest first
+// A forward query block is 128 rows when Hq/Hkv is even (its two halves are
+// two heads of one group) and 256 rows when it is odd (two consecutive
+// 128-row tiles of one head).
+struct PlanLayout {
+  int NQB, NKT, QROWS, Lpad, Spad;
+  size_t qlo, kend, fwd_range, bwd_range, fwd_order, bwd_order, total;
+};
+
+inline PlanLayout plan_layout(int B, int Hq, int Hkv, int L, int S) {
+  PlanLayout p{};
+  const int G = Hkv > 0 ? Hq / Hkv : 1;
+  p.QROWS = (G % 2 == 0) ? kBM : 2 * kBM;
+  p.NQB = cdiv(L, p.QROWS);
+  p.NKT = cdiv(S, kBN);
+  p.Lpad = p.NQB * p.QROWS;
+  p.Spad = p.NKT * kBN;
+  size_t off = 0;
+  p.qlo = off;       off = align256(off + sizeof(int32_t) * (size_t)B * p.Lpad);
+  p.kend = off;      off = align256(off + sizeof(int32_t) * (size_t)B * p.Spad);
+  p.fwd_range = off; off = align256(off + sizeof(int32_t) * 2 * (size_t)B * p.NQB);
+  p.bwd_range = off; off = align256(off + sizeof(int32_t) * 2 * (size_t)B * p.NKT);
+  p.fwd_order = off; off = align256(off + sizeof(int32_t) * (size_t)B * p.NQB);
+  p.bwd_order = off; off = align256(off + sizeof(int32_t) * (size_t)B * p.NKT);
+  p.total = off;
+  return p;
+}
+
+// Backward workspace: fp32 dq accumulator [B,Hq,L,D] and per-row
+// (lse * log2 e, Delta) pairs [B,Hq,Lq] with Lq = ceil(L/128)*128.
+struct BwdLayout {
+  int Lq;
+  size_t dqacc, lsed, total;
+};
+
+inline BwdLayout bwd_layout(int B, int Hq, int L, int D) {
+  BwdLayout w{};
+  w.Lq = cdiv(L, kBM) * kBM;
+  size_t off = 0;
+  w.dqacc = off; off = align256(off + sizeof(float) * (size_t)B * Hq * L * D);
+  w.lsed = off;  off = align256(off + sizeof(float) * 2 * (size_t)B * Hq * w.Lq);
+  w.total = off;
+  return w;
+}
+
+struct AttnDims {
+  int B, Hq, Hkv, L, S, D, seq_start;
+  float scale;        // softmax scale (resolved, > 0)
+  float scale_log2;   // scale * log2(e)
+};
+
+// ---- launchers (each enqueues on `stream`; returns the launch error) ----
+
+cudaError_t launch_doc_ids(const int32_t* cu, const int32_t* row_ptr, int B, int S, int32_t* ids,
+                           int32_t* status, cudaStream_t stream);
+cudaError_t launch_segments(const int32_t* ids, int B, int S, int32_t* seg, int32_t* seg_ids,
+                            int32_t* nseg, cudaStream_t stream);
+cudaError_t launch_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg, int B,
+                        int Hq, int Hkv, int L, int S, int seq_start, void* plan,
+                        cudaStream_t stream);
+
+// Tensor maps for q/k/v-like tensors [planes, rows, D] (bf16, 128-byte swizzle,
+// box 64 x 128 x 1).  Returns false when the driver rejects the map.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int planes, int rows, int D);
+
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const AttnDims& d, const void* plan, void* out, float* lse,
+                       int32_t* status, int num_sms, cudaStream_t stream);
+// Backward stages (bit mask): per-row terms + accumulator zeroing, the main
+// dK/dV/dQ kernel, and the dq conversion.
+constexpr int kBwdPrepare = 1, kBwdMain = 2, kBwdFinish = 4;
+
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const AttnDims& d, const void* plan,
+                       const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                       void* dv, void* workspace, int32_t* status, int stages, int num_sms,
+                       cudaStream_t stream);
+
+}  // namespace bd

@@ -1,0 +1,200 @@
+// Attention plan: mask bounds per row, non-empty tile ranges, longest-first
+// work lists.
+//
+// The mask is the per-document causal rule of cp_blockdiag_sdpa (page
+// "nemo_automodel.components.distributed.blockdiag_cp"): the query at global
+// position t attends keys j <= t of its own segment, and a query in a padding
+// segment (id 0) attends nothing.  Because segments are contiguous runs, each
+// query row's key set is one interval [lo(t), t], and each key p is attended
+// by the query interval [p, end of p's segment).  The kernels below turn the
+// segment list into those bounds and into the tile ranges the attention
+// kernels iterate over, so that fully masked tiles are never loaded.
+#include "bd_ptx.cuh"
+
+namespace bd {
+
+// first k with seg[k] > x, minus one: the segment holding x (seg[0] = 0 <= x < seg[n])
+__device__ __forceinline__ int find_segment(const int32_t* __restrict__ seg, int n, int x) {
+  int lo = 1, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (seg[mid] > x) hi = mid; else lo = mid + 1;
+  }
+  return lo - 1;
+}
+
+__global__ void __launch_bounds__(256) plan_rows_kernel(const int32_t* __restrict__ seg_all,
+                                                        const int32_t* __restrict__ seg_ids_all,
+                                                        const int32_t* __restrict__ nseg, int L,
+                                                        int S, int seq_start, int Lpad, int Spad,
+                                                        int32_t* __restrict__ qlo,
+                                                        int32_t* __restrict__ kend) {
+  const int b = blockIdx.y;
+  const int x = blockIdx.x * blockDim.x + threadIdx.x;
+  const int32_t* seg = seg_all + (size_t)b * (S + 1);
+  const int32_t* sid = seg_ids_all + (size_t)b * S;
+  const int n = nseg[b];
+  if (x < Lpad) {
+    int32_t lo = kPadLo;
+    if (x < L) {
+      const int t = seq_start + x;
+      const int k = find_segment(seg, n, t);
+      if (sid[k] != 0) lo = seg[k];
+    }
+    qlo[(size_t)b * Lpad + x] = lo;
+  }
+  if (x < Spad) {
+    int32_t e = x;
+    if (x < S) {
+      const int k = find_segment(seg, n, x);
+      if (sid[k] != 0) e = seg[k + 1];
+    }
+    kend[(size_t)b * Spad + x] = e;
+  }
+}
+
+// One warp per forward query block or backward key tile.
+__global__ void __launch_bounds__(256) plan_tiles_kernel(const int32_t* __restrict__ qlo,
+                                                         const int32_t* __restrict__ kend, int B,
+                                                         int L, int seq_start, int NQB, int QROWS,
+                                                         int Lpad, int NKT, int Spad,
+                                                         int32_t* __restrict__ fwd_range,
+                                                         int32_t* __restrict__ bwd_range) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nf = B * NQB;
+  if (w < nf) {
+    const int b = w / NQB, qb = w % NQB;
+    int mn = 0x7fffffff, mx = -1;
+    for (int r = lane; r < QROWS; r += 32) {
+      const int i = qb * QROWS + r;
+      const int32_t lo = qlo[(size_t)b * Lpad + i];
+      if (lo != kPadLo) {
+        mn = min(mn, lo);
+        mx = max(mx, seq_start + i);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (lane == 0) {
+      const bool any = mx >= 0;
+      fwd_range[2 * w] = any ? mn / kBN : 0;
+      fwd_range[2 * w + 1] = any ? mx / kBN : -1;
+    }
+  } else if (w < nf + B * NKT) {
+    const int u = w - nf;
+    const int b = u / NKT, kt = u % NKT;
+    int mn = 0x7fffffff, mx = -1;
+    for (int r = lane; r < kBN; r += 32) {
+      const int p = kt * kBN + r;
+      const int32_t e = kend[(size_t)b * Spad + p];
+      if (e > p) {
+        mn = min(mn, p);
+        mx = max(mx, e);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (lane == 0) {
+      int a = 0, c = 0;
+      if (mx >= 0) {
+        a = max(mn, seq_start) - seq_start;
+        c = min(mx, seq_start + L) - seq_start;
+      }
+      bwd_range[2 * u] = (a < c) ? a / kBM : 0;
+      bwd_range[2 * u + 1] = (a < c) ? (c - 1) / kBM : -1;
+    }
+  }
+}
+
+// Sort both work lists by cost (range length), longest first, ties by index.
+// One CTA; bitonic sort of 64-bit keys in shared memory.
+constexpr int kSortThreads = 1024;
+
+__device__ void sort_desc(const int32_t* __restrict__ range, int n, int32_t* __restrict__ order,
+                          unsigned long long* keys) {
+  int np = 1;
+  while (np < n) np <<= 1;
+  for (int i = threadIdx.x; i < np; i += blockDim.x) {
+    unsigned long long key = ~0ull;
+    if (i < n) {
+      const int cost = max(0, range[2 * i + 1] - range[2 * i] + 1);
+      key = (static_cast<unsigned long long>(0x7fffffffu - static_cast<unsigned>(cost)) << 32) |
+            static_cast<unsigned>(i);
+    }
+    keys[i] = key;
+  }
+  __syncthreads();
+  for (int size = 2; size <= np; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < np; i += blockDim.x) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool up = (i & size) == 0;
+          const unsigned long long a = keys[i], c = keys[j];
+          if ((a > c) == up) {
+            keys[i] = c;
+            keys[j] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    order[i] = static_cast<int32_t>(keys[i] & 0xffffffffu);
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kSortThreads) plan_sort_kernel(const int32_t* fwd_range, int nf,
+                                                                 int32_t* fwd_order,
+                                                                 const int32_t* bwd_range, int nb,
+                                                                 int32_t* bwd_order) {
+  extern __shared__ unsigned long long keys[];
+  sort_desc(fwd_range, nf, fwd_order, keys);
+  sort_desc(bwd_range, nb, bwd_order, keys);
+}
+
+cudaError_t launch_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg, int B,
+                        int Hq, int Hkv, int L, int S, int seq_start, void* plan,
+                        cudaStream_t stream) {
+  const PlanLayout pl = plan_layout(B, Hq, Hkv, L, S);
+  char* base = static_cast<char*>(plan);
+  int32_t* qlo = reinterpret_cast<int32_t*>(base + pl.qlo);
+  int32_t* kend = reinterpret_cast<int32_t*>(base + pl.kend);
+  int32_t* fr = reinterpret_cast<int32_t*>(base + pl.fwd_range);
+  int32_t* br = reinterpret_cast<int32_t*>(base + pl.bwd_range);
+  int32_t* fo = reinterpret_cast<int32_t*>(base + pl.fwd_order);
+  int32_t* bo = reinterpret_cast<int32_t*>(base + pl.bwd_order);
+
+  dim3 g1(cdiv(max(pl.Lpad, pl.Spad), 256), B);
+  plan_rows_kernel<<<g1, 256, 0, stream>>>(seg, seg_ids, nseg, L, S, seq_start, pl.Lpad, pl.Spad,
+                                           qlo, kend);
+  const int warps = B * pl.NQB + B * pl.NKT;
+  plan_tiles_kernel<<<cdiv(warps * 32, 256), 256, 0, stream>>>(
+      qlo, kend, B, L, seq_start, pl.NQB, pl.QROWS, pl.Lpad, pl.NKT, pl.Spad, fr, br);
+  const int nf = B * pl.NQB, nb = B * pl.NKT;
+  int np = 1;
+  while (np < max(nf, nb)) np <<= 1;
+  const size_t smem = sizeof(unsigned long long) * np;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (smem > 48 * 1024 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(plan_sort_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sizeof(unsigned long long) * kMaxListLen));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  plan_sort_kernel<<<1, kSortThreads, smem, stream>>>(fr, nf, fo, br, nb, bo);
+  return cudaGetLastError();
+}
+
+}  // namespace bd
