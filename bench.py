@@ -161,6 +161,7 @@ class HotPath:
         self.plans = [torch.empty(N.bd_attn_plan_size(B, Hq, Hkv, L, S), dtype=torch.uint8,
                                   device=device) for _ in wl.seq_starts]
         self.out = [torch.empty_like(x) for x in self.q_iv]
+        self.out_lo = [torch.empty_like(x) for x in self.q_iv]
         self.lse = [torch.empty((B, Hq, L), dtype=torch.float32, device=device)
                     for _ in wl.seq_starts]
         self.dq = [torch.empty_like(x) for x in self.q_iv]
@@ -184,20 +185,21 @@ class HotPath:
         for i, s0 in enumerate(wl.seq_starts):
             N.bd_attn_plan(self.seg, self.sid, self.nseg, B, Hq, Hkv, L, S, s0, self.plans[i])
             N.bd_attn_fwd(self.q_iv[i], self.k, self.v, B, Hq, Hkv, L, S, D, s0, self.scale,
-                          self.gqa, self.plans[i], self.out[i], self.lse[i], self.status)
+                          self.gqa, self.plans[i], self.out[i], self.lse[i], self.out_lo[i],
+                          self.status)
             args = (self.q_iv[i], self.k, self.v, self.out[i], self.lse[i], self.do_iv[i], B, Hq,
                     Hkv, L, S, D, s0, self.scale, self.gqa, self.plans[i], self.dq[i], self.dk,
                     self.dv, self.ws, self.status)
-            N.bd_attn_bwd_stages(*args, stages=1)
+            N.bd_attn_bwd_stages(*args, out_lo=self.out_lo[i], stages=1)
             if time_main:
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record()
-            N.bd_attn_bwd_stages(*args, stages=2)
+            N.bd_attn_bwd_stages(*args, out_lo=self.out_lo[i], stages=2)
             if time_main:
                 e1.record()
                 self.main_events.append((e0, e1))
-            N.bd_attn_bwd_stages(*args, stages=4)
+            N.bd_attn_bwd_stages(*args, out_lo=self.out_lo[i], stages=4)
 
     def e2e_buffers(self):
         """Pinned host copies of the inputs and room for the results."""

@@ -123,16 +123,22 @@ int bd_attn_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg
  *   out          bf16 [B, Hq, L, D] output.
  *   lse          fp32 [B, Hq, L] output: natural-log log-sum-exp of the
  *                scaled scores of each row (-inf for padding rows).
+ *   out_lo       optional bf16 [B, Hq, L, D] output (NULL to skip): the
+ *                rounding residual bf16(O - out) of the fp32 result O, so
+ *                that out + out_lo carries O to about 16 significant bits.
+ *                The backward uses it for Delta = <dout, O>; without it
+ *                Delta is formed from the bf16 output alone.
  */
 int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L, int S,
                 int D, int seq_start, float scale, int enable_gqa, const void* plan,
-                size_t plan_bytes, void* out, float* lse, int32_t* dev_status,
+                size_t plan_bytes, void* out, float* lse, void* out_lo, int32_t* dev_status,
                 bd_stream_t stream);
 
 /*
  * Backward pass: gradients of sum(out * dout) (the autograd backward of the
  * forward above).  Same arguments as bd_attn_fwd plus
  *   out, lse     the forward's outputs for these inputs.
+ *   out_lo       the forward's residual output, or NULL (less precise Delta).
  *   dout         bf16 [B, Hq, L, D].
  *   dq           bf16 [B, Hq, L, D] output.
  *   dk, dv       bf16 [B, Hkv, S, D] outputs, summed over the query heads of
@@ -143,8 +149,9 @@ int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int 
  * last bits between runs; dk and dv are deterministic.
  */
 size_t bd_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int S, int D);
-int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
-                const void* dout, int B, int Hq, int Hkv, int L, int S, int D, int seq_start,
+int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* out_lo,
+                const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S, int D,
+                int seq_start,
                 float scale, int enable_gqa, const void* plan, size_t plan_bytes, void* dq,
                 void* dk, void* dv, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                 bd_stream_t stream);
@@ -159,7 +166,8 @@ int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
  * for timing one stage at a time.
  */
 int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* out,
-                       const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S,
+                       const void* out_lo, const float* lse, const void* dout, int B, int Hq,
+                       int Hkv, int L, int S,
                        int D, int seq_start, float scale, int enable_gqa, const void* plan,
                        size_t plan_bytes, void* dq, void* dk, void* dv, void* workspace,
                        size_t workspace_bytes, int32_t* dev_status, int stages,

@@ -35,11 +35,11 @@ SIGNATURES = {
     "bd_attn_plan_size": (_c_size, [_c_int] * 5),
     "bd_attn_plan": (_c_int, [_vp, _vp, _vp] + [_c_int] * 6 + [_vp, _c_size, _vp]),
     "bd_attn_fwd": (_c_int, [_vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size,
-                                                               _vp, _vp, _vp, _vp]),
+                                                               _vp, _vp, _vp, _vp, _vp]),
     "bd_attn_bwd_workspace_size": (_c_size, [_c_int] * 6),
-    "bd_attn_bwd": (_c_int, [_vp] * 6 + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size, _vp,
+    "bd_attn_bwd": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size, _vp,
                                                          _vp, _vp, _vp, _c_size, _vp, _vp]),
-    "bd_attn_bwd_stages": (_c_int, [_vp] * 6 + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size,
+    "bd_attn_bwd_stages": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size,
                                                                 _vp, _vp, _vp, _vp, _c_size, _vp,
                                                                 _c_int, _vp]),
     "bd_get_device_status": (_c_int, [_vp, _vp, _vp]),
@@ -137,15 +137,17 @@ def bd_attn_plan(seg, seg_ids, nseg, B: int, Hq: int, Hkv: int, L: int, S: int, 
 
 
 def bd_attn_fwd(q, k, v, B: int, Hq: int, Hkv: int, L: int, S: int, D: int, seq_start: int,
-                scale: float, enable_gqa: bool, plan, out, lse, dev_status=None,
+                scale: float, enable_gqa: bool, plan, out, lse, out_lo=None, dev_status=None,
                 stream=None) -> None:
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
         _want(t, torch.bfloat16, n)
+    if out_lo is not None:
+        _want(out_lo, torch.bfloat16, "out_lo")
     _want(lse, torch.float32, "lse")
     _check(lib().bd_attn_fwd(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, L, S, D, seq_start,
                              float(scale), int(bool(enable_gqa)), _ptr(plan),
                              plan.numel() * plan.element_size(), _ptr(out), _ptr(lse),
-                             _ptr(dev_status), _stream(stream)), "bd_attn_fwd")
+                             _ptr(out_lo), _ptr(dev_status), _stream(stream)), "bd_attn_fwd")
 
 
 def bd_attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, L: int, S: int, D: int) -> int:
@@ -154,12 +156,13 @@ def bd_attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, L: int, S: int, D: int
 
 def bd_attn_bwd(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: int, D: int,
                 seq_start: int, scale: float, enable_gqa: bool, plan, dq, dk, dv, workspace,
-                dev_status=None, stream=None) -> None:
+                out_lo=None, dev_status=None, stream=None) -> None:
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"),
                  (dk, "dk"), (dv, "dv")):
         _want(t, torch.bfloat16, n)
     _want(lse, torch.float32, "lse")
-    _check(lib().bd_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), B, Hq,
+    _check(lib().bd_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo), _ptr(lse),
+                             _ptr(dout), B, Hq,
                              Hkv, L, S, D, seq_start, float(scale), int(bool(enable_gqa)),
                              _ptr(plan), plan.numel() * plan.element_size(), _ptr(dq), _ptr(dk),
                              _ptr(dv), _ptr(workspace),
@@ -169,8 +172,10 @@ def bd_attn_bwd(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: i
 
 def bd_attn_bwd_stages(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: int,
                        D: int, seq_start: int, scale: float, enable_gqa: bool, plan, dq, dk, dv,
-                       workspace, dev_status=None, stages: int = 7, stream=None) -> None:
-    _check(lib().bd_attn_bwd_stages(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                       workspace, out_lo=None, dev_status=None, stages: int = 7,
+                       stream=None) -> None:
+    _check(lib().bd_attn_bwd_stages(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo),
+                                    _ptr(lse), _ptr(dout),
                                     B, Hq, Hkv, L, S, D, seq_start, float(scale),
                                     int(bool(enable_gqa)), _ptr(plan),
                                     plan.numel() * plan.element_size(), _ptr(dq), _ptr(dk),

@@ -94,19 +94,24 @@ def _resolve_scale(scale, D):
     return float(D) ** -0.5 if scale is None else float(scale)
 
 
-def attn_forward(q, k, v, plan, seq_start=0, scale=None, enable_gqa=False):
-    """out [B,Hq,L,D] bf16 and lse [B,Hq,L] fp32 (no autograd)."""
+def attn_forward(q, k, v, plan, seq_start=0, scale=None, enable_gqa=False, residual=True):
+    """out [B,Hq,L,D] bf16, lse [B,Hq,L] fp32 and the rounding residual of out (no autograd).
+
+    The residual (bf16, same shape as out, or None when ``residual`` is
+    False) lets the backward form Delta = <dout, O> from O at ~16 bits.
+    """
     B, Hq, L, D = q.shape
     Hkv, S = k.shape[1], k.shape[2]
     out = torch.empty_like(q)
+    out_lo = torch.empty_like(q) if residual else None
     lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device)
     N.bd_attn_fwd(q, k, v, B, Hq, Hkv, L, S, D, seq_start, _resolve_scale(scale, D), enable_gqa,
-                  plan, out, lse, device_status_word(q.device))
-    return out, lse
+                  plan, out, lse, out_lo, device_status_word(q.device))
+    return out, lse, out_lo
 
 
 def attn_backward(q, k, v, out, lse, dout, plan, seq_start=0, scale=None, enable_gqa=False,
-                  workspace=None):
+                  workspace=None, out_lo=None):
     """dq, dk, dv (bf16) for the forward above (no autograd)."""
     B, Hq, L, D = q.shape
     Hkv, S = k.shape[1], k.shape[2]
@@ -117,7 +122,7 @@ def attn_backward(q, k, v, out, lse, dout, plan, seq_start=0, scale=None, enable
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
     N.bd_attn_bwd(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, seq_start,
-                  _resolve_scale(scale, D), enable_gqa, plan, dq, dk, dv, workspace,
+                  _resolve_scale(scale, D), enable_gqa, plan, dq, dk, dv, workspace, out_lo,
                   device_status_word(q.device))
     return dq, dk, dv
 
@@ -128,18 +133,18 @@ class BlockdiagAttention(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, plan, seq_start, scale, enable_gqa):
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
-        out, lse = attn_forward(q, k, v, plan, seq_start, scale, enable_gqa)
-        ctx.save_for_backward(q, k, v, out, lse, plan)
+        out, lse, out_lo = attn_forward(q, k, v, plan, seq_start, scale, enable_gqa)
+        ctx.save_for_backward(q, k, v, out, lse, plan, out_lo)
         ctx.args = (seq_start, scale, enable_gqa)
         ctx.mark_non_differentiable(lse)
         return out, lse
 
     @staticmethod
     def backward(ctx, dout, _dlse):
-        q, k, v, out, lse, plan = ctx.saved_tensors
+        q, k, v, out, lse, plan, out_lo = ctx.saved_tensors
         seq_start, scale, enable_gqa = ctx.args
         dq, dk, dv = attn_backward(q, k, v, out, lse, dout.contiguous(), plan, seq_start, scale,
-                                   enable_gqa)
+                                   enable_gqa, out_lo=out_lo)
         return dq, dk, dv, None, None, None, None
 
 

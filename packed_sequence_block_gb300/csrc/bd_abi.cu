@@ -150,11 +150,12 @@ int bd_attn_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg
 
 int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L, int S,
                 int D, int seq_start, float scale, int enable_gqa, const void* plan,
-                size_t plan_bytes, void* out, float* lse, int32_t* dev_status,
+                size_t plan_bytes, void* out, float* lse, void* out_lo, int32_t* dev_status,
                 bd_stream_t stream) {
   if (q == nullptr || k == nullptr || v == nullptr || plan == nullptr || out == nullptr ||
       lse == nullptr)
     return BD_ERR_INVALID_ARG;
+  if (out_lo != nullptr && !aligned(out_lo, 16)) return BD_ERR_INVALID_ARG;
   int st = check_dims(B, Hq, Hkv, L, S, D, seq_start, enable_gqa);
   if (st != BD_OK) return st;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
@@ -170,7 +171,7 @@ int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int 
     return BD_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return BD_ERR_CUDA;
-  return launch_fwd(tq, tk, tv, d, plan, out, lse, dev_status, sms, stream) == cudaSuccess
+  return launch_fwd(tq, tk, tv, d, plan, out, out_lo, lse, dev_status, sms, stream) == cudaSuccess
              ? BD_OK
              : BD_ERR_CUDA;
 }
@@ -183,7 +184,8 @@ size_t bd_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int S, int D) {
 }
 
 int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* out,
-                       const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S,
+                       const void* out_lo, const float* lse, const void* dout, int B, int Hq,
+                       int Hkv, int L, int S,
                        int D, int seq_start, float scale, int enable_gqa, const void* plan,
                        size_t plan_bytes, void* dq, void* dk, void* dv, void* workspace,
                        size_t workspace_bytes, int32_t* dev_status, int stages,
@@ -193,6 +195,7 @@ int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* 
       workspace == nullptr)
     return BD_ERR_INVALID_ARG;
   if (stages <= 0 || stages > (kBwdPrepare | kBwdMain | kBwdFinish)) return BD_ERR_INVALID_ARG;
+  if (out_lo != nullptr && !aligned(out_lo, 16)) return BD_ERR_INVALID_ARG;
   int st = check_dims(B, Hq, Hkv, L, S, D, seq_start, enable_gqa);
   if (st != BD_OK) return st;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
@@ -210,18 +213,19 @@ int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* 
     return BD_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return BD_ERR_CUDA;
-  return launch_bwd(tq, tk, tv, tdo, d, plan, out, lse, dout, dq, dk, dv, workspace, dev_status,
-                    stages, sms, stream) == cudaSuccess
+  return launch_bwd(tq, tk, tv, tdo, d, plan, out, out_lo, lse, dout, dq, dk, dv, workspace,
+                    dev_status, stages, sms, stream) == cudaSuccess
              ? BD_OK
              : BD_ERR_CUDA;
 }
 
-int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
-                const void* dout, int B, int Hq, int Hkv, int L, int S, int D, int seq_start,
+int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* out_lo,
+                const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S, int D,
+                int seq_start,
                 float scale, int enable_gqa, const void* plan, size_t plan_bytes, void* dq,
                 void* dk, void* dv, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                 bd_stream_t stream) {
-  return bd_attn_bwd_stages(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
+  return bd_attn_bwd_stages(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
                             enable_gqa, plan, plan_bytes, dq, dk, dv, workspace, workspace_bytes,
                             dev_status, kBwdPrepare | kBwdMain | kBwdFinish, stream);
 }

@@ -95,6 +95,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // One thread per 8 elements of a row; rows [0, Lq) of every (b, h) plane.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
+                                                      const __nv_bfloat16* __restrict__ out_lo,
                                                       const __nv_bfloat16* __restrict__ dout,
                                                       const float* __restrict__ lse, int planes,
                                                       int L, int Lq, float2* __restrict__ lsed,
@@ -111,14 +112,18 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     const size_t off = ((size_t)plane * L + i) * D + part * 8;
     const uint4 o4 = *reinterpret_cast<const uint4*>(out + off);
     const uint4 d4 = *reinterpret_cast<const uint4*>(dout + off);
+    const uint4 l4 = out_lo != nullptr ? *reinterpret_cast<const uint4*>(out_lo + off)
+                                       : make_uint4(0, 0, 0, 0);
     const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o4);
+    const __nv_bfloat162* l2v = reinterpret_cast<const __nv_bfloat162*>(&l4);
     const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&d4);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float2 a = __bfloat1622float2(o2[j]);
+      const float2 r = __bfloat1622float2(l2v[j]);
       const float2 b = __bfloat1622float2(d2[j]);
-      acc = fmaf(a.x, b.x, acc);
-      acc = fmaf(a.y, b.y, acc);
+      acc = fmaf(a.x + r.x, b.x, acc);
+      acc = fmaf(a.y + r.y, b.y, acc);
     }
     float4* z = reinterpret_cast<float4*>(dqacc + off);
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -508,8 +513,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const CUtensorMap& tdo,
-                                const BwdParams& p, const void* out, const float* lse,
-                                const void* dout, void* dq, int stages, int num_sms,
+                                const BwdParams& p, const void* out, const void* out_lo,
+                                const float* lse, const void* dout, void* dq, int stages,
+                                int num_sms,
                                 cudaStream_t stream) {
   using C = BwdCfg<D>;
   static bool attr_set[64] = {};
@@ -525,7 +531,8 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
   if (stages & kBwdPrepare) {
     const long long threads = (long long)planes * p.Lq * (D / 8);
     bwd_pre_kernel<D><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse,
+        static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(out_lo),
+        static_cast<const __nv_bfloat16*>(dout), lse,
         planes, p.L, p.Lq, const_cast<float2*>(p.lsed), p.dqacc);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -546,7 +553,8 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const AttnDims& d, const void* plan,
-                       const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                       const void* out, const void* out_lo, const float* lse, const void* dout,
+                       void* dq, void* dk,
                        void* dv, void* workspace, int32_t* status, int stages, int num_sms,
                        cudaStream_t stream) {
   const PlanLayout pl = plan_layout(d.B, d.Hq, d.Hkv, d.L, d.S);
@@ -575,9 +583,10 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.status = status;
-  if (d.D == 64) return launch_bwd_t<64>(tq, tk, tv, tdo, p, out, lse, dout, dq, stages, num_sms,
+  if (d.D == 64) return launch_bwd_t<64>(tq, tk, tv, tdo, p, out, out_lo, lse, dout, dq, stages, num_sms,
                                           stream);
-  return launch_bwd_t<128>(tq, tk, tv, tdo, p, out, lse, dout, dq, stages, num_sms, stream);
+  return launch_bwd_t<128>(tq, tk, tv, tdo, p, out, out_lo, lse, dout, dq, stages, num_sms,
+                           stream);
 }
 
 }  // namespace bd

@@ -46,6 +46,7 @@ struct FwdParams {
   const int32_t* fwd_range;
   const int32_t* fwd_order;
   __nv_bfloat16* out;
+  __nv_bfloat16* out_lo;  // optional: bf16(O - bf16(O)), the rounding residual of out
   float* lse;
   int32_t* status;
 };
@@ -301,6 +302,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint4* dst = reinterpret_cast<uint4*>(p.out + row * D);
 #pragma unroll
           for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+          if (p.out_lo != nullptr) {
+            uint4* dl = reinterpret_cast<uint4*>(p.out_lo + row * D);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) dl[c] = make_uint4(0, 0, 0, 0);
+          }
           p.lse[row] = -INFINITY;
         }
         continue;
@@ -405,16 +411,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tO + c * 32, v);
-        uint32_t pk[16];
+        uint32_t pk[16], pl[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
+        for (int e = 0; e < 16; ++e) {
+          const float a = __uint_as_float(v[2 * e]) * inv, b = __uint_as_float(v[2 * e + 1]) * inv;
+          pk[e] = pack_bf16x2(a, b);
+          pl[e] = pack_bf16x2(a - __uint_as_float(pk[e] << 16),
+                              b - __uint_as_float(pk[e] & 0xffff0000u));
+        }
         if (in_range) {
           uint4* dst = reinterpret_cast<uint4*>(p.out + row * D + c * 32);
           dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
           dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+          if (p.out_lo != nullptr) {
+            uint4* dl = reinterpret_cast<uint4*>(p.out_lo + row * D + c * 32);
+            dl[0] = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+            dl[1] = make_uint4(pl[4], pl[5], pl[6], pl[7]);
+            dl[2] = make_uint4(pl[8], pl[9], pl[10], pl[11]);
+            dl[3] = make_uint4(pl[12], pl[13], pl[14], pl[15]);
+          }
         }
       }
       if (in_range) p.lse[row] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
@@ -452,8 +469,8 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
 }
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const AttnDims& d, const void* plan, void* out, float* lse,
-                       int32_t* status, int num_sms, cudaStream_t stream) {
+                       const AttnDims& d, const void* plan, void* out, void* out_lo,
+                       float* lse, int32_t* status, int num_sms, cudaStream_t stream) {
   const PlanLayout pl = plan_layout(d.B, d.Hq, d.Hkv, d.L, d.S);
   const char* base = static_cast<const char*>(plan);
   FwdParams p{};
@@ -474,6 +491,7 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.fwd_range = reinterpret_cast<const int32_t*>(base + pl.fwd_range);
   p.fwd_order = reinterpret_cast<const int32_t*>(base + pl.fwd_order);
   p.out = static_cast<__nv_bfloat16*>(out);
+  p.out_lo = static_cast<__nv_bfloat16*>(out_lo);
   p.lse = lse;
   p.status = status;
   if (d.D == 64) return launch_fwd_t<64>(tq, tk, tv, p, num_sms, stream);

@@ -102,15 +102,16 @@ cudaError_t launch_plan(const int32_t* seg, const int32_t* seg_ids, const int32_
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int planes, int rows, int D);
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const AttnDims& d, const void* plan, void* out, float* lse,
-                       int32_t* status, int num_sms, cudaStream_t stream);
+                       const AttnDims& d, const void* plan, void* out, void* out_lo,
+                       float* lse, int32_t* status, int num_sms, cudaStream_t stream);
 // Backward stages (bit mask): per-row terms + accumulator zeroing, the main
 // dK/dV/dQ kernel, and the dq conversion.
 constexpr int kBwdPrepare = 1, kBwdMain = 2, kBwdFinish = 4;
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const AttnDims& d, const void* plan,
-                       const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                       const void* out, const void* out_lo, const float* lse, const void* dout,
+                       void* dq, void* dk,
                        void* dv, void* workspace, int32_t* status, int stages, int num_sms,
                        cudaStream_t stream);
 

@@ -51,8 +51,9 @@ def gpu_forward_backward(q, k, v, do, doc_ids, seq_start=0, scale=None, enable_g
         enable_gqa = q.shape[1] != k.shape[1]
     seg, sid, nseg = A.segment_cu_seqlens(doc_ids)
     plan = A.make_plan(seg, sid, nseg, q.shape[1], k.shape[1], q.shape[2], seq_start)
-    out, lse = A.attn_forward(q, k, v, plan, seq_start, scale, enable_gqa)
-    dq, dk, dv = A.attn_backward(q, k, v, out, lse, do, plan, seq_start, scale, enable_gqa)
+    out, lse, out_lo = A.attn_forward(q, k, v, plan, seq_start, scale, enable_gqa)
+    dq, dk, dv = A.attn_backward(q, k, v, out, lse, do, plan, seq_start, scale, enable_gqa,
+                                 out_lo=out_lo)
     A.check_device_status(q.device)
     return out, lse, dq, dk, dv
 

@@ -59,12 +59,12 @@ FAKE = 1 << 20  # a non-null, 256-aligned dummy address: never dereferenced on t
 
 def _fwd(lib, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, B=1, Hq=4, Hkv=2, L=256, S=256, D=64, seq_start=0,
-             scale=0.0, gqa=1, plan=FAKE, plan_bytes=1 << 30, out=FAKE, lse=FAKE, st=None,
-             stream=None)
+             scale=0.0, gqa=1, plan=FAKE, plan_bytes=1 << 30, out=FAKE, lse=FAKE, lo=None,
+             st=None, stream=None)
     a.update(kw)
     return lib.bd_attn_fwd(a["q"], a["k"], a["v"], a["B"], a["Hq"], a["Hkv"], a["L"], a["S"],
                          a["D"], a["seq_start"], a["scale"], a["gqa"], a["plan"], a["plan_bytes"],
-                         a["out"], a["lse"], a["st"], a["stream"])
+                         a["out"], a["lse"], a["lo"], a["st"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -79,6 +79,7 @@ def _fwd(lib, **kw):
     (dict(q=FAKE + 8), 1),
     (dict(plan=FAKE + 16), 1),
     (dict(plan_bytes=16), 5),
+    (dict(lo=FAKE + 2), 1),
 ])
 def test_fwd_rejects_bad_arguments(lib_, kw, code):
     assert _fwd(lib_, **kw) == code
@@ -86,16 +87,19 @@ def test_fwd_rejects_bad_arguments(lib_, kw, code):
 
 def test_bwd_and_plan_reject_bad_arguments(lib_):
     f = lib_.bd_attn_bwd
-    args = [FAKE] * 6 + [1, 4, 2, 256, 256, 64, 0, 0.0, 1, FAKE, 1 << 30, FAKE, FAKE, FAKE,
+    args = [FAKE] * 7 + [1, 4, 2, 256, 256, 64, 0, 0.0, 1, FAKE, 1 << 30, FAKE, FAKE, FAKE,
                          FAKE, 1 << 30, None, None]
     bad = list(args)
-    bad[11] = 100  # D
+    bad[12] = 100  # D
     assert f(*bad) == 2
     bad = list(args)
-    bad[21] = 8  # workspace too small
+    bad[22] = 8  # workspace too small
     assert f(*bad) == 5
     bad = list(args)
-    bad[19] = FAKE + 4  # misaligned dv
+    bad[20] = FAKE + 4  # misaligned dv
+    assert f(*bad) == 1
+    bad = list(args)
+    bad[4] = FAKE + 2  # misaligned out_lo
     assert f(*bad) == 1
     p = lib_.bd_attn_plan
     assert p(FAKE, FAKE, FAKE, 1, 4, 2, 256, 256, 0, FAKE, 8, None) == 5
