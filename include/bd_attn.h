@@ -99,8 +99,12 @@ int bd_segment_cu_seqlens(const int32_t* doc_ids, int B, int S, int32_t* seg, in
  *                       whether Hq / Hkv is even).
  *   L, seq_start        query rows are global positions seq_start .. +L-1.
  *   plan                device buffer of bd_attn_plan_size() bytes, 256-byte
- *                       aligned; read by bd_attn_fwd / bd_attn_bwd, which must
- *                       be given the same B, Hq, Hkv, L, S, seq_start.
+ *                       aligned, used by bd_attn_fwd / bd_attn_bwd, which must
+ *                       be given the same B, Hq, Hkv, L, S, seq_start.  It also
+ *                       holds the work counters those kernels take units from
+ *                       (longest first) and leave at zero when they finish, so
+ *                       one plan must not serve two launches that overlap in
+ *                       time (use one plan per stream).
  * Returns BD_ERR_UNSUPPORTED when B * ceil(L/128) or B * ceil(S/128)
  * exceeds 16384.
  */
@@ -130,7 +134,7 @@ int bd_attn_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg
  *                Delta is formed from the bf16 output alone.
  */
 int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L, int S,
-                int D, int seq_start, float scale, int enable_gqa, const void* plan,
+                int D, int seq_start, float scale, int enable_gqa, void* plan,
                 size_t plan_bytes, void* out, float* lse, void* out_lo, int32_t* dev_status,
                 bd_stream_t stream);
 
@@ -152,7 +156,7 @@ size_t bd_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int S, int D);
 int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* out_lo,
                 const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S, int D,
                 int seq_start,
-                float scale, int enable_gqa, const void* plan, size_t plan_bytes, void* dq,
+                float scale, int enable_gqa, void* plan, size_t plan_bytes, void* dq,
                 void* dk, void* dv, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                 bd_stream_t stream);
 
@@ -168,7 +172,7 @@ int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
 int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* out,
                        const void* out_lo, const float* lse, const void* dout, int B, int Hq,
                        int Hkv, int L, int S,
-                       int D, int seq_start, float scale, int enable_gqa, const void* plan,
+                       int D, int seq_start, float scale, int enable_gqa, void* plan,
                        size_t plan_bytes, void* dq, void* dk, void* dv, void* workspace,
                        size_t workspace_bytes, int32_t* dev_status, int stages,
                        bd_stream_t stream);

@@ -149,7 +149,7 @@ int bd_attn_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg
 }
 
 int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L, int S,
-                int D, int seq_start, float scale, int enable_gqa, const void* plan,
+                int D, int seq_start, float scale, int enable_gqa, void* plan,
                 size_t plan_bytes, void* out, float* lse, void* out_lo, int32_t* dev_status,
                 bd_stream_t stream) {
   if (q == nullptr || k == nullptr || v == nullptr || plan == nullptr || out == nullptr ||
@@ -186,7 +186,7 @@ size_t bd_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int S, int D) {
 int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* out,
                        const void* out_lo, const float* lse, const void* dout, int B, int Hq,
                        int Hkv, int L, int S,
-                       int D, int seq_start, float scale, int enable_gqa, const void* plan,
+                       int D, int seq_start, float scale, int enable_gqa, void* plan,
                        size_t plan_bytes, void* dq, void* dk, void* dv, void* workspace,
                        size_t workspace_bytes, int32_t* dev_status, int stages,
                        bd_stream_t stream) {
@@ -222,7 +222,7 @@ int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* 
 int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* out_lo,
                 const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S, int D,
                 int seq_start,
-                float scale, int enable_gqa, const void* plan, size_t plan_bytes, void* dq,
+                float scale, int enable_gqa, void* plan, size_t plan_bytes, void* dq,
                 void* dk, void* dv, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                 bd_stream_t stream) {
   return bd_attn_bwd_stages(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,

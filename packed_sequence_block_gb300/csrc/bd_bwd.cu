@@ -35,7 +35,7 @@ struct BwdCfg {
   static constexpr int OFF_DS = OFF_DO + 2 * TILE;    // 128 keys x 128 queries bf16
   static constexpr int OFF_LSED = OFF_DS + 32768;     // [2 stages] 128 x float2
   static constexpr int OFF_BAR = OFF_LSED + 2048;
-  static constexpr int SMEM = OFF_BAR + 256;
+  static constexpr int SMEM = OFF_BAR + 256;  // barriers, TMEM slot, abort flag, work ring
   static constexpr uint32_t IDESC_S = make_idesc_bf16(128, 128, 0, 0);   // S^T, dP^T
   static constexpr uint32_t IDESC_KV = make_idesc_bf16(128, D, 0, 1);    // dV, dK (A in TMEM)
   static constexpr uint32_t IDESC_DQ = make_idesc_bf16(128, D, 1, 1);    // dQ = dS K
@@ -52,6 +52,7 @@ struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int32_t* status;
+  int* ctr;  // work counters in the plan: [next unit, finished CTAs]
 };
 
 struct BUnit {
@@ -162,6 +163,16 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
 }
 
 // ------------------------------------------------------------------ main kernel
+//
+// Per iteration i (query tile x head of the unit's group), TMEM columns:
+//   dK [0,128)  dV [128,256)  S^T -> P^T [256,384)  dP^T -> dS^T -> dQ [384,512)
+// Tensor-core order (one thread):
+//   dV += P^T_i dO_i | S^T_{i+1} | dK += dS^T_i Q_i | dQ_i = dS_i K | dP^T_{i+1}
+// so that the P/dS work of warpgroup 1 overlaps MMAs: dS_i is formed while
+// dV_i and S^T_{i+1} run, P_{i+1} while dK_i, dQ_i and dP^T_{i+1} run.
+// Warpgroup 1 keeps P_i between its two phases as the bf16 values it also
+// hands to the dV MMA (64 registers), and forms dS = P (dP - Delta) in fp32
+// from them; dS is rounded to bf16 for the dK and dQ MMAs in any case.
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -177,13 +188,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* st_full = bars + 2;   // [2]
   uint64_t* st_empty = bars + 4;  // [2]
   uint64_t* s_full = bars + 6;
-  uint64_t* pds_full = bars + 7;
-  uint64_t* dq_full = bars + 8;
-  uint64_t* dq_empty = bars + 9;
-  uint64_t* dkdv_full = bars + 10;
-  uint64_t* drain = bars + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* dp_full = bars + 7;
+  uint64_t* p_full = bars + 8;
+  uint64_t* ds_full = bars + 9;
+  uint64_t* dq_full = bars + 10;
+  uint64_t* dq_empty = bars + 11;
+  uint64_t* dkdv_full = bars + 12;
+  uint64_t* drain = bars + 13;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  WorkRing* ring = reinterpret_cast<WorkRing*>(bars + 16);
+  static_assert(16 * 8 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -200,11 +215,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(st_empty + s, 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(pds_full, 128);
+    mbar_init(dp_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(ds_full, 128);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(dkdv_full, 1);
     mbar_init(drain, 1);
+    ring_init(ring);
     fence_mbar_init();
     prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_k);
@@ -222,10 +240,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool aborted_at_start = *abort_flag != 0;
 
   if (warp == 0 && !aborted_at_start) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer + work queue
     if (lane == 0) {
-      uint32_t kv_u = 0, st_it = 0;
-      for (int w = blockIdx.x; w < p.n_units; w += gridDim.x) {
+      uint32_t kv_u = 0, st_it = 0, kq = 0;
+      for (;;) {
+        int w;
+        if (!ring_publish(ring, kq++, p.ctr, p.n_units, abort_flag, p.status, w) || w < 0) break;
         const BUnit u = decode_bunit(p, w);
         if (u.n_it <= 0) continue;
         if (!mbar_wait(kv_empty, (kv_u & 1) ^ 1, abort_flag, p.status)) break;
@@ -275,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sdo0 = smem_u32(smem + C::OFF_DO);
       const uint32_t sds = smem_u32(smem + C::OFF_DS);
       const uint32_t tDK = tmem, tDV = tmem + 128, tS = tmem + 256, tDP = tmem + 384;
-      // A (K-major, M=128 keys) x B (K-major, N=128 queries), K-dim = D
+      // D[128 keys, 128 queries] = A[keys, D] (K-major) * B[queries, D]^T (K-major)
       auto issue_kmajor = [&](uint32_t d, uint32_t a, uint32_t b) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -284,23 +304,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                  C::IDESC_S, kk > 0);
         }
       };
-      // D[keys, D] (+)= A[tmem, keys x 128 q] * B[q, D] (MN-major smem)
+      // D[keys, D] (+)= A[tmem, keys x 128 queries] * B[queries, D] (MN-major smem)
       auto issue_ts = [&](uint32_t d, uint32_t a_tmem, uint32_t b, bool acc) {
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           mma_ts(d, a_tmem + ks * 8, make_sdesc_sw128(b + ks * 2048, 16384, 1024), C::IDESC_KV,
                  (acc || ks > 0));
       };
-      // dQ[q, D] = dS[q, keys] (MN-major smem) * K[keys, D] (MN-major smem)
+      // dQ[queries, D] = dS[queries, keys] (MN-major smem) * K[keys, D] (MN-major smem)
       auto issue_dq = [&]() {
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          mma_ss(tS, make_sdesc_sw128(sds + ks * 2048, 16384, 1024),
+          mma_ss(tDP, make_sdesc_sw128(sds + ks * 2048, 16384, 1024),
                  make_sdesc_sw128(sk + ks * 2048, 16384, 1024), C::IDESC_DQ, ks > 0);
       };
-      uint32_t kv_u = 0, st_it = 0, it_g = 0;
+      uint32_t kv_u = 0, st_it = 0, it_g = 0, kq = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < p.n_units && ok; w += gridDim.x) {
+      while (ok) {
+        int w;
+        if (!ring_take(ring, kq++, abort_flag, p.status, w) || w < 0) break;
         const BUnit u = decode_bunit(p, w);
         if (u.n_it <= 0) continue;
         ok = mbar_wait(kv_full, kv_u & 1, abort_flag, p.status);
@@ -309,36 +331,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(st_full + st, (st_it >> 1) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
-        issue_kmajor(tDP, sv, sdo0 + st * C::TILE);
-        if (it_g > 0) {
+        issue_kmajor(tS, sk, sq0 + st * C::TILE);
+        mma_commit(s_full);
+        if (it_g > 0) {  // the previous iteration's dQ must have left the dP columns
           ok = mbar_wait(dq_empty, (it_g - 1) & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
         }
-        issue_kmajor(tS, sk, sq0 + st * C::TILE);
-        mma_commit(s_full);
+        issue_kmajor(tDP, sv, sdo0 + st * C::TILE);
+        mma_commit(dp_full);
         for (int i = 0; i < u.n_it && ok; ++i) {
           const uint32_t si = st_it + i;
           st = si & 1;
-          ok = mbar_wait(pds_full, it_g & 1, abort_flag, p.status);
+          const int sn = (si + 1) & 1;
+          const bool more = i + 1 < u.n_it;
+          ok = mbar_wait(p_full, it_g & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
           issue_ts(tDV, tS, sdo0 + st * C::TILE, i > 0);
-          issue_ts(tDK, tDP, sq0 + st * C::TILE, i > 0);
-          mma_commit(st_empty + st);
-          issue_dq();
-          mma_commit(dq_full);
-          if (i + 1 < u.n_it) {
-            const int sn = (si + 1) & 1;
+          if (more) {
             ok = mbar_wait(st_full + sn, ((si + 1) >> 1) & 1, abort_flag, p.status);
-            if (!ok) break;
-            tc_fence_after();
-            issue_kmajor(tDP, sv, sdo0 + sn * C::TILE);
-            ok = mbar_wait(dq_empty, it_g & 1, abort_flag, p.status);
             if (!ok) break;
             tc_fence_after();
             issue_kmajor(tS, sk, sq0 + sn * C::TILE);
             mma_commit(s_full);
+          }
+          ok = mbar_wait(ds_full, it_g & 1, abort_flag, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_ts(tDK, tDP, sq0 + st * C::TILE, i > 0);
+          mma_commit(st_empty + st);
+          issue_dq();
+          mma_commit(dq_full);
+          if (more) {
+            ok = mbar_wait(dq_empty, it_g & 1, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_kmajor(tDP, sv, sdo0 + sn * C::TILE);
+            mma_commit(dp_full);
           }
           ++it_g;
         }
@@ -358,8 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t tS = tmem + lane_off + 256, tDP = tmem + lane_off + 384;
     const uint32_t sds_row = smem_u32(smem + C::OFF_DS) + (r >> 3) * 1024 + (r & 7) * 128;
-    uint32_t st_it = 0, it_g = 0, kv_u = 0;
-    for (int w = blockIdx.x; w < p.n_units; w += gridDim.x) {
+    uint32_t st_it = 0, it_g = 0, kv_u = 0, kq = 0;
+    for (;;) {
+      int w;
+      if (!ring_take_warp(ring, kq++, abort_flag, p.status, w) || w < 0) break;
       const BUnit u = decode_bunit(p, w);
       const int key = u.kt * kBN + r;
       const size_t krow = ((size_t)(u.b * p.Hkv + u.g) * p.S + key) * D;
@@ -380,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < u.n_it; ++i) {
         const int qt = u.qt_lo + i % u.nq;
         const int st = st_it & 1;
+        // ---- phase P: P^T = exp2(S^T * scale * log2 e - lse * log2 e), masked
         ok = mbar_wait_warp(s_full, it_g & 1, abort_flag, p.status);
         if (!ok) break;
         ok = mbar_wait_warp(st_full + st, (st_it >> 1) & 1, abort_flag, p.status);
@@ -393,30 +426,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           cb = min(kend, p.seq_start + p.L) - q0 - 1;
         }
         const bool full = __all_sync(0xffffffffu, ca <= 0 && cb >= kBM - 1);
-        const float2* ld = reinterpret_cast<const float2*>(smem + C::OFF_LSED + st * 1024);
+        const float4* ld4 = reinterpret_cast<const float4*>(smem + C::OFF_LSED + st * 1024);
+        uint32_t pk[64];  // P^T of this key row as bf16 pairs, kept for the dS phase
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t sv[32], dv[32];
-          tmem_ld32x2(tS + c * 32, tDP + c * 32, sv, dv);
-          float pr[32], ds[32];
+          uint32_t sv[32];
+          tmem_ld32(tS + c * 32, sv);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float2 x = ld[c * 32 + e];
-            float pe = fast_exp2(fmaf(__uint_as_float(sv[e]), p.scale_log2, -x.x));
+          for (int e = 0; e < 32; e += 2) {
+            const float4 x = ld4[(c * 32 + e) >> 1];  // (lse2, delta) of two columns
+            float p0 = fast_exp2(fmaf(__uint_as_float(sv[e]), p.scale_log2, -x.x));
+            float p1 = fast_exp2(fmaf(__uint_as_float(sv[e + 1]), p.scale_log2, -x.z));
             if (!full) {
               const int col = c * 32 + e;
-              pe = (col >= ca && col <= cb) ? pe : 0.f;
+              p0 = (col >= ca && col <= cb) ? p0 : 0.f;
+              p1 = (col + 1 >= ca && col + 1 <= cb) ? p1 : 0.f;
             }
-            pr[e] = pe;
-            ds[e] = pe * (__uint_as_float(dv[e]) - x.y);
+            pk[c * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
           }
-          uint32_t pk[16], dk[16];
+          uint32_t tmp[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            pk[e] = pack_bf16x2(pr[2 * e], pr[2 * e + 1]);
-            dk[e] = pack_bf16x2(ds[2 * e], ds[2 * e + 1]);
+          for (int e = 0; e < 16; ++e) tmp[e] = pk[c * 16 + e];
+          tmem_st16(tS + c * 16, tmp);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full);
+        // ---- phase dS: dS = P * (dP - Delta) -> TMEM (for dK) and smem (for dQ)
+        ok = mbar_wait_warp(dp_full, it_g & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t dv[32];
+          tmem_ld32(tDP + c * 32, dv);
+          uint32_t dk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float4 x = ld4[(c * 32 + e) >> 1];
+            const uint32_t pw = pk[c * 16 + (e >> 1)];
+            const float p0 = __uint_as_float(pw << 16), p1 = __uint_as_float(pw & 0xffff0000u);
+            dk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[e]) - x.y),
+                                     p1 * (__uint_as_float(dv[e + 1]) - x.w));
           }
-          tmem_st16(tS + c * 16, pk);
           tmem_st16(tDP + c * 16, dk);
           // dS (queries contiguous) into the MN-major, 128-byte-swizzled A tile of dQ = dS K
 #pragma unroll
@@ -429,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         fence_async_smem();
         tc_fence_before();
-        mbar_arrive(pds_full);
+        mbar_arrive(ds_full);
         ++st_it;
         ++it_g;
       }
@@ -468,9 +520,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ dQ warpgroup
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;  // query row of the tile = TMEM lane
-    const uint32_t tQ = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + 256;
-    uint32_t it_g = 0;
-    for (int w = blockIdx.x; w < p.n_units; w += gridDim.x) {
+    const uint32_t tQ = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + 384;
+    uint32_t it_g = 0, kq = 0;
+    for (;;) {
+      int w;
+      if (!ring_take_warp(ring, kq++, abort_flag, p.status, w) || w < 0) break;
       const BUnit u = decode_bunit(p, w);
       bool ok = true;
       for (int i = 0; i < u.n_it; ++i) {
@@ -479,24 +533,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait_warp(dq_full, it_g & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
-        uint32_t v[D];
+        float* dst = p.dqacc + ((size_t)(u.b * p.Hq + h) * p.L + row) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t t[32];
           tmem_ld32(tQ + c * 32, t);
+          if (row < p.L) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[c * 32 + e] = t[e];
+            for (int j = 0; j < 8; ++j)
+              red_add_v4(dst + c * 32 + 4 * j, __uint_as_float(t[4 * j]),
+                         __uint_as_float(t[4 * j + 1]), __uint_as_float(t[4 * j + 2]),
+                         __uint_as_float(t[4 * j + 3]));
+          }
         }
         tc_fence_before();
-        mbar_arrive(dq_empty);  // TMEM columns free again; the adds below run from registers
+        mbar_arrive(dq_empty);
         ++it_g;
-        if (row < p.L) {
-          float* dst = p.dqacc + ((size_t)(u.b * p.Hq + h) * p.L + row) * D;
-#pragma unroll
-          for (int j = 0; j < D / 4; ++j)
-            red_add_v4(dst + 4 * j, __uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                       __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-        }
       }
       if (!ok) break;
     }
@@ -508,6 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (threadIdx.x == 0) ring_retire(p.ctr);
 }
 
 template <int D>
@@ -552,14 +605,14 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
 }
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const AttnDims& d, const void* plan,
+                       const CUtensorMap& tdo, const AttnDims& d, void* plan,
                        const void* out, const void* out_lo, const float* lse, const void* dout,
                        void* dq, void* dk,
                        void* dv, void* workspace, int32_t* status, int stages, int num_sms,
                        cudaStream_t stream) {
   const PlanLayout pl = plan_layout(d.B, d.Hq, d.Hkv, d.L, d.S);
   const BwdLayout wl = bwd_layout(d.B, d.Hq, d.L, d.D);
-  const char* base = static_cast<const char*>(plan);
+  char* base = static_cast<char*>(plan);
   char* ws = static_cast<char*>(workspace);
   BwdParams p{};
   p.B = d.B;
@@ -583,6 +636,7 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.status = status;
+  p.ctr = reinterpret_cast<int*>(base + pl.sched) + 2;
   if (d.D == 64) return launch_bwd_t<64>(tq, tk, tv, tdo, p, out, out_lo, lse, dout, dq, stages, num_sms,
                                           stream);
   return launch_bwd_t<128>(tq, tk, tv, tdo, p, out, out_lo, lse, dout, dq, stages, num_sms,

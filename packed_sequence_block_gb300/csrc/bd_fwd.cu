@@ -49,6 +49,7 @@ struct FwdParams {
   __nv_bfloat16* out_lo;  // optional: bf16(O - bf16(O)), the rounding residual of out
   float* lse;
   int32_t* status;
+  int* ctr;  // work counters in the plan: [next unit, finished CTAs]
 };
 
 struct Unit {
@@ -112,6 +113,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = o_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  WorkRing* ring = reinterpret_cast<WorkRing*>(smem + C::OFF_BAR + 256);
+  static_assert(256 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -135,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(o_full + s, 1);
     }
     mbar_init(drain, 1);
+    ring_init(ring);
     fence_mbar_init();
     prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_k);
@@ -153,9 +157,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && !aborted_at_start) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t k_it = 0, v_it = 0, u_it = 0;
+      uint32_t k_it = 0, v_it = 0, u_it = 0, kq = 0;
       bool q_issued = false;
-      for (int w = blockIdx.x; w < p.n_units; w += gridDim.x) {
+      for (;;) {
+        int w;
+        if (!ring_publish(ring, kq++, p.ctr, p.n_units, abort_flag, p.status, w) || w < 0) break;
         const Unit u = decode_unit(p, w);
         if (u.n <= 0) continue;
         if (!mbar_wait(q_empty, (u_it & 1) ^ 1, abort_flag, p.status)) break;
@@ -227,9 +233,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                  make_sdesc_sw128(va + ks * 2048, 16384, 1024), C::IDESC_PV, (acc || ks > 0));
         }
       };
-      uint32_t kv_it = 0, u_it = 0, t_it = 0;
+      uint32_t kv_it = 0, u_it = 0, t_it = 0, kq = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < p.n_units && ok; w += gridDim.x) {
+      while (ok) {
+        int w;
+        if (!ring_take(ring, kq++, abort_flag, p.status, w) || w < 0) break;
         const Unit u = decode_unit(p, w);
         if (u.n <= 0) continue;
         ok = mbar_wait(q_full, u_it & 1, abort_flag, p.status);
@@ -287,8 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     const uint32_t tS = tmem + lane_off + wg * 128;
     const uint32_t tO = tmem + lane_off + 256 + wg * 128;
-    uint32_t t_it = 0, o_it = 0;
-    for (int w = blockIdx.x; w < p.n_units; w += gridDim.x) {
+    uint32_t t_it = 0, o_it = 0, kq = 0;
+    for (;;) {
+      int w;
+      if (!ring_take_warp(ring, kq++, abort_flag, p.status, w) || w < 0) break;
       const Unit u = decode_unit(p, w);
       const int h = wg ? u.h1 : u.h0;
       const int qt = wg ? u.qt1 : u.qt0;
@@ -446,6 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (threadIdx.x == 0) ring_retire(p.ctr);
 }
 
 template <int D>
@@ -469,10 +480,10 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
 }
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const AttnDims& d, const void* plan, void* out, void* out_lo,
+                       const AttnDims& d, void* plan, void* out, void* out_lo,
                        float* lse, int32_t* status, int num_sms, cudaStream_t stream) {
   const PlanLayout pl = plan_layout(d.B, d.Hq, d.Hkv, d.L, d.S);
-  const char* base = static_cast<const char*>(plan);
+  char* base = static_cast<char*>(plan);
   FwdParams p{};
   p.B = d.B;
   p.Hq = d.Hq;
@@ -494,6 +505,7 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.out_lo = static_cast<__nv_bfloat16*>(out_lo);
   p.lse = lse;
   p.status = status;
+  p.ctr = reinterpret_cast<int*>(base + pl.sched);
   if (d.D == 64) return launch_fwd_t<64>(tq, tk, tv, p, num_sms, stream);
   return launch_fwd_t<128>(tq, tk, tv, p, num_sms, stream);
 }

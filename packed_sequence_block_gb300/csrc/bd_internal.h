@@ -37,12 +37,15 @@ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 //   bwd_range int32 [B*NKT, 2] query-tile range [lo, hi] of each key tile
 //   fwd_order int32 [B*NQB]    query blocks sorted by cost, longest first
 //   bwd_order int32 [B*NKT]    key tiles sorted by cost, longest first
+//   sched     int32 [8]        work counters: [0..1] forward, [2..3] backward
+//                              (next unit, finished CTAs); zeroed by the
+//                              planner, reset by the last CTA of each launch
 // A forward query block is 128 rows when Hq/Hkv is even (its two halves are
 // two heads of one group) and 256 rows when it is odd (two consecutive
 // 128-row tiles of one head).
 struct PlanLayout {
   int NQB, NKT, QROWS, Lpad, Spad;
-  size_t qlo, kend, fwd_range, bwd_range, fwd_order, bwd_order, total;
+  size_t qlo, kend, fwd_range, bwd_range, fwd_order, bwd_order, sched, total;
 };
 
 inline PlanLayout plan_layout(int B, int Hq, int Hkv, int L, int S) {
@@ -60,6 +63,7 @@ inline PlanLayout plan_layout(int B, int Hq, int Hkv, int L, int S) {
   p.bwd_range = off; off = align256(off + sizeof(int32_t) * 2 * (size_t)B * p.NKT);
   p.fwd_order = off; off = align256(off + sizeof(int32_t) * (size_t)B * p.NQB);
   p.bwd_order = off; off = align256(off + sizeof(int32_t) * (size_t)B * p.NKT);
+  p.sched = off;     off = align256(off + sizeof(int32_t) * 8);
   p.total = off;
   return p;
 }
@@ -102,14 +106,14 @@ cudaError_t launch_plan(const int32_t* seg, const int32_t* seg_ids, const int32_
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int planes, int rows, int D);
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const AttnDims& d, const void* plan, void* out, void* out_lo,
+                       const AttnDims& d, void* plan, void* out, void* out_lo,
                        float* lse, int32_t* status, int num_sms, cudaStream_t stream);
 // Backward stages (bit mask): per-row terms + accumulator zeroing, the main
 // dK/dV/dQ kernel, and the dq conversion.
 constexpr int kBwdPrepare = 1, kBwdMain = 2, kBwdFinish = 4;
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const AttnDims& d, const void* plan,
+                       const CUtensorMap& tdo, const AttnDims& d, void* plan,
                        const void* out, const void* out_lo, const float* lse, const void* dout,
                        void* dq, void* dk,
                        void* dv, void* workspace, int32_t* status, int stages, int num_sms,

@@ -28,9 +28,11 @@ __global__ void __launch_bounds__(256) plan_rows_kernel(const int32_t* __restric
                                                         const int32_t* __restrict__ nseg, int L,
                                                         int S, int seq_start, int Lpad, int Spad,
                                                         int32_t* __restrict__ qlo,
-                                                        int32_t* __restrict__ kend) {
+                                                        int32_t* __restrict__ kend,
+                                                        int32_t* __restrict__ sched) {
   const int b = blockIdx.y;
   const int x = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b == 0 && x < 8) sched[x] = 0;
   const int32_t* seg = seg_all + (size_t)b * (S + 1);
   const int32_t* sid = seg_ids_all + (size_t)b * S;
   const int n = nseg[b];
@@ -172,10 +174,11 @@ cudaError_t launch_plan(const int32_t* seg, const int32_t* seg_ids, const int32_
   int32_t* br = reinterpret_cast<int32_t*>(base + pl.bwd_range);
   int32_t* fo = reinterpret_cast<int32_t*>(base + pl.fwd_order);
   int32_t* bo = reinterpret_cast<int32_t*>(base + pl.bwd_order);
+  int32_t* sc = reinterpret_cast<int32_t*>(base + pl.sched);
 
   dim3 g1(cdiv(max(pl.Lpad, pl.Spad), 256), B);
   plan_rows_kernel<<<g1, 256, 0, stream>>>(seg, seg_ids, nseg, L, S, seq_start, pl.Lpad, pl.Spad,
-                                           qlo, kend);
+                                           qlo, kend, sc);
   const int warps = B * pl.NQB + B * pl.NKT;
   plan_tiles_kernel<<<cdiv(warps * 32, 256), 256, 0, stream>>>(
       qlo, kend, B, L, seq_start, pl.NQB, pl.QROWS, pl.Lpad, pl.NKT, pl.Spad, fr, br);

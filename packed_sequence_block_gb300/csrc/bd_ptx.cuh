@@ -284,3 +284,77 @@ __device__ __forceinline__ void red_add_v4(float* gaddr, float a, float b, float
 }
 
 }  // namespace bd
+
+// ------------------------------------------------------------------ work queue
+//
+// Persistent kernels take work units from a global counter (longest units
+// first, because the lists are sorted that way) instead of a fixed stride, so
+// an SM that finishes early takes the next unit.  One thread per CTA (the TMA
+// producer) fetches; the index reaches the other roles through a small ring in
+// shared memory guarded by mbarriers.  counters[0] is the next unit,
+// counters[1] counts CTAs that finished; the last CTA resets both so the next
+// launch on the same plan starts from zero.
+
+namespace bd {
+
+constexpr int kRing = 4;
+// consumers of each ring slot: the MMA thread plus eight consumer warps (lane 0 each)
+constexpr int kRingConsumers = 9;
+
+struct WorkRing {
+  int idx[kRing];
+  uint64_t full[kRing];
+  uint64_t empty[kRing];
+};
+
+__device__ __forceinline__ void ring_init(WorkRing* r) {
+  for (int s = 0; s < kRing; ++s) {
+    mbar_init(&r->full[s], 1);
+    mbar_init(&r->empty[s], kRingConsumers);
+  }
+}
+
+// Producer: fetch this CTA's k-th unit and publish it (-1 = no more work).
+__device__ __forceinline__ bool ring_publish(WorkRing* r, uint32_t k, int* counters, int n_units,
+                                             volatile int* abort, int32_t* status, int& w) {
+  const int slot = k % kRing;
+  if (!mbar_wait(&r->empty[slot], ((k / kRing) & 1) ^ 1, abort, status)) return false;
+  w = atomicAdd(&counters[0], 1);
+  if (w >= n_units) w = -1;
+  *reinterpret_cast<volatile int*>(&r->idx[slot]) = w;
+  mbar_arrive(&r->full[slot]);
+  return true;
+}
+
+// Single-thread consumer.
+__device__ __forceinline__ bool ring_take(WorkRing* r, uint32_t k, volatile int* abort,
+                                          int32_t* status, int& w) {
+  const int slot = k % kRing;
+  if (!mbar_wait(&r->full[slot], (k / kRing) & 1, abort, status)) return false;
+  w = *reinterpret_cast<volatile int*>(&r->idx[slot]);
+  mbar_arrive(&r->empty[slot]);
+  return true;
+}
+
+// Whole-warp consumer: every lane gets the index, lane 0 releases the slot.
+__device__ __forceinline__ bool ring_take_warp(WorkRing* r, uint32_t k, volatile int* abort,
+                                               int32_t* status, int& w) {
+  const int slot = k % kRing;
+  if (!mbar_wait_warp(&r->full[slot], (k / kRing) & 1, abort, status)) return false;
+  w = *reinterpret_cast<volatile int*>(&r->idx[slot]);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&r->empty[slot]);
+  return true;
+}
+
+// Called by one thread per CTA after the CTA's last fetch (behind __syncthreads).
+__device__ __forceinline__ void ring_retire(int* counters) {
+  __threadfence();
+  if (atomicAdd(&counters[1], 1) == static_cast<int>(gridDim.x) - 1) {
+    __threadfence();
+    atomicExch(&counters[0], 0);
+    atomicExch(&counters[1], 0);
+  }
+}
+
+}  // namespace bd
