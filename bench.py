@@ -189,17 +189,20 @@ class HotPath:
                           self.status)
             args = (self.q_iv[i], self.k, self.v, self.out[i], self.lse[i], self.do_iv[i], B, Hq,
                     Hkv, L, S, D, s0, self.scale, self.gqa, self.plans[i], self.dq[i], self.dk,
-                    self.dv, self.ws, self.status)
-            N.bd_attn_bwd_stages(*args, out_lo=self.out_lo[i], stages=1)
+                    self.dv, self.ws)
+            N.bd_attn_bwd_stages(*args, out_lo=self.out_lo[i], dev_status=self.status,
+                                 stages=1)
             if time_main:
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record()
-            N.bd_attn_bwd_stages(*args, out_lo=self.out_lo[i], stages=2)
+            N.bd_attn_bwd_stages(*args, out_lo=self.out_lo[i], dev_status=self.status,
+                                 stages=2)
             if time_main:
                 e1.record()
                 self.main_events.append((e0, e1))
-            N.bd_attn_bwd_stages(*args, out_lo=self.out_lo[i], stages=4)
+            N.bd_attn_bwd_stages(*args, out_lo=self.out_lo[i], dev_status=self.status,
+                                 stages=4)
 
     def e2e_buffers(self):
         """Pinned host copies of the inputs and room for the results."""

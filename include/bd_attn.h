@@ -127,6 +127,9 @@ int bd_attn_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg
  *   out          bf16 [B, Hq, L, D] output.
  *   lse          fp32 [B, Hq, L] output: natural-log log-sum-exp of the
  *                scaled scores of each row (-inf for padding rows).
+ *                The P V product runs with fp16 operands (each v tile is
+ *                converted from bf16 in shared memory, exact for |x| in
+ *                [2^-14, 65504], so v must stay within the fp16 range).
  *   out_lo       optional bf16 [B, Hq, L, D] output (NULL to skip): the
  *                rounding residual bf16(O - out) of the fp32 result O, so
  *                that out + out_lo carries O to about 16 significant bits.
@@ -151,6 +154,11 @@ int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int 
  *                256-byte aligned (fp32 dq accumulator and per-row terms).
  * The dq accumulation uses floating-point atomics, so dq may differ in the
  * last bits between runs; dk and dv are deterministic.
+ * The products that involve dS = P (dP - Delta) or form S (K Q^T, dS^T Q,
+ * dS K) run with fp16 operands: q and k tiles are converted from bf16 in
+ * shared memory (exact for |x| in [2^-14, 65504]; larger values become inf,
+ * so q and k must stay within the fp16 range), which keeps 11 significant
+ * bits of dS instead of bf16's 8.
  */
 size_t bd_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int S, int D);
 int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* out_lo,

@@ -36,9 +36,15 @@ struct BwdCfg {
   static constexpr int OFF_LSED = OFF_DS + 32768;     // [2 stages] 128 x float2
   static constexpr int OFF_BAR = OFF_LSED + 2048;
   static constexpr int SMEM = OFF_BAR + 256;  // barriers, TMEM slot, abort flag, work ring
-  static constexpr uint32_t IDESC_S = make_idesc_bf16(128, 128, 0, 0);   // S^T, dP^T
-  static constexpr uint32_t IDESC_KV = make_idesc_bf16(128, D, 0, 1);    // dV, dK (A in TMEM)
-  static constexpr uint32_t IDESC_DQ = make_idesc_bf16(128, D, 1, 1);    // dQ = dS K
+  // K and Q tiles are converted to fp16 in shared memory, and dS is produced in
+  // fp16, so the three products that carry dS or feed it (S^T = K Q^T,
+  // dK += dS^T Q, dQ = dS K) run with fp16 operands: 11 significant bits for
+  // dS instead of 8.  dP^T = V dO^T and dV += P^T dO stay bf16.
+  static constexpr uint32_t IDESC_S = make_idesc(128, 128, 0, 0, 0);   // S^T = K Q^T (fp16)
+  static constexpr uint32_t IDESC_DP = make_idesc(128, 128, 0, 0, 1);  // dP^T = V dO^T (bf16)
+  static constexpr uint32_t IDESC_DV = make_idesc(128, D, 0, 1, 1);    // dV += P^T dO (bf16)
+  static constexpr uint32_t IDESC_DK = make_idesc(128, D, 0, 1, 0);    // dK += dS^T Q (fp16)
+  static constexpr uint32_t IDESC_DQ = make_idesc(128, D, 1, 1, 0);    // dQ = dS K (fp16)
 };
 
 struct BwdParams {
@@ -170,9 +176,8 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
 //   dV += P^T_i dO_i | S^T_{i+1} | dK += dS^T_i Q_i | dQ_i = dS_i K | dP^T_{i+1}
 // so that the P/dS work of warpgroup 1 overlaps MMAs: dS_i is formed while
 // dV_i and S^T_{i+1} run, P_{i+1} while dK_i, dQ_i and dP^T_{i+1} run.
-// Warpgroup 1 keeps P_i between its two phases as the bf16 values it also
-// hands to the dV MMA (64 registers), and forms dS = P (dP - Delta) in fp32
-// from them; dS is rounded to bf16 for the dK and dQ MMAs in any case.
+// Warpgroup 1 keeps P_i between its two phases as the bf16 pairs it hands to
+// the dV MMA (64 registers) and forms dS = P (dP - Delta) in fp32 from them.
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -195,10 +200,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dq_empty = bars + 11;
   uint64_t* dkdv_full = bars + 12;
   uint64_t* drain = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  uint64_t* k16_ready = bars + 14;  // K tile converted to fp16
+  uint64_t* q16_ready = bars + 15;  // [2] Q tile of the stage converted to fp16
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  WorkRing* ring = reinterpret_cast<WorkRing*>(bars + 16);
-  static_assert(16 * 8 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
+  WorkRing* ring = reinterpret_cast<WorkRing*>(bars + 18);
+  static_assert(18 * 8 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -222,7 +229,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dq_empty, 128);
     mbar_init(dkdv_full, 1);
     mbar_init(drain, 1);
-    ring_init(ring);
+    mbar_init(k16_ready, 64);
+    mbar_init(q16_ready + 0, 64);
+    mbar_init(q16_ready + 1, 64);
+    ring_init(ring, 11);  // MMA thread + converter, P/dS and dQ warps
     fence_mbar_init();
     prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_k);
@@ -296,19 +306,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sds = smem_u32(smem + C::OFF_DS);
       const uint32_t tDK = tmem, tDV = tmem + 128, tS = tmem + 256, tDP = tmem + 384;
       // D[128 keys, 128 queries] = A[keys, D] (K-major) * B[queries, D]^T (K-major)
-      auto issue_kmajor = [&](uint32_t d, uint32_t a, uint32_t b) {
+      auto issue_kmajor = [&](uint32_t d, uint32_t a, uint32_t b, uint32_t idesc) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_ss(d, make_sdesc_sw128(a + off, 16, 1024), make_sdesc_sw128(b + off, 16, 1024),
-                 C::IDESC_S, kk > 0);
+                 idesc, kk > 0);
         }
       };
       // D[keys, D] (+)= A[tmem, keys x 128 queries] * B[queries, D] (MN-major smem)
-      auto issue_ts = [&](uint32_t d, uint32_t a_tmem, uint32_t b, bool acc) {
+      auto issue_ts = [&](uint32_t d, uint32_t a_tmem, uint32_t b, bool acc, uint32_t idesc) {
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          mma_ts(d, a_tmem + ks * 8, make_sdesc_sw128(b + ks * 2048, 16384, 1024), C::IDESC_KV,
+          mma_ts(d, a_tmem + ks * 8, make_sdesc_sw128(b + ks * 2048, 16384, 1024), idesc,
                  (acc || ks > 0));
       };
       // dQ[queries, D] = dS[queries, keys] (MN-major smem) * K[keys, D] (MN-major smem)
@@ -325,20 +335,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ring_take(ring, kq++, abort_flag, p.status, w) || w < 0) break;
         const BUnit u = decode_bunit(p, w);
         if (u.n_it <= 0) continue;
-        ok = mbar_wait(kv_full, kv_u & 1, abort_flag, p.status);
+        ok = mbar_wait(k16_ready, kv_u & 1, abort_flag, p.status);  // implies kv_full
         if (!ok) break;
         int st = st_it & 1;
-        ok = mbar_wait(st_full + st, (st_it >> 1) & 1, abort_flag, p.status);
+        ok = mbar_wait(q16_ready + st, (st_it >> 1) & 1, abort_flag, p.status);  // implies st_full
         if (!ok) break;
         tc_fence_after();
-        issue_kmajor(tS, sk, sq0 + st * C::TILE);
+        issue_kmajor(tS, sk, sq0 + st * C::TILE, C::IDESC_S);
         mma_commit(s_full);
         if (it_g > 0) {  // the previous iteration's dQ must have left the dP columns
           ok = mbar_wait(dq_empty, (it_g - 1) & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
         }
-        issue_kmajor(tDP, sv, sdo0 + st * C::TILE);
+        issue_kmajor(tDP, sv, sdo0 + st * C::TILE, C::IDESC_DP);
         mma_commit(dp_full);
         for (int i = 0; i < u.n_it && ok; ++i) {
           const uint32_t si = st_it + i;
@@ -348,18 +358,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(p_full, it_g & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
-          issue_ts(tDV, tS, sdo0 + st * C::TILE, i > 0);
+          issue_ts(tDV, tS, sdo0 + st * C::TILE, i > 0, C::IDESC_DV);
           if (more) {
-            ok = mbar_wait(st_full + sn, ((si + 1) >> 1) & 1, abort_flag, p.status);
+            ok = mbar_wait(q16_ready + sn, ((si + 1) >> 1) & 1, abort_flag, p.status);
             if (!ok) break;
             tc_fence_after();
-            issue_kmajor(tS, sk, sq0 + sn * C::TILE);
+            issue_kmajor(tS, sk, sq0 + sn * C::TILE, C::IDESC_S);
             mma_commit(s_full);
           }
           ok = mbar_wait(ds_full, it_g & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
-          issue_ts(tDK, tDP, sq0 + st * C::TILE, i > 0);
+          issue_ts(tDK, tDP, sq0 + st * C::TILE, i > 0, C::IDESC_DK);
           mma_commit(st_empty + st);
           issue_dq();
           mma_commit(dq_full);
@@ -367,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(dq_empty, it_g & 1, abort_flag, p.status);
             if (!ok) break;
             tc_fence_after();
-            issue_kmajor(tDP, sv, sdo0 + sn * C::TILE);
+            issue_kmajor(tDP, sv, sdo0 + sn * C::TILE, C::IDESC_DP);
             mma_commit(dp_full);
           }
           ++it_g;
@@ -381,6 +391,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(drain, 0, p.status);
     }
     __syncwarp();
+  } else if ((warp == 2 || warp == 3) && !aborted_at_start) {
+    // ------------------------------------------------------------ bf16 -> fp16 converters
+    // K (once per unit) and each Q tile are rewritten in place, element by
+    // element, so the swizzled layout the descriptors describe is unchanged.
+    const int t = threadIdx.x - 64;  // 0..63
+    auto convert = [&](uint8_t* tile) {
+      const uint32_t base = smem_u32(tile);
+#pragma unroll 4
+      for (int c = t; c < C::TILE / 16; c += 64) {
+        uint32_t a, b, cc, d;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(a), "=r"(b), "=r"(cc), "=r"(d)
+                     : "r"(base + c * 16));
+        st_shared_v4(base + c * 16, bf16x2_to_f16x2(a), bf16x2_to_f16x2(b),
+                     bf16x2_to_f16x2(cc), bf16x2_to_f16x2(d));
+      }
+      fence_async_smem();
+    };
+    uint32_t kv_u = 0, st_it = 0, kq = 0;
+    for (;;) {
+      int w;
+      if (!ring_take_warp(ring, kq++, abort_flag, p.status, w) || w < 0) break;
+      const BUnit u = decode_bunit(p, w);
+      if (u.n_it <= 0) continue;
+      if (!mbar_wait_warp(kv_full, kv_u & 1, abort_flag, p.status)) break;
+      convert(smem + C::OFF_K);
+      mbar_arrive(k16_ready);
+      ++kv_u;
+      bool ok = true;
+      for (int i = 0; i < u.n_it; ++i) {
+        const int st = st_it & 1;
+        ok = mbar_wait_warp(st_full + st, (st_it >> 1) & 1, abort_flag, p.status);
+        if (!ok) break;
+        convert(smem + C::OFF_Q + st * C::TILE);
+        mbar_arrive(q16_ready + st);
+        ++st_it;
+      }
+      if (!ok) break;
+    }
   } else if (warp >= 4 && warp < 8 && !aborted_at_start) {
     // ------------------------------------------------------------ P / dS warpgroup
     const int q4 = warp & 3;
@@ -427,10 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const bool full = __all_sync(0xffffffffu, ca <= 0 && cb >= kBM - 1);
         const float4* ld4 = reinterpret_cast<const float4*>(smem + C::OFF_LSED + st * 1024);
-        uint32_t pk[64];  // P^T of this key row as bf16 pairs, kept for the dS phase
+        uint32_t pk[64];  // P^T of this key row as bf16 pairs (the dV MMA's operand), kept for dS
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t sv[32];
+          uint32_t sv[32], tmp[16];
           tmem_ld32(tS + c * 32, sv);
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
@@ -444,7 +493,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             pk[c * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
           }
-          uint32_t tmp[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) tmp[e] = pk[c * 16 + e];
           tmem_st16(tS + c * 16, tmp);
@@ -466,8 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float4 x = ld4[(c * 32 + e) >> 1];
             const uint32_t pw = pk[c * 16 + (e >> 1)];
             const float p0 = __uint_as_float(pw << 16), p1 = __uint_as_float(pw & 0xffff0000u);
-            dk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[e]) - x.y),
-                                     p1 * (__uint_as_float(dv[e + 1]) - x.w));
+            dk[e >> 1] = pack_f16x2(p0 * (__uint_as_float(dv[e]) - x.y),
+                                    p1 * (__uint_as_float(dv[e + 1]) - x.w));
           }
           tmem_st16(tDP + c * 16, dk);
           // dS (queries contiguous) into the MN-major, 128-byte-swizzled A tile of dQ = dS K

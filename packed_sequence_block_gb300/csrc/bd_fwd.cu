@@ -10,7 +10,8 @@
 //  * warp 0 streams Q and K/V tiles with TMA (128-byte swizzle) into shared
 //    memory; only the key tiles the plan marks non-empty are loaded;
 //  * warp 1 (one thread) issues tcgen05 MMAs: S_s = Q_s K^T into TMEM, then
-//    O_s += P_s V with P_s read back from TMEM;
+//    O_s += P_s V with P_s read back from TMEM (fp16; warps 2-3 convert each
+//    V tile to fp16 in shared memory as it lands);
 //  * warpgroups 1 and 2 run the softmax of sub-tile 0 and 1 (one thread per
 //    query row = one TMEM lane): mask, running max, exp2, bf16 P into TMEM,
 //    lazy rescaling of O, and the epilogue O / l -> bf16 plus the fp32 LSE.
@@ -36,7 +37,10 @@ struct FwdCfg {
   static constexpr int OFF_BAR = OFF_V + STAGES * KTILE;
   static constexpr int SMEM = OFF_BAR + 512;
   static constexpr uint32_t IDESC_S = make_idesc_bf16(128, 128, 0, 0);
-  static constexpr uint32_t IDESC_PV = make_idesc_bf16(128, D, 0, 1);
+  // P V runs with fp16 operands (V tiles converted in shared memory, P <= 2^8
+  // by the rescale threshold): O then carries P to 11 significant bits, and
+  // the backward's Delta = <dO, O> agrees with its own P to that precision.
+  static constexpr uint32_t IDESC_PV = make_idesc(128, D, 0, 1, 0);
 };
 
 struct FwdParams {
@@ -111,7 +115,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 2;                    // [2]
   uint64_t* o_full = p_full + 2;                    // [2]
   uint64_t* drain = o_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* v16_ready = drain + 1;                  // [STAGES] V tile converted to fp16
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(v16_ready + C::STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   WorkRing* ring = reinterpret_cast<WorkRing*>(smem + C::OFF_BAR + 256);
   static_assert(256 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
@@ -138,7 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(o_full + s, 1);
     }
     mbar_init(drain, 1);
-    ring_init(ring);
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(v16_ready + s, 64);
+    ring_init(ring, 11);  // MMA thread + 2 converter warps + 8 softmax warps
     fence_mbar_init();
     prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_k);
@@ -254,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t it = kv_it + jj;
           const int stj = it % C::STAGES;
           mma_commit(k_empty + stj);  // the S MMAs reading K_jj are all issued
-          ok = mbar_wait(v_full + stj, (it / C::STAGES) & 1, abort_flag, p.status);
+          ok = mbar_wait(v16_ready + stj, (it / C::STAGES) & 1, abort_flag, p.status);
           if (!ok) break;
           const bool last = (jj + 1 == u.n);
           const int stn = (it + 1) % C::STAGES;
@@ -287,6 +293,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(drain, 0, p.status);
     }
     __syncwarp();
+  } else if ((warp == 2 || warp == 3) && !aborted_at_start) {
+    // ------------------------------------------------------------ V tiles bf16 -> fp16
+    const int t = threadIdx.x - 64;  // 0..63
+    uint32_t v_it = 0, kq = 0;
+    for (;;) {
+      int w;
+      if (!ring_take_warp(ring, kq++, abort_flag, p.status, w) || w < 0) break;
+      const Unit u = decode_unit(p, w);
+      bool ok = true;
+      for (int jj = 0; jj < u.n; ++jj) {
+        const int st = v_it % C::STAGES;
+        ok = mbar_wait_warp(v_full + st, (v_it / C::STAGES) & 1, abort_flag, p.status);
+        if (!ok) break;
+        const uint32_t base = smem_u32(smem + C::OFF_V + st * C::KTILE);
+#pragma unroll 4
+        for (int c = t; c < C::KTILE / 16; c += 64) {
+          uint32_t a, b, cc, d;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(a), "=r"(b), "=r"(cc), "=r"(d)
+                       : "r"(base + c * 16));
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + c * 16),
+                       "r"(bf16x2_to_f16x2(a)), "r"(bf16x2_to_f16x2(b)),
+                       "r"(bf16x2_to_f16x2(cc)), "r"(bf16x2_to_f16x2(d))
+                       : "memory");
+        }
+        fence_async_smem();
+        mbar_arrive(v16_ready + st);
+        ++v_it;
+      }
+      if (!ok) break;
+    }
   } else if (warp >= 4 && !aborted_at_start) {
     // ------------------------------------------------------------ softmax
     const int wg = (warp - 4) >> 2;  // sub-tile
@@ -402,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pr[2 * e], pr[2 * e + 1]);
+          for (int e = 0; e < 16; ++e) pk[e] = pack_f16x2(pr[2 * e], pr[2 * e + 1]);
           tmem_st16(tS + c * 16, pk);
         }
         tmem_wait_st();

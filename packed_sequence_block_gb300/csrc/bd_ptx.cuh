@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -184,15 +185,20 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
-// a_mn / b_mn select MN-major (1) instead of K-major (0) operands.
-__host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, int a_mn, int b_mn) {
-  return (1u << 4)                            // D format: f32
-         | (1u << 7)                          // A format: bf16
-         | (1u << 10)                         // B format: bf16
-         | (static_cast<uint32_t>(a_mn) << 15)  // A major
-         | (static_cast<uint32_t>(b_mn) << 16)  // B major
+// Instruction descriptor, kind::f16 with fp32 D; A and B are both bf16
+// (bf16 = 1) or both fp16 (bf16 = 0).  a_mn / b_mn select MN-major (1)
+// instead of K-major (0) operands.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, int a_mn, int b_mn, int bf16) {
+  return (1u << 4)                                      // D format: f32
+         | (static_cast<uint32_t>(bf16) << 7)           // A format: f16 (0) / bf16 (1)
+         | (static_cast<uint32_t>(bf16) << 10)          // B format: same as A
+         | (static_cast<uint32_t>(a_mn) << 15)          // A major
+         | (static_cast<uint32_t>(b_mn) << 16)          // B major
          | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, int a_mn, int b_mn) {
+  return make_idesc(M, N, a_mn, b_mn, 1);
 }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
@@ -271,6 +277,27 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Two floats -> packed f16x2 (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Packed f16x2 -> two floats (lo from the low half).
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t w) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w));
+  return make_float2(lo, hi);
+}
+
+// Two bf16 (packed) -> two fp16 (packed); exact for |x| in [2^-14, 65504].
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+
 // Two floats -> packed bf16x2 (lo in the low half), round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -298,8 +325,6 @@ __device__ __forceinline__ void red_add_v4(float* gaddr, float a, float b, float
 namespace bd {
 
 constexpr int kRing = 4;
-// consumers of each ring slot: the MMA thread plus eight consumer warps (lane 0 each)
-constexpr int kRingConsumers = 9;
 
 struct WorkRing {
   int idx[kRing];
@@ -307,10 +332,11 @@ struct WorkRing {
   uint64_t empty[kRing];
 };
 
-__device__ __forceinline__ void ring_init(WorkRing* r) {
+// consumers = threads that release each slot (one per consumer warp, plus the MMA thread)
+__device__ __forceinline__ void ring_init(WorkRing* r, int consumers) {
   for (int s = 0; s < kRing; ++s) {
     mbar_init(&r->full[s], 1);
-    mbar_init(&r->empty[s], kRingConsumers);
+    mbar_init(&r->empty[s], consumers);
   }
 }
 
