@@ -186,6 +186,34 @@ int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* 
                        bd_stream_t stream);
 
 /*
+ * The backward pass without any caller-provided scratch, for callers that
+ * cannot allocate device memory: for example code running inside a host
+ * runtime that reserves all GPU memory when it starts and forbids further
+ * allocation (a cudaMalloc can synchronise the device, stall other work, or
+ * fail once memory is fragmented).  The pages describe no such variant; it
+ * is an addition of this library.
+ *
+ * Same arguments and results as bd_attn_bwd, minus the workspace.  The
+ * scratch is a fixed array of BD_NOALLOC_SCRATCH_BYTES (16 MiB) that the
+ * library image places on every GPU that loads it, held until the process
+ * exits.  Problems whose bd_attn_bwd_workspace_size() exceeds that return
+ * BD_ERR_WORKSPACE before anything is launched.  Nothing is allocated.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture begins.
+ *  - Every call uses the same array and leaves its contents behind; each call
+ *    clears what must start at zero itself.  Calls whose GPU work overlaps in
+ *    time (two streams, or several threads) race on the array and give wrong
+ *    results: serialise them.
+ */
+#define BD_NOALLOC_SCRATCH_BYTES (16u << 20)
+int bd_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
+                        const void* out_lo, const float* lse, const void* dout, int B, int Hq,
+                        int Hkv, int L, int S, int D, int seq_start, float scale, int enable_gqa,
+                        void* plan, size_t plan_bytes, void* dq, void* dk, void* dv,
+                        int32_t* dev_status, bd_stream_t stream);
+
+/*
  * Copy the device status word to *host_status after the work already queued
  * on `stream` finishes (this call synchronises `stream`; no other entry point
  * does).  Returns BD_OK or BD_ERR_CUDA.

@@ -42,8 +42,13 @@ SIGNATURES = {
     "bd_attn_bwd_stages": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size,
                                                                 _vp, _vp, _vp, _vp, _c_size, _vp,
                                                                 _c_int, _vp]),
+    "bd_attn_bwd_noalloc": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size,
+                                                                 _vp, _vp, _vp, _vp, _vp]),
     "bd_get_device_status": (_c_int, [_vp, _vp, _vp]),
 }
+
+# Size of the fixed scratch array bd_attn_bwd_noalloc uses (BD_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lib = None
 
@@ -183,6 +188,27 @@ def bd_attn_bwd_stages(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: in
                                     workspace.numel() * workspace.element_size(),
                                     _ptr(dev_status), int(stages), _stream(stream)),
            "bd_attn_bwd_stages")
+
+
+def bd_attn_bwd_noalloc(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: int,
+                        D: int, seq_start: int, scale: float, enable_gqa: bool, plan, dq, dk, dv,
+                        out_lo=None, dev_status=None, stream=None) -> None:
+    """bd_attn_bwd without a workspace argument: the library's own fixed scratch is used.
+
+    For callers that cannot allocate device memory.  Problems whose workspace
+    exceeds NOALLOC_SCRATCH_BYTES raise ValueError; calls that overlap on the
+    GPU race on the shared scratch.
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"),
+                 (dk, "dk"), (dv, "dv")):
+        _want(t, torch.bfloat16, n)
+    _want(lse, torch.float32, "lse")
+    _check(lib().bd_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo),
+                                     _ptr(lse), _ptr(dout), B, Hq, Hkv, L, S, D, seq_start,
+                                     float(scale), int(bool(enable_gqa)), _ptr(plan),
+                                     plan.numel() * plan.element_size(), _ptr(dq), _ptr(dk),
+                                     _ptr(dv), _ptr(dev_status), _stream(stream)),
+           "bd_attn_bwd_noalloc")
 
 
 def bd_get_device_status(dev_status, stream=None) -> int:
