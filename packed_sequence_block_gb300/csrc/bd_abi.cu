@@ -70,7 +70,8 @@ AttnDims resolve(int B, int Hq, int Hkv, int L, int S, int D, int seq_start, flo
 
 }  // namespace
 
-bool make_tmap_bf16(CUtensorMap* map, const void* base, int planes, int rows, int D) {
+static bool make_tmap_16bit(CUtensorMap* map, const void* base, int planes, int rows, int D,
+                            CUtensorMapDataType dtype) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
   if (enc == nullptr) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
@@ -79,10 +80,33 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int planes, int rows, in
                            static_cast<cuuint64_t>(rows) * D * 2};
   cuuint32_t box[3] = {64, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+  CUresult r = enc(map, dtype, 3, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_dqacc(CUtensorMap* map, void* base, int planes, int rows, int D) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4,
+                           static_cast<cuuint64_t>(rows) * D * 4};
+  cuuint32_t box[3] = {32, 64, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int planes, int rows, int D) {
+  return make_tmap_16bit(map, base, planes, rows, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+}
+
+bool make_tmap_f16(CUtensorMap* map, const void* base, int planes, int rows, int D) {
+  return make_tmap_16bit(map, base, planes, rows, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
 }
 
 }  // namespace bd
@@ -177,10 +201,8 @@ int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int 
 }
 
 size_t bd_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int S, int D) {
-  (void)Hkv;
-  (void)S;
-  if (B < 1 || Hq < 1 || L < 1 || D < 1) return 0;
-  return bwd_layout(B, Hq, L, D).total;
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || S < 1 || D < 1) return 0;
+  return bwd_layout(B, Hq, Hkv, L, S, D).total;
 }
 
 int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* out,
@@ -205,15 +227,20 @@ int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* 
   st = check_plan_lists(B, Hq, Hkv, L, S);
   if (st != BD_OK) return st;
   if (plan_bytes < plan_layout(B, Hq, Hkv, L, S).total) return BD_ERR_WORKSPACE;
-  if (workspace_bytes < bwd_layout(B, Hq, L, D).total) return BD_ERR_WORKSPACE;
+  const BwdLayout wl = bwd_layout(B, Hq, Hkv, L, S, D);
+  if (workspace_bytes < wl.total) return BD_ERR_WORKSPACE;
   const AttnDims d = resolve(B, Hq, Hkv, L, S, D, seq_start, scale);
-  CUtensorMap tq, tk, tv, tdo;
-  if (!make_tmap_bf16(&tq, q, B * Hq, L, D) || !make_tmap_bf16(&tk, k, B * Hkv, S, D) ||
-      !make_tmap_bf16(&tv, v, B * Hkv, S, D) || !make_tmap_bf16(&tdo, dout, B * Hq, L, D))
+  // q and k tiles reach the main kernel as the fp16 copies the first stage writes
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  char* ws = static_cast<char*>(workspace);
+  if (!make_tmap_f16(&tq, ws + wl.q16, B * Hq, L, D) ||
+      !make_tmap_f16(&tk, ws + wl.k16, B * Hkv, S, D) ||
+      !make_tmap_bf16(&tv, v, B * Hkv, S, D) || !make_tmap_bf16(&tdo, dout, B * Hq, L, D) ||
+      !make_tmap_dqacc(&tdq, ws + wl.dqacc, B * Hq, L, D))
     return BD_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return BD_ERR_CUDA;
-  return launch_bwd(tq, tk, tv, tdo, d, plan, out, out_lo, lse, dout, dq, dk, dv, workspace,
+  return launch_bwd(tq, tk, tv, tdo, tdq, d, plan, q, k, out, out_lo, lse, dout, dq, dk, dv, workspace,
                     dev_status, stages, sms, stream) == cudaSuccess
              ? BD_OK
              : BD_ERR_CUDA;

@@ -10,11 +10,12 @@
 //             looping over the G query heads of the group and the query tiles
 //             the plan marks non-empty.  Per iteration (tcgen05, TMEM):
 //               S^T = K Q^T, dP^T = V dO^T          (cols 256, 384)
-//               P^T, dS^T -> bf16 into TMEM; dS -> smem
+//               P^T (bf16), dS^T (fp16) back into TMEM; dS -> smem
 //               dV += P^T dO, dK += dS^T Q          (cols 128, 0)
-//               dQ = dS K                           (cols 256, after dV)
-//             warpgroup 2 reads dQ out of TMEM and adds it into the fp32
-//             accumulator with vector reductions; dK, dV leave once per unit.
+//               dQ = dS K                           (cols 384, after dK)
+//             warpgroup 2 reads dQ out of TMEM, stages it in shared memory
+//             and adds it into the fp32 accumulator with TMA reductions;
+//             dK, dV leave once per unit.
 //  bwd_dq     dq = bf16(scale * accumulator)
 #include "bd_ptx.cuh"
 
@@ -31,15 +32,20 @@ struct BwdCfg {
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = TILE;
   static constexpr int OFF_Q = 2 * TILE;              // [2 stages]
-  static constexpr int OFF_DO = OFF_Q + 2 * TILE;     // [2 stages]
-  static constexpr int OFF_DS = OFF_DO + 2 * TILE;    // 128 keys x 128 queries bf16
-  static constexpr int OFF_LSED = OFF_DS + 32768;     // [2 stages] 128 x float2
+  // dO_i is read only by dP^T_i (the end of iteration i-1) and dV_i (the start
+  // of iteration i), so one buffer suffices: dO_{i+1} loads while dS_i is
+  // formed.  The 32 KB this saves hold the dQ staging buffer.
+  static constexpr int OFF_DO = OFF_Q + 2 * TILE;
+  static constexpr int OFF_DS = OFF_DO + TILE;        // 128 keys x 128 queries fp16
+  static constexpr int OFF_STG = OFF_DS + 32768;      // 64 rows of dQ_i in fp32
+  static constexpr int OFF_LSED = OFF_STG + 32768;    // [2 stages] 128 x float2
   static constexpr int OFF_BAR = OFF_LSED + 2048;
   static constexpr int SMEM = OFF_BAR + 256;  // barriers, TMEM slot, abort flag, work ring
-  // K and Q tiles are converted to fp16 in shared memory, and dS is produced in
-  // fp16, so the three products that carry dS or feed it (S^T = K Q^T,
-  // dK += dS^T Q, dQ = dS K) run with fp16 operands: 11 significant bits for
-  // dS instead of 8.  dP^T = V dO^T and dV += P^T dO stay bf16.
+  // K and Q arrive as fp16 copies (written by the preprocess stage) and dS is
+  // produced in fp16, so the three products that carry dS or feed it
+  // (S^T = K Q^T, dK += dS^T Q, dQ = dS K) run with fp16 operands: 11
+  // significant bits for dS instead of 8.  dP^T = V dO^T and dV += P^T dO
+  // stay bf16.
   static constexpr uint32_t IDESC_S = make_idesc(128, 128, 0, 0, 0);   // S^T = K Q^T (fp16)
   static constexpr uint32_t IDESC_DP = make_idesc(128, 128, 0, 0, 1);  // dP^T = V dO^T (bf16)
   static constexpr uint32_t IDESC_DV = make_idesc(128, D, 0, 1, 1);    // dV += P^T dO (bf16)
@@ -53,7 +59,8 @@ struct BwdParams {
   const int32_t* kend;
   const int32_t* bwd_range;
   const int32_t* bwd_order;
-  const float2* lsed;
+  const float* lse2;   // lse * log2(e) per query row, +inf where the row attends nothing
+  const float* delta;  // Delta = <dO, O> per query row
   float* dqacc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -99,23 +106,35 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 // ------------------------------------------------------------------ preprocess
 
-// One thread per 8 elements of a row; rows [0, Lq) of every (b, h) plane.
+// One thread per 8 elements of a row.  Threads [0, planes*Lq*TPR) take the
+// query rows (Delta, lse in log2 units, zeroed dq accumulator, fp16 copy of
+// q); the rest convert the key rows to fp16.
 template <int D>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ out,
-                                                      const __nv_bfloat16* __restrict__ out_lo,
-                                                      const __nv_bfloat16* __restrict__ dout,
-                                                      const float* __restrict__ lse, int planes,
-                                                      int L, int Lq, float2* __restrict__ lsed,
-                                                      float* __restrict__ dqacc) {
+__global__ void __launch_bounds__(256) bwd_pre_kernel(
+    const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ out_lo,
+    const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
+    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int planes,
+    int kvplanes, int L, int S, int Lq, float* __restrict__ lse2o, float* __restrict__ deltao,
+    float* __restrict__ dqacc,
+    uint4* __restrict__ q16, uint4* __restrict__ k16) {
   constexpr int TPR = D / 8;  // threads per row (a power of two dividing 32)
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nq = (long long)planes * Lq * TPR;  // a multiple of 32
+  if (tid >= nq) {
+    const long long t = tid - nq;
+    if (t < (long long)kvplanes * S * TPR) {
+      const uint4 x = reinterpret_cast<const uint4*>(k)[t];
+      k16[t] = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
+                          bf16x2_to_f16x2(x.w));
+    }
+    return;
+  }
   const long long rowg = tid / TPR;
   const int part = static_cast<int>(tid % TPR);
-  const bool active = rowg < (long long)planes * Lq;
-  const int plane = active ? static_cast<int>(rowg / Lq) : 0;
-  const int i = active ? static_cast<int>(rowg % Lq) : 0;
+  const int plane = static_cast<int>(rowg / Lq);
+  const int i = static_cast<int>(rowg % Lq);
   float acc = 0.f;
-  if (active && i < L) {
+  if (i < L) {
     const size_t off = ((size_t)plane * L + i) * D + part * 8;
     const uint4 o4 = *reinterpret_cast<const uint4*>(out + off);
     const uint4 d4 = *reinterpret_cast<const uint4*>(dout + off);
@@ -135,11 +154,14 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     float4* z = reinterpret_cast<float4*>(dqacc + off);
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const uint4 x = *reinterpret_cast<const uint4*>(q + off);
+    q16[off / 8] = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
+                              bf16x2_to_f16x2(x.w));
   }
-  // every lane of the warp takes part in the shuffles (inactive lanes add 0)
+  // every lane of the warp takes part in the shuffles (rows past L add 0)
 #pragma unroll
   for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, TPR);
-  if (active && part == 0) {
+  if (part == 0) {
     float l2 = INFINITY, dl = 0.f;
     if (i < L) {
       const float x = lse[(size_t)plane * L + i];
@@ -148,7 +170,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
         dl = acc;
       }
     }
-    lsed[(size_t)plane * Lq + i] = make_float2(l2, dl);
+    lse2o[(size_t)plane * Lq + i] = l2;
+    deltao[(size_t)plane * Lq + i] = dl;
   }
 }
 
@@ -184,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bd_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v,
-                  const __grid_constant__ CUtensorMap tmap_do, const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tmap_do,
+                  const __grid_constant__ CUtensorMap tmap_dq, const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -200,12 +224,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dq_empty = bars + 11;
   uint64_t* dkdv_full = bars + 12;
   uint64_t* drain = bars + 13;
-  uint64_t* k16_ready = bars + 14;  // K tile converted to fp16
-  uint64_t* q16_ready = bars + 15;  // [2] Q tile of the stage converted to fp16
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+  uint64_t* stg_full = bars + 14;  // [2] half h of dQ_i written into the staging buffer
+  uint64_t* stg_read = bars + 16;  // [2] the TMA has read half h (one phase per iteration each,
+                                   // so no waiter can be two phases behind)
+  uint64_t* do_full = bars + 18;   // dO_i landed
+  uint64_t* do_empty = bars + 19;  // dV_i done: the dO buffer may be refilled
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  WorkRing* ring = reinterpret_cast<WorkRing*>(bars + 18);
-  static_assert(18 * 8 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
+  WorkRing* ring = reinterpret_cast<WorkRing*>(bars + 21);
+  static_assert(21 * 8 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -229,15 +256,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dq_empty, 128);
     mbar_init(dkdv_full, 1);
     mbar_init(drain, 1);
-    mbar_init(k16_ready, 64);
-    mbar_init(q16_ready + 0, 64);
-    mbar_init(q16_ready + 1, 64);
-    ring_init(ring, 11);  // MMA thread + converter, P/dS and dQ warps
+    mbar_init(stg_full + 0, 64);
+    mbar_init(stg_full + 1, 64);
+    mbar_init(stg_read + 0, 1);
+    mbar_init(stg_read + 1, 1);
+    mbar_init(do_full, 1);
+    mbar_init(do_empty, 1);
+    ring_init(ring, 9);  // MMA thread + P/dS and dQ warps
     fence_mbar_init();
     prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
     prefetch_tmap(&tmap_do);
+    prefetch_tmap(&tmap_dq);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -252,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && !aborted_at_start) {
     // ------------------------------------------------------------ producer + work queue
     if (lane == 0) {
-      uint32_t kv_u = 0, st_it = 0, kq = 0;
+      uint32_t kv_u = 0, st_it = 0, do_it = 0, kq = 0;  // fills issued: K/V, Q stages, dO
       for (;;) {
         int w;
         if (!ring_publish(ring, kq++, p.ctr, p.n_units, abort_flag, p.status, w) || w < 0) break;
@@ -273,17 +304,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int st = st_it & 1;
           ok = mbar_wait(st_empty + st, ((st_it >> 1) & 1) ^ 1, abort_flag, p.status);
           if (!ok) break;
-          mbar_arrive_expect_tx(st_full + st, 2 * C::TILE + 1024);
+          mbar_arrive_expect_tx(st_full + st, C::TILE + 1024);
           const int qplane = u.b * p.Hq + h;
-          for (int j = 0; j < D / 64; ++j) {
+          for (int j = 0; j < D / 64; ++j)
             tma_load_3d(smem + C::OFF_Q + st * C::TILE + j * 16384, &tmap_q, st_full + st, 64 * j,
                         qt * kBM, qplane);
-            tma_load_3d(smem + C::OFF_DO + st * C::TILE + j * 16384, &tmap_do, st_full + st,
-                        64 * j, qt * kBM, qplane);
-          }
-          bulk_load(smem + C::OFF_LSED + st * 1024, p.lsed + (size_t)qplane * p.Lq + qt * kBM,
-                    1024, st_full + st);
+          const size_t ro = (size_t)qplane * p.Lq + qt * kBM;
+          bulk_load(smem + C::OFF_LSED + st * 1024, p.lse2 + ro, 512, st_full + st);
+          bulk_load(smem + C::OFF_LSED + st * 1024 + 512, p.delta + ro, 512, st_full + st);
           ++st_it;
+          // dO_i after dV_{i-1}; Q_{i+1} (next round) waits for dK_{i-1}, which follows dV_{i-1}
+          ok = mbar_wait(do_empty, (do_it & 1) ^ 1, abort_flag, p.status);
+          if (!ok) break;
+          mbar_arrive_expect_tx(do_full, C::TILE);
+          for (int j = 0; j < D / 64; ++j)
+            tma_load_3d(smem + C::OFF_DO + j * 16384, &tmap_do, do_full, 64 * j, qt * kBM, qplane);
+          ++do_it;
         }
         if (!ok) break;
       }
@@ -294,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           drain_wait(st_full + st, (last >> 1) & 1, p.status);
         }
       }
+      if (do_it > 0) drain_wait(do_full, (do_it - 1) & 1, p.status);
     }
     __syncwarp();
   } else if (warp == 1 && !aborted_at_start) {
@@ -335,10 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ring_take(ring, kq++, abort_flag, p.status, w) || w < 0) break;
         const BUnit u = decode_bunit(p, w);
         if (u.n_it <= 0) continue;
-        ok = mbar_wait(k16_ready, kv_u & 1, abort_flag, p.status);  // implies kv_full
+        ok = mbar_wait(kv_full, kv_u & 1, abort_flag, p.status);
         if (!ok) break;
         int st = st_it & 1;
-        ok = mbar_wait(q16_ready + st, (st_it >> 1) & 1, abort_flag, p.status);  // implies st_full
+        ok = mbar_wait(st_full + st, (st_it >> 1) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
         issue_kmajor(tS, sk, sq0 + st * C::TILE, C::IDESC_S);
@@ -346,9 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it_g > 0) {  // the previous iteration's dQ must have left the dP columns
           ok = mbar_wait(dq_empty, (it_g - 1) & 1, abort_flag, p.status);
           if (!ok) break;
-          tc_fence_after();
         }
-        issue_kmajor(tDP, sv, sdo0 + st * C::TILE, C::IDESC_DP);
+        ok = mbar_wait(do_full, st_it & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        issue_kmajor(tDP, sv, sdo0, C::IDESC_DP);
         mma_commit(dp_full);
         for (int i = 0; i < u.n_it && ok; ++i) {
           const uint32_t si = st_it + i;
@@ -358,9 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(p_full, it_g & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
-          issue_ts(tDV, tS, sdo0 + st * C::TILE, i > 0, C::IDESC_DV);
+          issue_ts(tDV, tS, sdo0, i > 0, C::IDESC_DV);
+          mma_commit(do_empty);  // dO_i is no longer read
           if (more) {
-            ok = mbar_wait(q16_ready + sn, ((si + 1) >> 1) & 1, abort_flag, p.status);
+            ok = mbar_wait(st_full + sn, ((si + 1) >> 1) & 1, abort_flag, p.status);
             if (!ok) break;
             tc_fence_after();
             issue_kmajor(tS, sk, sq0 + sn * C::TILE, C::IDESC_S);
@@ -370,14 +410,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           issue_ts(tDK, tDP, sq0 + st * C::TILE, i > 0, C::IDESC_DK);
-          mma_commit(st_empty + st);
+          mma_commit(st_empty + st);  // Q_i is no longer read after dK_i
           issue_dq();
           mma_commit(dq_full);
           if (more) {
             ok = mbar_wait(dq_empty, it_g & 1, abort_flag, p.status);
             if (!ok) break;
+            ok = mbar_wait(do_full, (si + 1) & 1, abort_flag, p.status);
+            if (!ok) break;
             tc_fence_after();
-            issue_kmajor(tDP, sv, sdo0 + sn * C::TILE, C::IDESC_DP);
+            issue_kmajor(tDP, sv, sdo0, C::IDESC_DP);
             mma_commit(dp_full);
           }
           ++it_g;
@@ -391,45 +433,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(drain, 0, p.status);
     }
     __syncwarp();
-  } else if ((warp == 2 || warp == 3) && !aborted_at_start) {
-    // ------------------------------------------------------------ bf16 -> fp16 converters
-    // K (once per unit) and each Q tile are rewritten in place, element by
-    // element, so the swizzled layout the descriptors describe is unchanged.
-    const int t = threadIdx.x - 64;  // 0..63
-    auto convert = [&](uint8_t* tile) {
-      const uint32_t base = smem_u32(tile);
-#pragma unroll 4
-      for (int c = t; c < C::TILE / 16; c += 64) {
-        uint32_t a, b, cc, d;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(a), "=r"(b), "=r"(cc), "=r"(d)
-                     : "r"(base + c * 16));
-        st_shared_v4(base + c * 16, bf16x2_to_f16x2(a), bf16x2_to_f16x2(b),
-                     bf16x2_to_f16x2(cc), bf16x2_to_f16x2(d));
-      }
-      fence_async_smem();
-    };
-    uint32_t kv_u = 0, st_it = 0, kq = 0;
-    for (;;) {
-      int w;
-      if (!ring_take_warp(ring, kq++, abort_flag, p.status, w) || w < 0) break;
-      const BUnit u = decode_bunit(p, w);
-      if (u.n_it <= 0) continue;
-      if (!mbar_wait_warp(kv_full, kv_u & 1, abort_flag, p.status)) break;
-      convert(smem + C::OFF_K);
-      mbar_arrive(k16_ready);
-      ++kv_u;
-      bool ok = true;
-      for (int i = 0; i < u.n_it; ++i) {
-        const int st = st_it & 1;
-        ok = mbar_wait_warp(st_full + st, (st_it >> 1) & 1, abort_flag, p.status);
-        if (!ok) break;
-        convert(smem + C::OFF_Q + st * C::TILE);
-        mbar_arrive(q16_ready + st);
-        ++st_it;
-      }
-      if (!ok) break;
-    }
   } else if (warp >= 4 && warp < 8 && !aborted_at_start) {
     // ------------------------------------------------------------ P / dS warpgroup
     const int q4 = warp & 3;
@@ -475,23 +478,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           cb = min(kend, p.seq_start + p.L) - q0 - 1;
         }
         const bool full = __all_sync(0xffffffffu, ca <= 0 && cb >= kBM - 1);
-        const float4* ld4 = reinterpret_cast<const float4*>(smem + C::OFF_LSED + st * 1024);
+        // the stage holds lse*log2(e) of the tile's 128 queries, then their Delta
+        const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LSED + st * 1024);
+        const float4* dl4 = lse4 + 32;
         uint32_t pk[64];  // P^T of this key row as bf16 pairs (the dV MMA's operand), kept for dS
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t sv[32], tmp[16];
           tmem_ld32(tS + c * 32, sv);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float4 x = ld4[(c * 32 + e) >> 1];  // (lse2, delta) of two columns
+          for (int e = 0; e < 32; e += 4) {
+            const float4 x = lse4[(c * 32 + e) >> 2];  // lse*log2(e) of four columns
             float p0 = fast_exp2(fmaf(__uint_as_float(sv[e]), p.scale_log2, -x.x));
-            float p1 = fast_exp2(fmaf(__uint_as_float(sv[e + 1]), p.scale_log2, -x.z));
+            float p1 = fast_exp2(fmaf(__uint_as_float(sv[e + 1]), p.scale_log2, -x.y));
+            float p2 = fast_exp2(fmaf(__uint_as_float(sv[e + 2]), p.scale_log2, -x.z));
+            float p3 = fast_exp2(fmaf(__uint_as_float(sv[e + 3]), p.scale_log2, -x.w));
             if (!full) {
               const int col = c * 32 + e;
               p0 = (col >= ca && col <= cb) ? p0 : 0.f;
               p1 = (col + 1 >= ca && col + 1 <= cb) ? p1 : 0.f;
+              p2 = (col + 2 >= ca && col + 2 <= cb) ? p2 : 0.f;
+              p3 = (col + 3 >= ca && col + 3 <= cb) ? p3 : 0.f;
             }
             pk[c * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
+            pk[c * 16 + (e >> 1) + 1] = pack_bf16x2(p2, p3);
           }
 #pragma unroll
           for (int e = 0; e < 16; ++e) tmp[e] = pk[c * 16 + e];
@@ -510,12 +520,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tDP + c * 32, dv);
           uint32_t dk[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float4 x = ld4[(c * 32 + e) >> 1];
-            const uint32_t pw = pk[c * 16 + (e >> 1)];
-            const float p0 = __uint_as_float(pw << 16), p1 = __uint_as_float(pw & 0xffff0000u);
-            dk[e >> 1] = pack_f16x2(p0 * (__uint_as_float(dv[e]) - x.y),
-                                    p1 * (__uint_as_float(dv[e + 1]) - x.w));
+          for (int e = 0; e < 32; e += 4) {
+            const float4 x = dl4[(c * 32 + e) >> 2];  // Delta of four columns
+            const uint32_t pa = pk[c * 16 + (e >> 1)], pb = pk[c * 16 + (e >> 1) + 1];
+            dk[e >> 1] = pack_f16x2(__uint_as_float(pa << 16) * (__uint_as_float(dv[e]) - x.x),
+                                    __uint_as_float(pa & 0xffff0000u) *
+                                        (__uint_as_float(dv[e + 1]) - x.y));
+            dk[(e >> 1) + 1] =
+                pack_f16x2(__uint_as_float(pb << 16) * (__uint_as_float(dv[e + 2]) - x.z),
+                           __uint_as_float(pb & 0xffff0000u) * (__uint_as_float(dv[e + 3]) - x.w));
           }
           tmem_st16(tDP + c * 16, dk);
           // dS (queries contiguous) into the MN-major, 128-byte-swizzled A tile of dQ = dS K
@@ -566,9 +579,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 8 && !aborted_at_start) {
     // ------------------------------------------------------------ dQ warpgroup
+    // dQ_i leaves TMEM in one load (the MMA warp may then reuse the columns).
+    // The fp32 tile goes out through the staging buffer in two halves of 64
+    // rows: the threads of a half write their rows in 128-byte-swizzled boxes
+    // of 64 rows x 32 columns, and one thread adds them into the accumulator
+    // with TMA reductions, so the reductions never occupy the SM's load/store
+    // path.  Half 0 of dQ_i waits for the TMA to have read half 1 of dQ_{i-1};
+    // half 1 waits for half 0.
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;  // query row of the tile = TMEM lane
+    const int half = r >> 6, rr = r & 63;
     const uint32_t tQ = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + 384;
+    const uint32_t sstg = smem_u32(smem + C::OFF_STG);
+    const bool leader = threadIdx.x == 256;
     uint32_t it_g = 0, kq = 0;
     for (;;) {
       int w;
@@ -577,29 +600,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int i = 0; i < u.n_it; ++i) {
         const int h = u.g * p.G + i / u.nq;
-        const int row = (u.qt_lo + i % u.nq) * kBM + r;
+        const int qt = u.qt_lo + i % u.nq;
         ok = mbar_wait_warp(dq_full, it_g & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
-        float* dst = p.dqacc + ((size_t)(u.b * p.Hq + h) * p.L + row) * D;
+        uint32_t v[D];
+        if constexpr (D == 128) {
+          tmem_ld128(tQ, v);
+        } else {
+          uint32_t t0[32], t1[32];
+          tmem_ld32(tQ, t0);
+          tmem_ld32(tQ + 32, t1);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t t[32];
-          tmem_ld32(tQ + c * 32, t);
-          if (row < p.L) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              red_add_v4(dst + c * 32 + 4 * j, __uint_as_float(t[4 * j]),
-                         __uint_as_float(t[4 * j + 1]), __uint_as_float(t[4 * j + 2]),
-                         __uint_as_float(t[4 * j + 3]));
+          for (int e = 0; e < 32; ++e) {
+            v[e] = t0[e];
+            v[32 + e] = t1[e];
           }
         }
         tc_fence_before();
-        mbar_arrive(dq_empty);
+        mbar_arrive(dq_empty);  // TMEM columns free again
+        const int plane = u.b * p.Hq + h;
+        if (half == 1) {
+          ok = mbar_wait_warp(stg_read + 0, it_g & 1, abort_flag, p.status);
+          if (!ok) break;
+        } else if (it_g > 0) {
+          ok = mbar_wait_warp(stg_read + 1, (it_g - 1) & 1, abort_flag, p.status);
+          if (!ok) break;
+        }
+        const uint32_t row = sstg + rr * 128;
+#pragma unroll
+        for (int b = 0; b < D / 32; ++b) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(row + b * 8192 + ((c ^ (rr & 7)) << 4), v[b * 32 + c * 4],
+                         v[b * 32 + c * 4 + 1], v[b * 32 + c * 4 + 2], v[b * 32 + c * 4 + 3]);
+        }
+        fence_async_smem();
+        mbar_arrive(stg_full + half);
+        if (leader) {
+          for (int hh = 0; hh < 2 && ok; ++hh) {
+            ok = mbar_wait(stg_full + hh, it_g & 1, abort_flag, p.status);
+            if (!ok) break;
+#pragma unroll
+            for (int b = 0; b < D / 32; ++b)
+              tma_reduce_add_3d(&tmap_dq, smem + C::OFF_STG + b * 8192, 32 * b,
+                                qt * kBM + 64 * hh, plane);
+            bulk_commit_group();
+            bulk_wait_read_all();
+            mbar_arrive(stg_read + hh);
+          }
+        }
+        ok = __all_sync(0xffffffffu, ok);
         ++it_g;
+        if (!ok) break;
       }
       if (!ok) break;
     }
+    if (leader) bulk_wait_all();  // the reductions finish before the CTA's memory goes
   }
 
   tc_fence_before();
@@ -614,8 +671,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const CUtensorMap& tdo,
-                                const BwdParams& p, const void* out, const void* out_lo,
-                                const float* lse, const void* dout, void* dq, int stages,
+                                const CUtensorMap& tdq,
+                                const BwdParams& p, const void* q, const void* k,
+                                const void* out, const void* out_lo, const float* lse,
+                                const void* dout, void* dq, void* q16, void* k16, int stages,
                                 int num_sms,
                                 cudaStream_t stream) {
   using C = BwdCfg<D>;
@@ -630,17 +689,21 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
   }
   const int planes = p.B * p.Hq;
   if (stages & kBwdPrepare) {
-    const long long threads = (long long)planes * p.Lq * (D / 8);
+    const long long threads =
+        ((long long)planes * p.Lq + (long long)p.B * p.Hkv * p.S) * (D / 8);
     bwd_pre_kernel<D><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(out_lo),
-        static_cast<const __nv_bfloat16*>(dout), lse,
-        planes, p.L, p.Lq, const_cast<float2*>(p.lsed), p.dqacc);
+        static_cast<const __nv_bfloat16*>(dout), lse, static_cast<const __nv_bfloat16*>(q),
+        static_cast<const __nv_bfloat16*>(k), planes, p.B * p.Hkv, p.L, p.S, p.Lq,
+        const_cast<float*>(p.lse2), const_cast<float*>(p.delta), p.dqacc,
+        static_cast<uint4*>(q16),
+        static_cast<uint4*>(k16));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   const int grid = p.n_units < num_sms ? p.n_units : num_sms;
   if ((stages & kBwdMain) && grid > 0) {
-    bd_bwd_kernel<D><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, p);
+    bd_bwd_kernel<D><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -653,13 +716,14 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
 }
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const AttnDims& d, void* plan,
-                       const void* out, const void* out_lo, const float* lse, const void* dout,
-                       void* dq, void* dk,
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const AttnDims& d,
+                       void* plan, const void* q,
+                       const void* k, const void* out, const void* out_lo, const float* lse,
+                       const void* dout, void* dq, void* dk,
                        void* dv, void* workspace, int32_t* status, int stages, int num_sms,
                        cudaStream_t stream) {
   const PlanLayout pl = plan_layout(d.B, d.Hq, d.Hkv, d.L, d.S);
-  const BwdLayout wl = bwd_layout(d.B, d.Hq, d.L, d.D);
+  const BwdLayout wl = bwd_layout(d.B, d.Hq, d.Hkv, d.L, d.S, d.D);
   char* base = static_cast<char*>(plan);
   char* ws = static_cast<char*>(workspace);
   BwdParams p{};
@@ -679,15 +743,18 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.kend = reinterpret_cast<const int32_t*>(base + pl.kend);
   p.bwd_range = reinterpret_cast<const int32_t*>(base + pl.bwd_range);
   p.bwd_order = reinterpret_cast<const int32_t*>(base + pl.bwd_order);
-  p.lsed = reinterpret_cast<const float2*>(ws + wl.lsed);
+  p.lse2 = reinterpret_cast<const float*>(ws + wl.lsed);
+  p.delta = p.lse2 + (size_t)d.B * d.Hq * wl.Lq;
   p.dqacc = reinterpret_cast<float*>(ws + wl.dqacc);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.status = status;
   p.ctr = reinterpret_cast<int*>(base + pl.sched) + 2;
-  if (d.D == 64) return launch_bwd_t<64>(tq, tk, tv, tdo, p, out, out_lo, lse, dout, dq, stages, num_sms,
+  if (d.D == 64) return launch_bwd_t<64>(tq, tk, tv, tdo, tdq, p, q, k, out, out_lo, lse, dout, dq, ws + wl.q16,
+                                          ws + wl.k16, stages, num_sms,
                                           stream);
-  return launch_bwd_t<128>(tq, tk, tv, tdo, p, out, out_lo, lse, dout, dq, stages, num_sms,
+  return launch_bwd_t<128>(tq, tk, tv, tdo, tdq, p, q, k, out, out_lo, lse, dout, dq, ws + wl.q16,
+                           ws + wl.k16, stages, num_sms,
                            stream);
 }
 
