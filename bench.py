@@ -18,6 +18,7 @@ the workload (weak scaling, no collective on the data path).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -72,6 +73,35 @@ def describe(wl):
     return (f"{wl.name}: {wl.B} row(s) x {wl.S} tokens, Hq={wl.Hq}, Hkv={wl.Hkv}, D={wl.D}, "
             f"{docs} docs, {pad} padding tokens, {len(wl.seq_starts)} query interval(s) of "
             f"{wl.L}, seed {wl.seed}")
+
+
+def profiled_traffic(workload, seed):
+    """DRAM bytes per launch of the backward main kernel from the committed ncu
+    summary, or None when the kernel sources differ from the profiled ones or
+    the workload is not the profiled one."""
+    if workload != "lognormal8k" or seed != 0:
+        return None, "no capture for this workload"
+    path = os.path.join(ROOT, "profiles", "bd_bwd_kernel_lognormal8k.md")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None, "no capture"
+    traffic, shas = None, {}
+    for ln in lines:
+        ln = ln.strip()
+        if ln.startswith("traffic_bytes_per_launch:"):
+            traffic = int(ln.split(":", 1)[1])
+        elif ln.startswith("source_sha256:"):
+            name, digest = ln.split(":", 1)[1].split()
+            shas[name] = digest
+    if traffic is None or not shas:
+        return None, "no capture"
+    csrc = os.path.join(ROOT, "packed_sequence_block_gb300", "csrc")
+    for name, digest in shas.items():
+        with open(os.path.join(csrc, name), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != digest:
+                return None, f"{name} changed since the ncu capture"
+    return traffic, "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch"
 
 
 def read_peaks():
@@ -398,6 +428,7 @@ def main():
     achieved = flops_bwd_main_step * args.steps / (sum(main_ms) * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
     clocks = sampler.summary(local)
+    traffic, traffic_src = profiled_traffic(args.workload, args.seed)
 
     if rank == 0:
         line = {
@@ -419,7 +450,8 @@ def main():
             "gpu_launches": hp.launches_per_step() * args.steps,
             "roofline": {"kernel": "bd_bwd_kernel (backward main)", "bound": "tensor",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak, "traffic": traffic,
+                         "traffic_source": traffic_src,
                          "peak_source": f"{peak_src} bf16_tflops (burst)",
                          "avg_launch_ms": main_avg},
             "clocks": clocks,
