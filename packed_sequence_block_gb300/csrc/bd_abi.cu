@@ -93,7 +93,7 @@ bool make_tmap_dqacc(CUtensorMap* map, void* base, int planes, int rows, int D) 
                         static_cast<cuuint64_t>(planes)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4,
                            static_cast<cuuint64_t>(rows) * D * 4};
-  cuuint32_t box[3] = {32, 64, 1};
+  cuuint32_t box[3] = {32, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

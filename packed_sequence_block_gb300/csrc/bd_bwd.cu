@@ -13,7 +13,7 @@
 //               P^T (bf16), dS^T (fp16) back into TMEM; dS -> smem
 //               dV += P^T dO, dK += dS^T Q          (cols 128, 0)
 //               dQ = dS K                           (cols 384, after dK)
-//             warpgroup 2 reads dQ out of TMEM, stages it in shared memory
+//             four warps read dQ out of TMEM, stage it in shared memory
 //             and adds it into the fp32 accumulator with TMA reductions;
 //             dK, dV leave once per unit.
 //  bwd_dq     dq = bf16(scale * accumulator)
@@ -23,7 +23,9 @@ namespace bd {
 
 namespace {
 
-constexpr int kThreads = 384;
+// 16 warps: producer, MMA, dQ reduction issuer, one idle warp, two P/dS
+// warpgroups and the dQ readers.
+constexpr int kThreads = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -37,7 +39,7 @@ struct BwdCfg {
   // formed.  The 32 KB this saves hold the dQ staging buffer.
   static constexpr int OFF_DO = OFF_Q + 2 * TILE;
   static constexpr int OFF_DS = OFF_DO + TILE;        // 128 keys x 128 queries fp16
-  static constexpr int OFF_STG = OFF_DS + 32768;      // 64 rows of dQ_i in fp32
+  static constexpr int OFF_STG = OFF_DS + 32768;      // 64 columns of dQ_i in fp32
   static constexpr int OFF_LSED = OFF_STG + 32768;    // [2 stages] 128 x float2
   static constexpr int OFF_BAR = OFF_LSED + 2048;
   static constexpr int SMEM = OFF_BAR + 256;  // barriers, TMEM slot, abort flag, work ring
@@ -197,10 +199,12 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
 //   dK [0,128)  dV [128,256)  S^T -> P^T [256,384)  dP^T -> dS^T -> dQ [384,512)
 // Tensor-core order (one thread):
 //   dV += P^T_i dO_i | S^T_{i+1} | dK += dS^T_i Q_i | dQ_i = dS_i K | dP^T_{i+1}
-// so that the P/dS work of warpgroup 1 overlaps MMAs: dS_i is formed while
-// dV_i and S^T_{i+1} run, P_{i+1} while dK_i, dQ_i and dP^T_{i+1} run.
-// Warpgroup 1 keeps P_i between its two phases as the bf16 pairs it hands to
-// the dV MMA (64 registers) and forms dS = P (dP - Delta) in fp32 from them.
+// so that the P/dS work overlaps MMAs: dS_i is formed while dV_i and S^T_{i+1}
+// run, P_{i+1} while dK_i, dQ_i and dP^T_{i+1} run.  Two warpgroups share
+// that work by query columns (64 each), which puts two such warps on every
+// scheduler.  Each keeps P_i between its two phases as the bf16 pairs it
+// hands to the dV MMA (32 registers) and forms dS = P (dP - Delta) in fp32
+// from them.
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -224,9 +228,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dq_empty = bars + 11;
   uint64_t* dkdv_full = bars + 12;
   uint64_t* drain = bars + 13;
-  uint64_t* stg_full = bars + 14;  // [2] half h of dQ_i written into the staging buffer
-  uint64_t* stg_read = bars + 16;  // [2] the TMA has read half h (one phase per iteration each,
-                                   // so no waiter can be two phases behind)
+  // a round of dQ_i is in the staging buffer / the TMA has read it; only the
+  // writers and the issuer wait on these, one phase per round, so neither
+  // side can be two phases behind
+  uint64_t* stg_full = bars + 14;
+  uint64_t* stg_read = bars + 16;
   uint64_t* do_full = bars + 18;   // dO_i landed
   uint64_t* do_empty = bars + 19;  // dV_i done: the dO buffer may be refilled
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
@@ -250,19 +256,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_full, 128);
-    mbar_init(ds_full, 128);
+    mbar_init(p_full, 256);
+    mbar_init(ds_full, 256);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(dkdv_full, 1);
     mbar_init(drain, 1);
-    mbar_init(stg_full + 0, 64);
-    mbar_init(stg_full + 1, 64);
-    mbar_init(stg_read + 0, 1);
-    mbar_init(stg_read + 1, 1);
+    mbar_init(stg_full, 128);
+    mbar_init(stg_read, 1);
     mbar_init(do_full, 1);
     mbar_init(do_empty, 1);
-    ring_init(ring, 9);  // MMA thread + P/dS and dQ warps
+    ring_init(ring, 14);  // MMA thread, reduction issuer, 8 P/dS warps, 4 dQ readers
     fence_mbar_init();
     prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_k);
@@ -351,12 +355,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                  idesc, kk > 0);
         }
       };
-      // D[keys, D] (+)= A[tmem, keys x 128 queries] * B[queries, D] (MN-major smem)
+      // D[keys, D] (+)= A[tmem, keys x 128 queries] * B[queries, D] (MN-major smem).
+      // A's 16-bit pairs for queries [0, 64) sit at columns [0, 32) of its
+      // 128-column region and those for [64, 128) at [64, 96) (each P/dS
+      // warpgroup packs into the first half of its own columns).
       auto issue_ts = [&](uint32_t d, uint32_t a_tmem, uint32_t b, bool acc, uint32_t idesc) {
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          mma_ts(d, a_tmem + ks * 8, make_sdesc_sw128(b + ks * 2048, 16384, 1024), idesc,
-                 (acc || ks > 0));
+          mma_ts(d, a_tmem + ks * 8 + (ks >= 4 ? 32 : 0),
+                 make_sdesc_sw128(b + ks * 2048, 16384, 1024), idesc, (acc || ks > 0));
       };
       // dQ[queries, D] = dS[queries, keys] (MN-major smem) * K[keys, D] (MN-major smem)
       auto issue_dq = [&]() {
@@ -433,13 +440,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(drain, 0, p.status);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 8 && !aborted_at_start) {
-    // ------------------------------------------------------------ P / dS warpgroup
+  } else if (warp >= 4 && warp < 12 && !aborted_at_start) {
+    // ------------------------------------------------------------ P / dS warpgroups
+    // Warpgroup hf (1 or 2 -> hf 0 or 1) takes the 64 queries [64 hf, 64 hf + 64)
+    // of every key row; the two groups reach the same TMEM lanes (lane access
+    // follows the warp's index mod 4).
+    const int hf = (warp - 4) >> 2;
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;  // key row of the tile = TMEM lane
+    const int c0 = 64 * hf;        // first query column of this group
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t tS = tmem + lane_off + 256, tDP = tmem + lane_off + 384;
-    const uint32_t sds_row = smem_u32(smem + C::OFF_DS) + (r >> 3) * 1024 + (r & 7) * 128;
+    // S^T / dP^T columns of this group; P^T and dS^T (16-bit pairs) go back into
+    // the first half of them, behind the reads
+    const uint32_t tS = tmem + lane_off + 256 + c0, tDP = tmem + lane_off + 384 + c0;
+    const uint32_t sds_row = smem_u32(smem + C::OFF_DS) + hf * 16384 + (r >> 3) * 1024 +
+                             (r & 7) * 128;
     uint32_t st_it = 0, it_g = 0, kv_u = 0, kq = 0;
     for (;;) {
       int w;
@@ -447,15 +462,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const BUnit u = decode_bunit(p, w);
       const int key = u.kt * kBN + r;
       const size_t krow = ((size_t)(u.b * p.Hkv + u.g) * p.S + key) * D;
+      // group 1 owns dK of the tile, group 2 dV
+      __nv_bfloat16* const grad = (hf == 0 ? p.dk : p.dv) + krow;
       if (u.n_it <= 0) {
         if (key < p.S) {
-          uint4* a = reinterpret_cast<uint4*>(p.dk + krow);
-          uint4* b = reinterpret_cast<uint4*>(p.dv + krow);
+          uint4* a = reinterpret_cast<uint4*>(grad);
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) {
-            a[c] = make_uint4(0, 0, 0, 0);
-            b[c] = make_uint4(0, 0, 0, 0);
-          }
+          for (int c = 0; c < D / 8; ++c) a[c] = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -477,13 +490,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ca = key - q0;
           cb = min(kend, p.seq_start + p.L) - q0 - 1;
         }
-        const bool full = __all_sync(0xffffffffu, ca <= 0 && cb >= kBM - 1);
+        const bool full = __all_sync(0xffffffffu, ca <= c0 && cb >= c0 + 63);
         // the stage holds lse*log2(e) of the tile's 128 queries, then their Delta
-        const float4* lse4 = reinterpret_cast<const float4*>(smem + C::OFF_LSED + st * 1024);
+        const float4* lse4 =
+            reinterpret_cast<const float4*>(smem + C::OFF_LSED + st * 1024) + (c0 >> 2);
         const float4* dl4 = lse4 + 32;
-        uint32_t pk[64];  // P^T of this key row as bf16 pairs (the dV MMA's operand), kept for dS
+        uint32_t pk[32];  // P^T of this key row as bf16 pairs (the dV MMA's operand), kept for dS
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t sv[32], tmp[16];
           tmem_ld32(tS + c * 32, sv);
 #pragma unroll
@@ -494,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float p2 = fast_exp2(fmaf(__uint_as_float(sv[e + 2]), p.scale_log2, -x.z));
             float p3 = fast_exp2(fmaf(__uint_as_float(sv[e + 3]), p.scale_log2, -x.w));
             if (!full) {
-              const int col = c * 32 + e;
+              const int col = c0 + c * 32 + e;
               p0 = (col >= ca && col <= cb) ? p0 : 0.f;
               p1 = (col + 1 >= ca && col + 1 <= cb) ? p1 : 0.f;
               p2 = (col + 2 >= ca && col + 2 <= cb) ? p2 : 0.f;
@@ -515,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t dv[32];
           tmem_ld32(tDP + c * 32, dv);
           uint32_t dk[16];
@@ -534,8 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dS (queries contiguous) into the MN-major, 128-byte-swizzled A tile of dQ = dS K
 #pragma unroll
           for (int gq = 0; gq < 4; ++gq) {
-            const int cq = c * 4 + gq;  // 16-byte chunk index along the queries
-            const uint32_t addr = sds_row + (cq >> 3) * 16384 + (((cq & 7) ^ (r & 7)) << 4);
+            const int cq = c * 4 + gq;  // 16-byte chunk index along this group's queries
+            const uint32_t addr = sds_row + ((cq ^ (r & 7)) << 4);
             st_shared_v4(addr, dk[4 * gq], dk[4 * gq + 1], dk[4 * gq + 2], dk[4 * gq + 3]);
           }
         }
@@ -547,116 +561,112 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++it_g;
       }
       if (!ok) break;
-      // epilogue: dK (scaled) and dV of this key tile
+      // epilogue: dK (scaled, group 1) or dV (group 2) of this key tile
       ok = mbar_wait_warp(dkdv_full, kv_u & 1, abort_flag, p.status);
       if (!ok) break;
       ++kv_u;
       tc_fence_after();
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const uint32_t tsrc = tmem + lane_off + half * 128;
-        __nv_bfloat16* dst = (half == 0 ? p.dk : p.dv) + krow;
-        const float mul = half == 0 ? p.scale : 1.f;
+      {
+        const uint32_t tsrc = tmem + lane_off + hf * 128;
+        const float mul = hf == 0 ? p.scale : 1.f;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(tsrc + c * 32, v);
-          uint32_t pk[16];
+          uint32_t pk2[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul,
-                                __uint_as_float(v[2 * e + 1]) * mul);
+            pk2[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul,
+                                 __uint_as_float(v[2 * e + 1]) * mul);
           if (key < p.S) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-            d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            d4[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
-            d4[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+            uint4* d4 = reinterpret_cast<uint4*>(grad + c * 32);
+            d4[0] = make_uint4(pk2[0], pk2[1], pk2[2], pk2[3]);
+            d4[1] = make_uint4(pk2[4], pk2[5], pk2[6], pk2[7]);
+            d4[2] = make_uint4(pk2[8], pk2[9], pk2[10], pk2[11]);
+            d4[3] = make_uint4(pk2[12], pk2[13], pk2[14], pk2[15]);
           }
         }
       }
       tc_fence_before();
     }
-  } else if (warp >= 8 && !aborted_at_start) {
-    // ------------------------------------------------------------ dQ warpgroup
-    // dQ_i leaves TMEM in one load (the MMA warp may then reuse the columns).
-    // The fp32 tile goes out through the staging buffer in two halves of 64
-    // rows: the threads of a half write their rows in 128-byte-swizzled boxes
-    // of 64 rows x 32 columns, and one thread adds them into the accumulator
-    // with TMA reductions, so the reductions never occupy the SM's load/store
-    // path.  Half 0 of dQ_i waits for the TMA to have read half 1 of dQ_{i-1};
-    // half 1 waits for half 0.
+  } else if (warp >= 12 && !aborted_at_start) {
+    // ------------------------------------------------------------ dQ readers
+    // dQ_i leaves TMEM in rounds of 64 columns (64 registers a thread); after
+    // the last round's load the MMA warp may reuse the columns.  Each round is
+    // written into the staging buffer as two 128-byte-swizzled boxes of 128
+    // rows x 32 columns, which warp 2 adds into the fp32 accumulator with TMA
+    // reductions, so the reductions never occupy the SM's load/store path.
+    // A round waits until the TMA has read the previous one.
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;  // query row of the tile = TMEM lane
-    const int half = r >> 6, rr = r & 63;
     const uint32_t tQ = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + 384;
-    const uint32_t sstg = smem_u32(smem + C::OFF_STG);
-    const bool leader = threadIdx.x == 256;
-    uint32_t it_g = 0, kq = 0;
+    const uint32_t srow = smem_u32(smem + C::OFF_STG) + r * 128;
+    uint32_t it_g = 0, rnd = 0, kq = 0;
     for (;;) {
       int w;
       if (!ring_take_warp(ring, kq++, abort_flag, p.status, w) || w < 0) break;
       const BUnit u = decode_bunit(p, w);
       bool ok = true;
-      for (int i = 0; i < u.n_it; ++i) {
-        const int h = u.g * p.G + i / u.nq;
-        const int qt = u.qt_lo + i % u.nq;
+      for (int i = 0; i < u.n_it && ok; ++i) {
         ok = mbar_wait_warp(dq_full, it_g & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
-        uint32_t v[D];
-        if constexpr (D == 128) {
-          tmem_ld128(tQ, v);
-        } else {
-          uint32_t t0[32], t1[32];
-          tmem_ld32(tQ, t0);
-          tmem_ld32(tQ + 32, t1);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            v[e] = t0[e];
-            v[32 + e] = t1[e];
+        for (int rd = 0; rd < D / 64; ++rd) {
+          uint32_t va[32], vb[32];
+          tmem_ld32x2(tQ + 64 * rd, tQ + 64 * rd + 32, va, vb);
+          if (rd == D / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(dq_empty);  // TMEM columns free again
           }
-        }
-        tc_fence_before();
-        mbar_arrive(dq_empty);  // TMEM columns free again
-        const int plane = u.b * p.Hq + h;
-        if (half == 1) {
-          ok = mbar_wait_warp(stg_read + 0, it_g & 1, abort_flag, p.status);
-          if (!ok) break;
-        } else if (it_g > 0) {
-          ok = mbar_wait_warp(stg_read + 1, (it_g - 1) & 1, abort_flag, p.status);
-          if (!ok) break;
-        }
-        const uint32_t row = sstg + rr * 128;
-#pragma unroll
-        for (int b = 0; b < D / 32; ++b) {
+          if (rnd > 0) {
+            ok = mbar_wait_warp(stg_read, (rnd - 1) & 1, abort_flag, p.status);
+            if (!ok) break;
+          }
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            st_shared_v4(row + b * 8192 + ((c ^ (rr & 7)) << 4), v[b * 32 + c * 4],
-                         v[b * 32 + c * 4 + 1], v[b * 32 + c * 4 + 2], v[b * 32 + c * 4 + 3]);
-        }
-        fence_async_smem();
-        mbar_arrive(stg_full + half);
-        if (leader) {
-          for (int hh = 0; hh < 2 && ok; ++hh) {
-            ok = mbar_wait(stg_full + hh, it_g & 1, abort_flag, p.status);
-            if (!ok) break;
+            st_shared_v4(srow + ((c ^ (r & 7)) << 4), va[c * 4], va[c * 4 + 1], va[c * 4 + 2],
+                         va[c * 4 + 3]);
 #pragma unroll
-            for (int b = 0; b < D / 32; ++b)
-              tma_reduce_add_3d(&tmap_dq, smem + C::OFF_STG + b * 8192, 32 * b,
-                                qt * kBM + 64 * hh, plane);
-            bulk_commit_group();
-            bulk_wait_read_all();
-            mbar_arrive(stg_read + hh);
-          }
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(srow + 16384 + ((c ^ (r & 7)) << 4), vb[c * 4], vb[c * 4 + 1],
+                         vb[c * 4 + 2], vb[c * 4 + 3]);
+          fence_async_smem();
+          mbar_arrive(stg_full);
+          ++rnd;
         }
-        ok = __all_sync(0xffffffffu, ok);
         ++it_g;
-        if (!ok) break;
       }
       if (!ok) break;
     }
-    if (leader) bulk_wait_all();  // the reductions finish before the CTA's memory goes
+  } else if (warp == 2 && !aborted_at_start) {
+    // ------------------------------------------------------------ dQ reductions
+    if (lane == 0) {
+      uint32_t rnd = 0, kq = 0;
+      bool ok = true;
+      while (ok) {
+        int w;
+        if (!ring_take(ring, kq++, abort_flag, p.status, w) || w < 0) break;
+        const BUnit u = decode_bunit(p, w);
+        for (int i = 0; i < u.n_it && ok; ++i) {
+          const int h = u.g * p.G + i / u.nq;
+          const int qt = u.qt_lo + i % u.nq;
+          const int plane = u.b * p.Hq + h;
+          for (int rd = 0; rd < D / 64; ++rd) {
+            ok = mbar_wait(stg_full, rnd & 1, abort_flag, p.status);
+            if (!ok) break;
+            tma_reduce_add_3d(&tmap_dq, smem + C::OFF_STG, 64 * rd, qt * kBM, plane);
+            tma_reduce_add_3d(&tmap_dq, smem + C::OFF_STG + 16384, 64 * rd + 32, qt * kBM, plane);
+            bulk_commit_group();
+            bulk_wait_read_all();
+            mbar_arrive(stg_read);
+            ++rnd;
+          }
+        }
+      }
+      bulk_wait_all();  // the reductions finish before the CTA's memory goes
+    }
+    __syncwarp();
   }
 
   tc_fence_before();

@@ -111,7 +111,7 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int planes, int rows, in
 // The same for fp16 data.
 bool make_tmap_f16(CUtensorMap* map, const void* base, int planes, int rows, int D);
 // Tensor map for the fp32 dq accumulator [planes, rows, D] (128-byte swizzle,
-// box 32 x 64 x 1), the target of the backward's TMA reduce-adds.
+// box 32 x 128 x 1), the target of the backward's TMA reduce-adds.
 bool make_tmap_dqacc(CUtensorMap* map, void* base, int planes, int rows, int D);
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
