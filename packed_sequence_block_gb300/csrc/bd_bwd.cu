@@ -10,9 +10,9 @@
 //             looping over the G query heads of the group and the query tiles
 //             the plan marks non-empty.  Per iteration (tcgen05, TMEM):
 //               S^T = K Q^T, dP^T = V dO^T          (cols 256, 384)
-//               P^T (bf16), dS^T (fp16) back into TMEM; dS -> smem
+//               P^T (bf16) back into TMEM; dS (fp16) -> smem
 //               dV += P^T dO, dK += dS^T Q          (cols 128, 0)
-//               dQ = dS K                           (cols 384, after dK)
+//               dQ = dS K                           (cols 384, once dS is formed)
 //             four warps read dQ out of TMEM, stage it in shared memory
 //             and adds it into the fp32 accumulator with TMA reductions;
 //             dK, dV leave once per unit.
@@ -196,11 +196,14 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
 // ------------------------------------------------------------------ main kernel
 //
 // Per iteration i (query tile x head of the unit's group), TMEM columns:
-//   dK [0,128)  dV [128,256)  S^T -> P^T [256,384)  dP^T -> dS^T -> dQ [384,512)
+//   dK [0,128)  dV [128,256)  S^T -> P^T [256,384)  dP^T -> dQ [384,512)
 // Tensor-core order (one thread):
 //   dV += P^T_i dO_i | S^T_{i+1} | dK += dS^T_i Q_i | dQ_i = dS_i K | dP^T_{i+1}
 // so that the P/dS work overlaps MMAs: dS_i is formed while dV_i and S^T_{i+1}
-// run, P_{i+1} while dK_i, dQ_i and dP^T_{i+1} run.  Two warpgroups share
+// run, P_{i+1} while dK_i, dQ_i and dP^T_{i+1} run.  dS_i lives only in
+// shared memory (the A operand of both dK_i and dQ_i), so dQ_i can take the
+// dP^T columns as soon as dS_i is formed.  (dK_i goes first: the dQ read-out
+// then starts later but finds the staging buffer free sooner.)  Two warpgroups share
 // that work by query columns (64 each), which puts two such warps on every
 // scheduler.  Each keeps P_i between its two phases as the bf16 pairs it
 // hands to the dV MMA (32 registers) and forms dS = P (dP - Delta) in fp32
@@ -365,6 +368,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(d, a_tmem + ks * 8 + (ks >= 4 ? 32 : 0),
                  make_sdesc_sw128(b + ks * 2048, 16384, 1024), idesc, (acc || ks > 0));
       };
+      // dK[keys, D] += dS^T[keys, queries] * Q[queries, D]: the dS tile (key rows,
+      // queries contiguous) is the K-major A operand, Q the MN-major B operand
+      auto issue_dk = [&](uint32_t b, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tDK, make_sdesc_sw128(sds + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                 make_sdesc_sw128(b + kk * 2048, 16384, 1024), C::IDESC_DK, acc || kk > 0);
+      };
       // dQ[queries, D] = dS[queries, keys] (MN-major smem) * K[keys, D] (MN-major smem)
       auto issue_dq = [&]() {
 #pragma unroll
@@ -416,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(ds_full, it_g & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
-          issue_ts(tDK, tDP, sq0 + st * C::TILE, i > 0, C::IDESC_DK);
+          issue_dk(sq0 + st * C::TILE, i > 0);
           mma_commit(st_empty + st);  // Q_i is no longer read after dK_i
           issue_dq();
           mma_commit(dq_full);
@@ -450,8 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q4 * 32 + lane;  // key row of the tile = TMEM lane
     const int c0 = 64 * hf;        // first query column of this group
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-    // S^T / dP^T columns of this group; P^T and dS^T (16-bit pairs) go back into
-    // the first half of them, behind the reads
+    // S^T / dP^T columns of this group; P^T (bf16 pairs) goes back into the
+    // first half of its S^T columns, behind the reads
     const uint32_t tS = tmem + lane_off + 256 + c0, tDP = tmem + lane_off + 384 + c0;
     const uint32_t sds_row = smem_u32(smem + C::OFF_DS) + hf * 16384 + (r >> 3) * 1024 +
                              (r & 7) * 128;
@@ -524,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(p_full);
-        // ---- phase dS: dS = P * (dP - Delta) -> TMEM (for dK) and smem (for dQ)
+        // ---- phase dS: dS = P * (dP - Delta) -> smem (the A operand of dK and dQ)
         ok = mbar_wait_warp(dp_full, it_g & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
@@ -544,8 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pack_f16x2(__uint_as_float(pb << 16) * (__uint_as_float(dv[e + 2]) - x.z),
                            __uint_as_float(pb & 0xffff0000u) * (__uint_as_float(dv[e + 3]) - x.w));
           }
-          tmem_st16(tDP + c * 16, dk);
-          // dS (queries contiguous) into the MN-major, 128-byte-swizzled A tile of dQ = dS K
+          // dS (queries contiguous) into the 128-byte-swizzled tile that is the K-major
+          // A operand of dK = dS^T Q and the MN-major A operand of dQ = dS K
 #pragma unroll
           for (int gq = 0; gq < 4; ++gq) {
             const int cq = c * 4 + gq;  // 16-byte chunk index along this group's queries
@@ -553,7 +564,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             st_shared_v4(addr, dk[4 * gq], dk[4 * gq + 1], dk[4 * gq + 2], dk[4 * gq + 3]);
           }
         }
-        tmem_wait_st();
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(ds_full);

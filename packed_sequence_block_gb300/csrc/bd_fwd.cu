@@ -372,24 +372,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           cb = t - k0;
         }
         const bool full = __all_sync(0xffffffffu, ca <= 0 && cb >= kBN - 1);
-        // pass 1: row max of the allowed scores
-        float mx = -INFINITY;
+        // the row's 128 scores in one read; masked ones become -inf, which
+        // neither raises the max nor adds to the sum (exp2(-inf) = 0)
+        uint32_t v[128];
+        tmem_ld128(tS, v);
+        if (!full) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tS + c * 32, v);
-          if (full) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int col = c * 32 + e;
-              const float x = (col >= ca && col <= cb) ? __uint_as_float(v[e]) : -INFINITY;
-              mx = fmaxf(mx, x);
-            }
-          }
+          for (int e = 0; e < kBN; ++e)
+            v[e] = (e >= ca && e <= cb) ? v[e] : 0xff800000u;
         }
+        // row max over four independent chains of three-input maxima
+        float m4[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) m4[j] = fmaxf(__uint_as_float(v[j]), __uint_as_float(v[j + 4]));
+#pragma unroll
+        for (int e = 8; e < kBN; e += 8) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            m4[j] = fmax3(m4[j], __uint_as_float(v[e + j]), __uint_as_float(v[e + 4 + j]));
+        }
+        const float mx = fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
         const float m_tile = mx * p.scale_log2;
         const float m_new = fmaxf(m_used, m_tile);
         float factor = 1.f;
@@ -404,43 +406,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             rescale = true;
           }
         }
+        // P = exp2(s * scale * log2 e - m) as fp16 pairs into the S columns; the
+        // row sum over eight independent partial sums
+        const float m_use = (m_used == -INFINITY) ? 0.f : m_used;
+        float l8[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) l8[j] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float x0 = fast_exp2(fmaf(__uint_as_float(v[c * 32 + e]), p.scale_log2, -m_use));
+            const float x1 =
+                fast_exp2(fmaf(__uint_as_float(v[c * 32 + e + 1]), p.scale_log2, -m_use));
+            l8[(e >> 1) & 7] += x0 + x1;
+            pk[e >> 1] = pack_f16x2(x0, x1);
+          }
+          tmem_st16(tS + c * 16, pk);
+        }
+        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
         if (__any_sync(0xffffffffu, rescale)) {
-          // O holds P_0..P_{jj-1} times V: the S_full wait covered those MMAs
+          // O holds P_0..P_{jj-1} times V (the S_full wait covered those MMAs);
+          // done after P is written, when the scores no longer hold registers
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tO + c * 32, v);
+            uint32_t ov[32];
+            tmem_ld32(tO + c * 32, ov);
             uint32_t a[16], b2[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              a[e] = __float_as_uint(__uint_as_float(v[e]) * factor);
-              b2[e] = __float_as_uint(__uint_as_float(v[16 + e]) * factor);
+              a[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
+              b2[e] = __float_as_uint(__uint_as_float(ov[16 + e]) * factor);
             }
             tmem_st16(tO + c * 32, a);
             tmem_st16(tO + c * 32 + 16, b2);
           }
-        }
-        // pass 2: P = exp2(s * scale * log2 e - m), row sum, bf16 P into TMEM
-        const float m_use = (m_used == -INFINITY) ? 0.f : m_used;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tS + c * 32, v);
-          float pr[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float x = fast_exp2(fmaf(__uint_as_float(v[e]), p.scale_log2, -m_use));
-            if (!full) {
-              const int col = c * 32 + e;
-              x = (col >= ca && col <= cb) ? x : 0.f;
-            }
-            pr[e] = x;
-            l += x;
-          }
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) pk[e] = pack_f16x2(pr[2 * e], pr[2 * e + 1]);
-          tmem_st16(tS + c * 16, pk);
         }
         tmem_wait_st();
         tc_fence_before();
