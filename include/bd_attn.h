@@ -154,11 +154,9 @@ int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int 
  *                256-byte aligned (fp32 dq accumulator and per-row terms).
  * The dq accumulation uses floating-point atomics, so dq may differ in the
  * last bits between runs; dk and dv are deterministic.
- * The products that involve dS = P (dP - Delta) or form S (K Q^T, dS^T Q,
- * dS K) run with fp16 operands: q and k tiles are converted from bf16 in
- * shared memory (exact for |x| in [2^-14, 65504]; larger values become inf,
- * so q and k must stay within the fp16 range), which keeps 11 significant
- * bits of dS instead of bf16's 8.
+ * All five products (K Q^T, V dO^T, P^T dO, dS^T Q, dS K) take bf16
+ * operands with fp32 accumulation; P and dS = P (dP - Delta) are rounded to
+ * bf16 for them.
  */
 size_t bd_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int S, int D);
 int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* out_lo,

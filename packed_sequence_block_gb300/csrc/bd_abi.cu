@@ -105,10 +105,6 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int planes, int rows, in
   return make_tmap_16bit(map, base, planes, rows, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 }
 
-bool make_tmap_f16(CUtensorMap* map, const void* base, int planes, int rows, int D) {
-  return make_tmap_16bit(map, base, planes, rows, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
-}
-
 }  // namespace bd
 
 using namespace bd;
@@ -230,17 +226,15 @@ int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* 
   const BwdLayout wl = bwd_layout(B, Hq, Hkv, L, S, D);
   if (workspace_bytes < wl.total) return BD_ERR_WORKSPACE;
   const AttnDims d = resolve(B, Hq, Hkv, L, S, D, seq_start, scale);
-  // q and k tiles reach the main kernel as the fp16 copies the first stage writes
   CUtensorMap tq, tk, tv, tdo, tdq;
   char* ws = static_cast<char*>(workspace);
-  if (!make_tmap_f16(&tq, ws + wl.q16, B * Hq, L, D) ||
-      !make_tmap_f16(&tk, ws + wl.k16, B * Hkv, S, D) ||
+  if (!make_tmap_bf16(&tq, q, B * Hq, L, D) || !make_tmap_bf16(&tk, k, B * Hkv, S, D) ||
       !make_tmap_bf16(&tv, v, B * Hkv, S, D) || !make_tmap_bf16(&tdo, dout, B * Hq, L, D) ||
       !make_tmap_dqacc(&tdq, ws + wl.dqacc, B * Hq, L, D))
     return BD_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return BD_ERR_CUDA;
-  return launch_bwd(tq, tk, tv, tdo, tdq, d, plan, q, k, out, out_lo, lse, dout, dq, dk, dv, workspace,
+  return launch_bwd(tq, tk, tv, tdo, tdq, d, plan, out, out_lo, lse, dout, dq, dk, dv, workspace,
                     dev_status, stages, sms, stream) == cudaSuccess
              ? BD_OK
              : BD_ERR_CUDA;

@@ -10,7 +10,7 @@
 //             looping over the G query heads of the group and the query tiles
 //             the plan marks non-empty.  Per iteration (tcgen05, TMEM):
 //               S^T = K Q^T, dP^T = V dO^T          (cols 256, 384)
-//               P^T (bf16) back into TMEM; dS (fp16) -> smem
+//               P^T back into TMEM; dS -> smem (both bf16)
 //               dV += P^T dO, dK += dS^T Q          (cols 128, 0)
 //               dQ = dS K                           (cols 384, once dS is formed)
 //             four warps read dQ out of TMEM, stage it in shared memory
@@ -38,21 +38,18 @@ struct BwdCfg {
   // of iteration i), so one buffer suffices: dO_{i+1} loads while dS_i is
   // formed.  The 32 KB this saves hold the dQ staging buffer.
   static constexpr int OFF_DO = OFF_Q + 2 * TILE;
-  static constexpr int OFF_DS = OFF_DO + TILE;        // 128 keys x 128 queries fp16
+  static constexpr int OFF_DS = OFF_DO + TILE;        // 128 keys x 128 queries bf16
   static constexpr int OFF_STG = OFF_DS + 32768;      // 64 columns of dQ_i in fp32
   static constexpr int OFF_LSED = OFF_STG + 32768;    // [2 stages] 128 x float2
   static constexpr int OFF_BAR = OFF_LSED + 2048;
   static constexpr int SMEM = OFF_BAR + 256;  // barriers, TMEM slot, abort flag, work ring
-  // K and Q arrive as fp16 copies (written by the preprocess stage) and dS is
-  // produced in fp16, so the three products that carry dS or feed it
-  // (S^T = K Q^T, dK += dS^T Q, dQ = dS K) run with fp16 operands: 11
-  // significant bits for dS instead of 8.  dP^T = V dO^T and dV += P^T dO
-  // stay bf16.
-  static constexpr uint32_t IDESC_S = make_idesc(128, 128, 0, 0, 0);   // S^T = K Q^T (fp16)
-  static constexpr uint32_t IDESC_DP = make_idesc(128, 128, 0, 0, 1);  // dP^T = V dO^T (bf16)
-  static constexpr uint32_t IDESC_DV = make_idesc(128, D, 0, 1, 1);    // dV += P^T dO (bf16)
-  static constexpr uint32_t IDESC_DK = make_idesc(128, D, 0, 1, 0);    // dK += dS^T Q (fp16)
-  static constexpr uint32_t IDESC_DQ = make_idesc(128, D, 1, 1, 0);    // dQ = dS K (fp16)
+  // All five products take bf16 operands straight from the inputs (P and dS
+  // rounded to bf16), fp32 accumulation in TMEM.
+  static constexpr uint32_t IDESC_S = make_idesc(128, 128, 0, 0, 1);   // S^T = K Q^T
+  static constexpr uint32_t IDESC_DP = make_idesc(128, 128, 0, 0, 1);  // dP^T = V dO^T
+  static constexpr uint32_t IDESC_DV = make_idesc(128, D, 0, 1, 1);    // dV += P^T dO
+  static constexpr uint32_t IDESC_DK = make_idesc(128, D, 0, 1, 1);    // dK += dS^T Q
+  static constexpr uint32_t IDESC_DQ = make_idesc(128, D, 1, 1, 1);    // dQ = dS K
 };
 
 struct BwdParams {
@@ -108,29 +105,16 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 // ------------------------------------------------------------------ preprocess
 
-// One thread per 8 elements of a row.  Threads [0, planes*Lq*TPR) take the
-// query rows (Delta, lse in log2 units, zeroed dq accumulator, fp16 copy of
-// q); the rest convert the key rows to fp16.
+// One thread per 8 elements of a query row: Delta, lse in log2 units and the
+// zeroed dq accumulator.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(
     const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ out_lo,
-    const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
-    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int planes,
-    int kvplanes, int L, int S, int Lq, float* __restrict__ lse2o, float* __restrict__ deltao,
-    float* __restrict__ dqacc,
-    uint4* __restrict__ q16, uint4* __restrict__ k16) {
+    const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse, int planes, int L,
+    int Lq, float* __restrict__ lse2o, float* __restrict__ deltao, float* __restrict__ dqacc) {
   constexpr int TPR = D / 8;  // threads per row (a power of two dividing 32)
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long nq = (long long)planes * Lq * TPR;  // a multiple of 32
-  if (tid >= nq) {
-    const long long t = tid - nq;
-    if (t < (long long)kvplanes * S * TPR) {
-      const uint4 x = reinterpret_cast<const uint4*>(k)[t];
-      k16[t] = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
-                          bf16x2_to_f16x2(x.w));
-    }
-    return;
-  }
+  if (tid >= (long long)planes * Lq * TPR) return;  // a multiple of 32: whole warps leave
   const long long rowg = tid / TPR;
   const int part = static_cast<int>(tid % TPR);
   const int plane = static_cast<int>(rowg / Lq);
@@ -156,9 +140,6 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(
     float4* z = reinterpret_cast<float4*>(dqacc + off);
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const uint4 x = *reinterpret_cast<const uint4*>(q + off);
-    q16[off / 8] = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
-                              bf16x2_to_f16x2(x.w));
   }
   // every lane of the warp takes part in the shuffles (rows past L add 0)
 #pragma unroll
@@ -548,11 +529,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; e += 4) {
             const float4 x = dl4[(c * 32 + e) >> 2];  // Delta of four columns
             const uint32_t pa = pk[c * 16 + (e >> 1)], pb = pk[c * 16 + (e >> 1) + 1];
-            dk[e >> 1] = pack_f16x2(__uint_as_float(pa << 16) * (__uint_as_float(dv[e]) - x.x),
+            dk[e >> 1] = pack_bf16x2(__uint_as_float(pa << 16) * (__uint_as_float(dv[e]) - x.x),
                                     __uint_as_float(pa & 0xffff0000u) *
                                         (__uint_as_float(dv[e + 1]) - x.y));
             dk[(e >> 1) + 1] =
-                pack_f16x2(__uint_as_float(pb << 16) * (__uint_as_float(dv[e + 2]) - x.z),
+                pack_bf16x2(__uint_as_float(pb << 16) * (__uint_as_float(dv[e + 2]) - x.z),
                            __uint_as_float(pb & 0xffff0000u) * (__uint_as_float(dv[e + 3]) - x.w));
           }
           // dS (queries contiguous) into the 128-byte-swizzled tile that is the K-major
@@ -692,9 +673,9 @@ template <int D>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const CUtensorMap& tdo,
                                 const CUtensorMap& tdq,
-                                const BwdParams& p, const void* q, const void* k,
+                                const BwdParams& p,
                                 const void* out, const void* out_lo, const float* lse,
-                                const void* dout, void* dq, void* q16, void* k16, int stages,
+                                const void* dout, void* dq, int stages,
                                 int num_sms,
                                 cudaStream_t stream) {
   using C = BwdCfg<D>;
@@ -709,15 +690,11 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
   }
   const int planes = p.B * p.Hq;
   if (stages & kBwdPrepare) {
-    const long long threads =
-        ((long long)planes * p.Lq + (long long)p.B * p.Hkv * p.S) * (D / 8);
+    const long long threads = (long long)planes * p.Lq * (D / 8);
     bwd_pre_kernel<D><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(out_lo),
-        static_cast<const __nv_bfloat16*>(dout), lse, static_cast<const __nv_bfloat16*>(q),
-        static_cast<const __nv_bfloat16*>(k), planes, p.B * p.Hkv, p.L, p.S, p.Lq,
-        const_cast<float*>(p.lse2), const_cast<float*>(p.delta), p.dqacc,
-        static_cast<uint4*>(q16),
-        static_cast<uint4*>(k16));
+        static_cast<const __nv_bfloat16*>(dout), lse, planes, p.L, p.Lq,
+        const_cast<float*>(p.lse2), const_cast<float*>(p.delta), p.dqacc);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -737,8 +714,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const AttnDims& d,
-                       void* plan, const void* q,
-                       const void* k, const void* out, const void* out_lo, const float* lse,
+                       void* plan, const void* out, const void* out_lo, const float* lse,
                        const void* dout, void* dq, void* dk,
                        void* dv, void* workspace, int32_t* status, int stages, int num_sms,
                        cudaStream_t stream) {
@@ -770,11 +746,10 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.status = status;
   p.ctr = reinterpret_cast<int*>(base + pl.sched) + 2;
-  if (d.D == 64) return launch_bwd_t<64>(tq, tk, tv, tdo, tdq, p, q, k, out, out_lo, lse, dout, dq, ws + wl.q16,
-                                          ws + wl.k16, stages, num_sms,
-                                          stream);
-  return launch_bwd_t<128>(tq, tk, tv, tdo, tdq, p, q, k, out, out_lo, lse, dout, dq, ws + wl.q16,
-                           ws + wl.k16, stages, num_sms,
+  if (d.D == 64)
+    return launch_bwd_t<64>(tq, tk, tv, tdo, tdq, p, out, out_lo, lse, dout, dq, stages, num_sms,
+                            stream);
+  return launch_bwd_t<128>(tq, tk, tv, tdo, tdq, p, out, out_lo, lse, dout, dq, stages, num_sms,
                            stream);
 }
 

@@ -68,13 +68,11 @@ inline PlanLayout plan_layout(int B, int Hq, int Hkv, int L, int S) {
   return p;
 }
 
-// Backward workspace: fp32 dq accumulator [B,Hq,L,D], per-row lse * log2 e
-// [B,Hq,Lq] followed by Delta [B,Hq,Lq] (Lq = ceil(L/128)*128), and fp16
-// copies of q [B,Hq,L,D] and k [B,Hkv,S,D] (the products that carry dS run
-// with fp16 operands).
+// Backward workspace: fp32 dq accumulator [B,Hq,L,D], then per-row
+// lse * log2 e [B,Hq,Lq] followed by Delta [B,Hq,Lq] (Lq = ceil(L/128)*128).
 struct BwdLayout {
   int Lq;
-  size_t dqacc, lsed, q16, k16, total;
+  size_t dqacc, lsed, total;
 };
 
 inline BwdLayout bwd_layout(int B, int Hq, int Hkv, int L, int S, int D) {
@@ -83,8 +81,6 @@ inline BwdLayout bwd_layout(int B, int Hq, int Hkv, int L, int S, int D) {
   size_t off = 0;
   w.dqacc = off; off = align256(off + sizeof(float) * (size_t)B * Hq * L * D);
   w.lsed = off;  off = align256(off + sizeof(float) * 2 * (size_t)B * Hq * w.Lq);
-  w.q16 = off;   off = align256(off + 2 * (size_t)B * Hq * L * D);
-  w.k16 = off;   off = align256(off + 2 * (size_t)B * Hkv * S * D);
   w.total = off;
   return w;
 }
@@ -108,8 +104,6 @@ cudaError_t launch_plan(const int32_t* seg, const int32_t* seg_ids, const int32_
 // Tensor maps for q/k/v-like tensors [planes, rows, D] (bf16, 128-byte swizzle,
 // box 64 x 128 x 1).  Returns false when the driver rejects the map.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int planes, int rows, int D);
-// The same for fp16 data.
-bool make_tmap_f16(CUtensorMap* map, const void* base, int planes, int rows, int D);
 // Tensor map for the fp32 dq accumulator [planes, rows, D] (128-byte swizzle,
 // box 32 x 128 x 1), the target of the backward's TMA reduce-adds.
 bool make_tmap_dqacc(CUtensorMap* map, void* base, int planes, int rows, int D);
@@ -123,10 +117,8 @@ constexpr int kBwdPrepare = 1, kBwdMain = 2, kBwdFinish = 4;
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const AttnDims& d,
-                       void* plan, const void* q,
-                       const void* k, const void* out, const void* out_lo, const float* lse,
-                       const void* dout,
-                       void* dq, void* dk,
+                       void* plan, const void* out, const void* out_lo, const float* lse,
+                       const void* dout, void* dq, void* dk,
                        void* dv, void* workspace, int32_t* status, int stages, int num_sms,
                        cudaStream_t stream);
 
