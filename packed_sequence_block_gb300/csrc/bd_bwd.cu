@@ -23,9 +23,9 @@ namespace bd {
 
 namespace {
 
-// 16 warps: producer, MMA, dQ reduction issuer, one idle warp, two P/dS
-// warpgroups and the dQ readers.
-constexpr int kThreads = 512;
+// 20 warps: producer, MMA, dQ reduction issuer, one idle warp, two P/dS
+// warpgroups and two dQ reader warpgroups (64 columns of dQ each).
+constexpr int kThreads = 640;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -42,7 +42,7 @@ struct BwdCfg {
   static constexpr int OFF_STG = OFF_DS + 32768;      // 64 columns of dQ_i in fp32
   static constexpr int OFF_LSED = OFF_STG + 32768;    // [2 stages] 128 x float2
   static constexpr int OFF_BAR = OFF_LSED + 2048;
-  static constexpr int SMEM = OFF_BAR + 256;  // barriers, TMEM slot, abort flag, work ring
+  static constexpr int SMEM = OFF_BAR + 320;  // barriers, TMEM slot, abort flag, work ring
   // All five products take bf16 operands straight from the inputs (P and dS
   // rounded to bf16), fp32 accumulation in TMEM.
   static constexpr uint32_t IDESC_S = make_idesc(128, 128, 0, 0, 1);   // S^T = K Q^T
@@ -82,6 +82,15 @@ __device__ __forceinline__ BUnit decode_bunit(const BwdParams& p, int w) {
   u.nq = p.bwd_range[2 * ktl + 1] - u.qt_lo + 1;
   u.n_it = u.nq > 0 ? u.nq * p.G : 0;
   return u;
+}
+
+// Iteration i of a unit: query head g*G + i/nq, query tile counted down from
+// the last one the key tile reaches.  Every unit of a document and head then
+// starts on the same tile and the units running side by side walk the same
+// Q/dO tiles and dq-accumulator rows at about the same time, which keeps them
+// in L2.
+__device__ __forceinline__ int unit_qtile(const BUnit& u, int i) {
+  return u.qt_lo + u.nq - 1 - i % u.nq;
 }
 
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
@@ -212,17 +221,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dq_empty = bars + 11;
   uint64_t* dkdv_full = bars + 12;
   uint64_t* drain = bars + 13;
-  // a round of dQ_i is in the staging buffer / the TMA has read it; only the
-  // writers and the issuer wait on these, one phase per round, so neither
-  // side can be two phases behind
-  uint64_t* stg_full = bars + 14;
-  uint64_t* stg_read = bars + 16;
-  uint64_t* do_full = bars + 18;   // dO_i landed
-  uint64_t* do_empty = bars + 19;  // dV_i done: the dO buffer may be refilled
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  // stg_full[s]: a 16 KB box of dQ_i is in staging slot s (the issuer alone
+  // waits, box by box).  stg_read[2 s + g]: the TMA has read the box that
+  // reader group g put in slot s; one phase per iteration each, so a reader
+  // that waits for the other group's box cannot be two phases behind (its own
+  // previous box in the slot may still be unread).
+  uint64_t* stg_full = bars + 14;  // [2]
+  uint64_t* stg_read = bars + 16;  // [4]
+  uint64_t* do_full = bars + 20;   // dO_i landed
+  uint64_t* do_empty = bars + 21;  // dV_i done: the dO buffer may be refilled
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 22);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  WorkRing* ring = reinterpret_cast<WorkRing*>(bars + 21);
-  static_assert(21 * 8 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
+  WorkRing* ring = reinterpret_cast<WorkRing*>(bars + 23);
+  static_assert(23 * 8 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
+  static_assert(C::SMEM <= 232448, "shared memory over the per-block limit");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -243,14 +255,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(p_full, 256);
     mbar_init(ds_full, 256);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128);
+    mbar_init(dq_empty, 2 * D);  // the reader threads that hold dQ columns
     mbar_init(dkdv_full, 1);
     mbar_init(drain, 1);
-    mbar_init(stg_full, 128);
-    mbar_init(stg_read, 1);
+    for (int s = 0; s < 2; ++s) mbar_init(stg_full + s, 128);
+    for (int s = 0; s < 4; ++s) mbar_init(stg_read + s, 1);
     mbar_init(do_full, 1);
     mbar_init(do_empty, 1);
-    ring_init(ring, 14);  // MMA thread, reduction issuer, 8 P/dS warps, 4 dQ readers
+    ring_init(ring, 18);  // MMA thread, reduction issuer, 8 P/dS warps, 8 dQ readers
     fence_mbar_init();
     prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_k);
@@ -288,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int i = 0; i < u.n_it; ++i) {
           const int h = u.g * p.G + i / u.nq;
-          const int qt = u.qt_lo + i % u.nq;
+          const int qt = unit_qtile(u, i);
           const int st = st_it & 1;
           ok = mbar_wait(st_empty + st, ((st_it >> 1) & 1) ^ 1, abort_flag, p.status);
           if (!ok) break;
@@ -467,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kend = p.kend[(size_t)u.b * p.Spad + key];
       bool ok = true;
       for (int i = 0; i < u.n_it; ++i) {
-        const int qt = u.qt_lo + i % u.nq;
+        const int qt = unit_qtile(u, i);
         const int st = st_it & 1;
         // ---- phase P: P^T = exp2(S^T * scale * log2 e - lse * log2 e), masked
         ok = mbar_wait_warp(s_full, it_g & 1, abort_flag, p.status);
@@ -580,60 +592,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
     }
-  } else if (warp >= 12 && !aborted_at_start) {
+  } else if (warp >= 12 && warp < 20 && !aborted_at_start) {
     // ------------------------------------------------------------ dQ readers
-    // dQ_i leaves TMEM in rounds of 64 columns (64 registers a thread); after
-    // the last round's load the MMA warp may reuse the columns.  Each round is
-    // written into the staging buffer as two 128-byte-swizzled boxes of 128
-    // rows x 32 columns, which warp 2 adds into the fp32 accumulator with TMA
-    // reductions, so the reductions never occupy the SM's load/store path.
-    // A round waits until the TMA has read the previous one.
+    // Reader warpgroup rg takes dQ columns [64 rg, 64 rg + 64) of every row in
+    // one TMEM load (64 registers a thread) and hands the columns back at
+    // once, so dP^T_{i+1} never waits for the staging.  Its columns then go
+    // into the staging buffer as two 128-byte-swizzled boxes of 128 rows x 32
+    // columns, box k of the call into 16 KB slot k & 1 once the TMA has read
+    // the slot's previous box; warp 2 adds each box into the fp32 accumulator
+    // with a TMA reduction, so the reductions never occupy the SM's load/store
+    // path.
+    const int rg = (warp - 12) >> 2;
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;  // query row of the tile = TMEM lane
-    const uint32_t tQ = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + 384;
+    const uint32_t tQ = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + 384 + 64 * rg;
     const uint32_t srow = smem_u32(smem + C::OFF_STG) + r * 128;
-    uint32_t it_g = 0, rnd = 0, kq = 0;
+    constexpr uint32_t kBoxes = D / 32;  // boxes per dQ tile
+    const bool active = 64 * rg < D;
+    uint32_t it_g = 0, kq = 0;
+    // box k of the call: slot k & 1, reader group (k mod kBoxes) / 2, and the
+    // slot's previous box k - 2 was read in that box's group's iteration
+    // (k - 2) / kBoxes
+    auto stage_box = [&](const uint32_t (&v)[32], uint32_t k) -> bool {
+      const uint32_t slot = k & 1;
+      if (k >= 2) {
+        const uint32_t kp = k - 2;
+        const uint32_t gp = (kp % kBoxes) >> 1;
+        if (!mbar_wait_warp(stg_read + 2 * slot + gp, (kp / kBoxes) & 1, abort_flag, p.status))
+          return false;
+      }
+      const uint32_t row = srow + slot * 16384;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_shared_v4(row + ((c ^ (r & 7)) << 4), v[c * 4], v[c * 4 + 1], v[c * 4 + 2],
+                     v[c * 4 + 3]);
+      fence_async_smem();
+      mbar_arrive(stg_full + slot);
+      return true;
+    };
     for (;;) {
       int w;
       if (!ring_take_warp(ring, kq++, abort_flag, p.status, w) || w < 0) break;
       const BUnit u = decode_bunit(p, w);
+      if (!active) continue;
       bool ok = true;
       for (int i = 0; i < u.n_it && ok; ++i) {
         ok = mbar_wait_warp(dq_full, it_g & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll
-        for (int rd = 0; rd < D / 64; ++rd) {
-          uint32_t va[32], vb[32];
-          tmem_ld32x2(tQ + 64 * rd, tQ + 64 * rd + 32, va, vb);
-          if (rd == D / 64 - 1) {
-            tc_fence_before();
-            mbar_arrive(dq_empty);  // TMEM columns free again
-          }
-          if (rnd > 0) {
-            ok = mbar_wait_warp(stg_read, (rnd - 1) & 1, abort_flag, p.status);
-            if (!ok) break;
-          }
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_shared_v4(srow + ((c ^ (r & 7)) << 4), va[c * 4], va[c * 4 + 1], va[c * 4 + 2],
-                         va[c * 4 + 3]);
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_shared_v4(srow + 16384 + ((c ^ (r & 7)) << 4), vb[c * 4], vb[c * 4 + 1],
-                         vb[c * 4 + 2], vb[c * 4 + 3]);
-          fence_async_smem();
-          mbar_arrive(stg_full);
-          ++rnd;
-        }
+        uint32_t va[32], vb[32];
+        tmem_ld32x2(tQ, tQ + 32, va, vb);
+        tc_fence_before();
+        mbar_arrive(dq_empty);  // these TMEM columns are free again
+        const uint32_t k = kBoxes * it_g + 2 * rg;
+        ok = stage_box(va, k) && stage_box(vb, k + 1);
         ++it_g;
       }
       if (!ok) break;
     }
   } else if (warp == 2 && !aborted_at_start) {
     // ------------------------------------------------------------ dQ reductions
+    // Box kb (32 columns of one dQ tile) is issued as its own bulk group; once
+    // box kb is in flight, box kb - 1 has had its source read when all groups
+    // but the newest have, and its slot is handed back.
     if (lane == 0) {
-      uint32_t rnd = 0, kq = 0;
+      uint32_t kb = 0, kq = 0;
       bool ok = true;
       while (ok) {
         int w;
@@ -641,19 +664,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const BUnit u = decode_bunit(p, w);
         for (int i = 0; i < u.n_it && ok; ++i) {
           const int h = u.g * p.G + i / u.nq;
-          const int qt = u.qt_lo + i % u.nq;
+          const int qt = unit_qtile(u, i);
           const int plane = u.b * p.Hq + h;
-          for (int rd = 0; rd < D / 64; ++rd) {
-            ok = mbar_wait(stg_full, rnd & 1, abort_flag, p.status);
+          for (int j = 0; j < D / 32; ++j) {
+            const uint32_t slot = kb & 1;
+            ok = mbar_wait(stg_full + slot, (kb >> 1) & 1, abort_flag, p.status);
             if (!ok) break;
-            tma_reduce_add_3d(&tmap_dq, smem + C::OFF_STG, 64 * rd, qt * kBM, plane);
-            tma_reduce_add_3d(&tmap_dq, smem + C::OFF_STG + 16384, 64 * rd + 32, qt * kBM, plane);
+            tma_reduce_add_3d(&tmap_dq, smem + C::OFF_STG + slot * 16384, 32 * j, qt * kBM, plane);
             bulk_commit_group();
-            bulk_wait_read_all();
-            mbar_arrive(stg_read);
-            ++rnd;
+            if (kb >= 1) {
+              bulk_wait_read_but1();
+              const uint32_t kp = kb - 1;
+              mbar_arrive(stg_read + 2 * (kp & 1) + ((kp % (D / 32)) >> 1));
+            }
+            ++kb;
           }
         }
+      }
+      bulk_wait_read_all();
+      if (kb >= 1) {
+        const uint32_t kp = kb - 1;
+        mbar_arrive(stg_read + 2 * (kp & 1) + ((kp % (D / 32)) >> 1));
       }
       bulk_wait_all();  // the reductions finish before the CTA's memory goes
     }
