@@ -197,6 +197,8 @@ class HotPath:
         self.dq = [torch.empty_like(x) for x in self.q_iv]
         self.dk = torch.empty_like(k)
         self.dv = torch.empty_like(v)
+        self.fws = torch.empty(N.bd_attn_fwd_workspace_size(B, Hkv, S, D), dtype=torch.uint8,
+                               device=device)
         self.ws = torch.empty(N.bd_attn_bwd_workspace_size(B, Hq, Hkv, L, S, D),
                               dtype=torch.uint8, device=device)
         self.status = device_status_word(device)
@@ -216,7 +218,7 @@ class HotPath:
             N.bd_attn_plan(self.seg, self.sid, self.nseg, B, Hq, Hkv, L, S, s0, self.plans[i])
             N.bd_attn_fwd(self.q_iv[i], self.k, self.v, B, Hq, Hkv, L, S, D, s0, self.scale,
                           self.gqa, self.plans[i], self.out[i], self.lse[i], self.out_lo[i],
-                          self.status)
+                          self.fws, self.status)
             args = (self.q_iv[i], self.k, self.v, self.out[i], self.lse[i], self.do_iv[i], B, Hq,
                     Hkv, L, S, D, s0, self.scale, self.gqa, self.plans[i], self.dq[i], self.dk,
                     self.dv, self.ws)

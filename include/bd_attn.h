@@ -127,19 +127,23 @@ int bd_attn_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg
  *   out          bf16 [B, Hq, L, D] output.
  *   lse          fp32 [B, Hq, L] output: natural-log log-sum-exp of the
  *                scaled scores of each row (-inf for padding rows).
- *                The P V product runs with fp16 operands (each v tile is
- *                converted from bf16 in shared memory, exact for |x| in
- *                [2^-14, 65504], so v must stay within the fp16 range).
  *   out_lo       optional bf16 [B, Hq, L, D] output (NULL to skip): the
  *                rounding residual bf16(O - out) of the fp32 result O, so
  *                that out + out_lo carries O to about 16 significant bits.
  *                The backward uses it for Delta = <dout, O>; without it
  *                Delta is formed from the bf16 output alone.
+ *   workspace    device scratch of bd_attn_fwd_workspace_size() bytes,
+ *                256-byte aligned, owned by the caller; the call writes an
+ *                fp16 copy of v there first.  The P V product runs with
+ *                fp16 operands (the copy is exact for |x| in [2^-14, 65504];
+ *                larger values become inf, so v must stay within the fp16
+ *                range).  Too small: BD_ERR_WORKSPACE.
  */
+size_t bd_attn_fwd_workspace_size(int B, int Hkv, int S, int D);
 int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L, int S,
                 int D, int seq_start, float scale, int enable_gqa, void* plan,
-                size_t plan_bytes, void* out, float* lse, void* out_lo, int32_t* dev_status,
-                bd_stream_t stream);
+                size_t plan_bytes, void* out, float* lse, void* out_lo, void* workspace,
+                size_t workspace_bytes, int32_t* dev_status, bd_stream_t stream);
 
 /*
  * Backward pass: gradients of sum(out * dout) (the autograd backward of the

@@ -34,8 +34,10 @@ SIGNATURES = {
     "bd_segment_cu_seqlens": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp, _vp]),
     "bd_attn_plan_size": (_c_size, [_c_int] * 5),
     "bd_attn_plan": (_c_int, [_vp, _vp, _vp] + [_c_int] * 6 + [_vp, _c_size, _vp]),
+    "bd_attn_fwd_workspace_size": (_c_size, [_c_int] * 4),
     "bd_attn_fwd": (_c_int, [_vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size,
-                                                               _vp, _vp, _vp, _vp, _vp]),
+                                                               _vp, _vp, _vp, _vp, _c_size,
+                                                               _vp, _vp]),
     "bd_attn_bwd_workspace_size": (_c_size, [_c_int] * 6),
     "bd_attn_bwd": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size, _vp,
                                                          _vp, _vp, _vp, _c_size, _vp, _vp]),
@@ -141,18 +143,24 @@ def bd_attn_plan(seg, seg_ids, nseg, B: int, Hq: int, Hkv: int, L: int, S: int, 
            "bd_attn_plan")
 
 
+def bd_attn_fwd_workspace_size(B: int, Hkv: int, S: int, D: int) -> int:
+    return int(lib().bd_attn_fwd_workspace_size(B, Hkv, S, D))
+
+
 def bd_attn_fwd(q, k, v, B: int, Hq: int, Hkv: int, L: int, S: int, D: int, seq_start: int,
-                scale: float, enable_gqa: bool, plan, out, lse, out_lo=None, dev_status=None,
-                stream=None) -> None:
+                scale: float, enable_gqa: bool, plan, out, lse, out_lo=None, workspace=None,
+                dev_status=None, stream=None) -> None:
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
         _want(t, torch.bfloat16, n)
     if out_lo is not None:
         _want(out_lo, torch.bfloat16, "out_lo")
     _want(lse, torch.float32, "lse")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().bd_attn_fwd(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, L, S, D, seq_start,
                              float(scale), int(bool(enable_gqa)), _ptr(plan),
                              plan.numel() * plan.element_size(), _ptr(out), _ptr(lse),
-                             _ptr(out_lo), _ptr(dev_status), _stream(stream)), "bd_attn_fwd")
+                             _ptr(out_lo), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                             _stream(stream)), "bd_attn_fwd")
 
 
 def bd_attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, L: int, S: int, D: int) -> int:

@@ -94,19 +94,25 @@ def _resolve_scale(scale, D):
     return float(D) ** -0.5 if scale is None else float(scale)
 
 
-def attn_forward(q, k, v, plan, seq_start=0, scale=None, enable_gqa=False, residual=True):
+def attn_forward(q, k, v, plan, seq_start=0, scale=None, enable_gqa=False, residual=True,
+                 workspace=None):
     """out [B,Hq,L,D] bf16, lse [B,Hq,L] fp32 and the rounding residual of out (no autograd).
 
     The residual (bf16, same shape as out, or None when ``residual`` is
     False) lets the backward form Delta = <dout, O> from O at ~16 bits.
+    ``workspace`` (uint8, at least bd_attn_fwd_workspace_size bytes) is
+    allocated here when not given.
     """
     B, Hq, L, D = q.shape
     Hkv, S = k.shape[1], k.shape[2]
+    if workspace is None:
+        workspace = torch.empty(N.bd_attn_fwd_workspace_size(B, Hkv, S, D), dtype=torch.uint8,
+                                device=q.device)
     out = torch.empty_like(q)
     out_lo = torch.empty_like(q) if residual else None
     lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device)
     N.bd_attn_fwd(q, k, v, B, Hq, Hkv, L, S, D, seq_start, _resolve_scale(scale, D), enable_gqa,
-                  plan, out, lse, out_lo, device_status_word(q.device))
+                  plan, out, lse, out_lo, workspace, device_status_word(q.device))
     return out, lse, out_lo
 
 

@@ -105,6 +105,10 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int planes, int rows, in
   return make_tmap_16bit(map, base, planes, rows, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 }
 
+bool make_tmap_f16(CUtensorMap* map, const void* base, int planes, int rows, int D) {
+  return make_tmap_16bit(map, base, planes, rows, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+}
+
 }  // namespace bd
 
 using namespace bd;
@@ -168,30 +172,38 @@ int bd_attn_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg
              : BD_ERR_CUDA;
 }
 
+size_t bd_attn_fwd_workspace_size(int B, int Hkv, int S, int D) {
+  if (B < 1 || Hkv < 1 || S < 1 || D < 1) return 0;
+  return align256(2 * (size_t)B * Hkv * S * D);
+}
+
 int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L, int S,
                 int D, int seq_start, float scale, int enable_gqa, void* plan,
-                size_t plan_bytes, void* out, float* lse, void* out_lo, int32_t* dev_status,
-                bd_stream_t stream) {
+                size_t plan_bytes, void* out, float* lse, void* out_lo, void* workspace,
+                size_t workspace_bytes, int32_t* dev_status, bd_stream_t stream) {
   if (q == nullptr || k == nullptr || v == nullptr || plan == nullptr || out == nullptr ||
-      lse == nullptr)
+      lse == nullptr || workspace == nullptr)
     return BD_ERR_INVALID_ARG;
   if (out_lo != nullptr && !aligned(out_lo, 16)) return BD_ERR_INVALID_ARG;
   int st = check_dims(B, Hq, Hkv, L, S, D, seq_start, enable_gqa);
   if (st != BD_OK) return st;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
-      !aligned(lse, 4) || !aligned(plan, 256))
+      !aligned(lse, 4) || !aligned(plan, 256) || !aligned(workspace, 256))
     return BD_ERR_INVALID_ARG;
   st = check_plan_lists(B, Hq, Hkv, L, S);
   if (st != BD_OK) return st;
   if (plan_bytes < plan_layout(B, Hq, Hkv, L, S).total) return BD_ERR_WORKSPACE;
+  if (workspace_bytes < bd_attn_fwd_workspace_size(B, Hkv, S, D)) return BD_ERR_WORKSPACE;
   const AttnDims d = resolve(B, Hq, Hkv, L, S, D, seq_start, scale);
+  // the P V product reads v through its fp16 copy in the workspace
   CUtensorMap tq, tk, tv;
   if (!make_tmap_bf16(&tq, q, B * Hq, L, D) || !make_tmap_bf16(&tk, k, B * Hkv, S, D) ||
-      !make_tmap_bf16(&tv, v, B * Hkv, S, D))
+      !make_tmap_f16(&tv, workspace, B * Hkv, S, D))
     return BD_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return BD_ERR_CUDA;
-  return launch_fwd(tq, tk, tv, d, plan, out, out_lo, lse, dev_status, sms, stream) == cudaSuccess
+  return launch_fwd(tq, tk, tv, d, plan, v, workspace, out, out_lo, lse, dev_status, sms,
+                    stream) == cudaSuccess
              ? BD_OK
              : BD_ERR_CUDA;
 }

@@ -10,8 +10,8 @@
 //  * warp 0 streams Q and K/V tiles with TMA (128-byte swizzle) into shared
 //    memory; only the key tiles the plan marks non-empty are loaded;
 //  * warp 1 (one thread) issues tcgen05 MMAs: S_s = Q_s K^T into TMEM, then
-//    O_s += P_s V with P_s read back from TMEM (fp16; warps 2-3 convert each
-//    V tile to fp16 in shared memory as it lands);
+//    O_s += P_s V with P_s read back from TMEM (fp16, with V read from the
+//    fp16 copy that v_to_f16 writes before the kernel starts);
 //  * warpgroups 1 and 2 run the softmax of sub-tile 0 and 1 (one thread per
 //    query row = one TMEM lane): mask, running max, exp2, bf16 P into TMEM,
 //    lazy rescaling of O, and the epilogue O / l -> bf16 plus the fp32 LSE.
@@ -37,9 +37,9 @@ struct FwdCfg {
   static constexpr int OFF_BAR = OFF_V + STAGES * KTILE;
   static constexpr int SMEM = OFF_BAR + 512;
   static constexpr uint32_t IDESC_S = make_idesc_bf16(128, 128, 0, 0);
-  // P V runs with fp16 operands (V tiles converted in shared memory, P <= 2^8
-  // by the rescale threshold): O then carries P to 11 significant bits, and
-  // the backward's Delta = <dO, O> agrees with its own P to that precision.
+  // P V runs with fp16 operands (V from its fp16 copy, P <= 2^8 by the
+  // rescale threshold): O then carries P to 11 significant bits, and the
+  // backward's Delta = <dO, O> agrees with its own P to that precision.
   static constexpr uint32_t IDESC_PV = make_idesc(128, D, 0, 1, 0);
 };
 
@@ -115,8 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 2;                    // [2]
   uint64_t* o_full = p_full + 2;                    // [2]
   uint64_t* drain = o_full + 2;
-  uint64_t* v16_ready = drain + 1;                  // [STAGES] V tile converted to fp16
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(v16_ready + C::STAGES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   WorkRing* ring = reinterpret_cast<WorkRing*>(smem + C::OFF_BAR + 256);
   static_assert(256 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
@@ -143,8 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(o_full + s, 1);
     }
     mbar_init(drain, 1);
-    for (int s = 0; s < C::STAGES; ++s) mbar_init(v16_ready + s, 64);
-    ring_init(ring, 11);  // MMA thread + 2 converter warps + 8 softmax warps
+    ring_init(ring, 9);  // MMA thread + 8 softmax warps
     fence_mbar_init();
     prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_k);
@@ -256,11 +254,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(s_full + 0);
         issue_s(1, st);
         mma_commit(s_full + 1);
+        // only the S products read Q: once the unit's last ones are issued the
+        // producer may load the next unit's Q behind them
+        if (u.n == 1) mma_commit(q_empty);
         for (int jj = 0; jj < u.n && ok; ++jj) {
           const uint32_t it = kv_it + jj;
           const int stj = it % C::STAGES;
           mma_commit(k_empty + stj);  // the S MMAs reading K_jj are all issued
-          ok = mbar_wait(v16_ready + stj, (it / C::STAGES) & 1, abort_flag, p.status);
+          ok = mbar_wait(v_full + stj, (it / C::STAGES) & 1, abort_flag, p.status);
           if (!ok) break;
           const bool last = (jj + 1 == u.n);
           const int stn = (it + 1) % C::STAGES;
@@ -277,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               issue_s(s, stn);
               mma_commit(s_full + s);
+              if (s == 1 && jj + 2 == u.n) mma_commit(q_empty);
             } else {
               mma_commit(o_full + s);
             }
@@ -285,7 +287,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++t_it;
         }
         kv_it += u.n;
-        mma_commit(q_empty);
         ++u_it;
       }
       // teardown: wait for every MMA issued so far
@@ -293,37 +294,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(drain, 0, p.status);
     }
     __syncwarp();
-  } else if ((warp == 2 || warp == 3) && !aborted_at_start) {
-    // ------------------------------------------------------------ V tiles bf16 -> fp16
-    const int t = threadIdx.x - 64;  // 0..63
-    uint32_t v_it = 0, kq = 0;
-    for (;;) {
-      int w;
-      if (!ring_take_warp(ring, kq++, abort_flag, p.status, w) || w < 0) break;
-      const Unit u = decode_unit(p, w);
-      bool ok = true;
-      for (int jj = 0; jj < u.n; ++jj) {
-        const int st = v_it % C::STAGES;
-        ok = mbar_wait_warp(v_full + st, (v_it / C::STAGES) & 1, abort_flag, p.status);
-        if (!ok) break;
-        const uint32_t base = smem_u32(smem + C::OFF_V + st * C::KTILE);
-#pragma unroll 4
-        for (int c = t; c < C::KTILE / 16; c += 64) {
-          uint32_t a, b, cc, d;
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(a), "=r"(b), "=r"(cc), "=r"(d)
-                       : "r"(base + c * 16));
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + c * 16),
-                       "r"(bf16x2_to_f16x2(a)), "r"(bf16x2_to_f16x2(b)),
-                       "r"(bf16x2_to_f16x2(cc)), "r"(bf16x2_to_f16x2(d))
-                       : "memory");
-        }
-        fence_async_smem();
-        mbar_arrive(v16_ready + st);
-        ++v_it;
-      }
-      if (!ok) break;
-    }
   } else if (warp >= 4 && !aborted_at_start) {
     // ------------------------------------------------------------ softmax
     const int wg = (warp - 4) >> 2;  // sub-tile
@@ -409,23 +379,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P = exp2(s * scale * log2 e - m) as fp16 pairs into the S columns; the
         // row sum over eight independent partial sums
         const float m_use = (m_used == -INFINITY) ? 0.f : m_used;
-        float l8[8];
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-m_use, -m_use);
+        float2 l4[4];  // eight partial sums, as pairs
 #pragma unroll
-        for (int j = 0; j < 8; ++j) l8[j] = 0.f;
+        for (int j = 0; j < 4; ++j) l4[j] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float x0 = fast_exp2(fmaf(__uint_as_float(v[c * 32 + e]), p.scale_log2, -m_use));
-            const float x1 =
-                fast_exp2(fmaf(__uint_as_float(v[c * 32 + e + 1]), p.scale_log2, -m_use));
-            l8[(e >> 1) & 7] += x0 + x1;
-            pk[e >> 1] = pack_f16x2(x0, x1);
+            const float2 t = ffma2(make_float2(__uint_as_float(v[c * 32 + e]),
+                                               __uint_as_float(v[c * 32 + e + 1])), sc2, nm2);
+            const float2 x = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+            l4[(e >> 1) & 3] = fadd2(l4[(e >> 1) & 3], x);
+            pk[e >> 1] = pack_f16x2(x.x, x.y);
           }
           tmem_st16(tS + c * 16, pk);
         }
-        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        l += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
         if (__any_sync(0xffffffffu, rescale)) {
           // O holds P_0..P_{jj-1} times V (the S_full wait covered those MMAs);
           // done after P is written, when the scores no longer hold registers
@@ -517,9 +488,30 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
   return cudaGetLastError();
 }
 
+// v (bf16) -> fp16, eight elements a thread per step of a grid-stride loop.
+__global__ void __launch_bounds__(256) v_to_f16_kernel(const uint4* __restrict__ v,
+                                                       uint4* __restrict__ v16, long long n8) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint4 x = v[i];
+    v16[i] = make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
+                        bf16x2_to_f16x2(x.w));
+  }
+}
+
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const AttnDims& d, void* plan, void* out, void* out_lo,
-                       float* lse, int32_t* status, int num_sms, cudaStream_t stream) {
+                       const AttnDims& d, void* plan, const void* v, void* v16, void* out,
+                       void* out_lo, float* lse, int32_t* status, int num_sms,
+                       cudaStream_t stream) {
+  {
+    const long long n8 = (long long)d.B * d.Hkv * d.S * d.D / 8;
+    const long long want = (n8 + 255) / 256;
+    const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
+    v_to_f16_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(v),
+                                                static_cast<uint4*>(v16), n8);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   const PlanLayout pl = plan_layout(d.B, d.Hq, d.Hkv, d.L, d.S);
   char* base = static_cast<char*>(plan);
   FwdParams p{};

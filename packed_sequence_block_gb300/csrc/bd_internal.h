@@ -104,13 +104,17 @@ cudaError_t launch_plan(const int32_t* seg, const int32_t* seg_ids, const int32_
 // Tensor maps for q/k/v-like tensors [planes, rows, D] (bf16, 128-byte swizzle,
 // box 64 x 128 x 1).  Returns false when the driver rejects the map.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int planes, int rows, int D);
+// The same for fp16 data.
+bool make_tmap_f16(CUtensorMap* map, const void* base, int planes, int rows, int D);
 // Tensor map for the fp32 dq accumulator [planes, rows, D] (128-byte swizzle,
 // box 32 x 128 x 1), the target of the backward's TMA reduce-adds.
 bool make_tmap_dqacc(CUtensorMap* map, void* base, int planes, int rows, int D);
 
+// Converts v to fp16 into v16 (the map tv describes v16), then runs the forward.
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const AttnDims& d, void* plan, void* out, void* out_lo,
-                       float* lse, int32_t* status, int num_sms, cudaStream_t stream);
+                       const AttnDims& d, void* plan, const void* v, void* v16, void* out,
+                       void* out_lo, float* lse, int32_t* status, int num_sms,
+                       cudaStream_t stream);
 // Backward stages (bit mask): per-row terms + accumulator zeroing, the main
 // dK/dV/dQ kernel, and the dq conversion.
 constexpr int kBwdPrepare = 1, kBwdMain = 2, kBwdFinish = 4;

@@ -60,11 +60,12 @@ FAKE = 1 << 20  # a non-null, 256-aligned dummy address: never dereferenced on t
 def _fwd(lib, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, B=1, Hq=4, Hkv=2, L=256, S=256, D=64, seq_start=0,
              scale=0.0, gqa=1, plan=FAKE, plan_bytes=1 << 30, out=FAKE, lse=FAKE, lo=None,
-             st=None, stream=None)
+             ws=FAKE, ws_bytes=1 << 30, st=None, stream=None)
     a.update(kw)
     return lib.bd_attn_fwd(a["q"], a["k"], a["v"], a["B"], a["Hq"], a["Hkv"], a["L"], a["S"],
                          a["D"], a["seq_start"], a["scale"], a["gqa"], a["plan"], a["plan_bytes"],
-                         a["out"], a["lse"], a["lo"], a["st"], a["stream"])
+                         a["out"], a["lse"], a["lo"], a["ws"], a["ws_bytes"], a["st"],
+                         a["stream"])
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -80,6 +81,9 @@ def _fwd(lib, **kw):
     (dict(plan=FAKE + 16), 1),
     (dict(plan_bytes=16), 5),
     (dict(lo=FAKE + 2), 1),
+    (dict(ws=None), 1),
+    (dict(ws=FAKE + 16), 1),
+    (dict(ws_bytes=16), 5),
 ])
 def test_fwd_rejects_bad_arguments(lib_, kw, code):
     assert _fwd(lib_, **kw) == code
