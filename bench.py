@@ -207,9 +207,9 @@ class HotPath:
         self.main_events = []
 
     def launches_per_step(self):
-        # ids, segments; per interval: 3 plan kernels, v conversion + forward,
+        # ids, segments; per interval: 2 plan kernels, v conversion + forward,
         # backward preprocess, main and dq conversion
-        return 2 + len(self.wl.seq_starts) * 8
+        return 2 + len(self.wl.seq_starts) * 7
 
     def step(self, time_main=False):
         N, wl = self.N, self.wl

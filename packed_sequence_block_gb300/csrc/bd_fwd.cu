@@ -30,11 +30,15 @@ template <int D>
 struct FwdCfg {
   static constexpr int QTILE = kBM * D * 2;  // bytes of one 128-row bf16 tile
   static constexpr int KTILE = kBN * D * 2;
-  static constexpr int STAGES = (D == 64) ? 3 : 2;
+  // A K stage frees once the S products of its tile are done, a V stage only
+  // once the P V products are: V gets one stage more, so that a V tile loads
+  // over about two periods.
+  static constexpr int KSTAGES = (D == 64) ? 3 : 2;
+  static constexpr int VSTAGES = KSTAGES + 1;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + 2 * QTILE;
-  static constexpr int OFF_V = OFF_K + STAGES * KTILE;
-  static constexpr int OFF_BAR = OFF_V + STAGES * KTILE;
+  static constexpr int OFF_V = OFF_K + KSTAGES * KTILE;
+  static constexpr int OFF_BAR = OFF_V + VSTAGES * KTILE;
   static constexpr int SMEM = OFF_BAR + 512;
   static constexpr uint32_t IDESC_S = make_idesc_bf16(128, 128, 0, 0);
   // P V runs with fp16 operands (V from its fp16 copy, P <= 2^8 by the
@@ -107,11 +111,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;                      // [STAGES]
-  uint64_t* k_empty = k_full + C::STAGES;           // [STAGES]
-  uint64_t* v_full = k_empty + C::STAGES;           // [STAGES]
-  uint64_t* v_empty = v_full + C::STAGES;           // [STAGES]
-  uint64_t* s_full = v_empty + C::STAGES;           // [2]
+  uint64_t* k_full = bars + 2;                      // [KSTAGES]
+  uint64_t* k_empty = k_full + C::KSTAGES;          // [KSTAGES]
+  uint64_t* v_full = k_empty + C::KSTAGES;          // [VSTAGES]
+  uint64_t* v_empty = v_full + C::VSTAGES;          // [VSTAGES]
+  uint64_t* s_full = v_empty + C::VSTAGES;          // [2]
   uint64_t* p_full = s_full + 2;                    // [2]
   uint64_t* o_full = p_full + 2;                    // [2]
   uint64_t* drain = o_full + 2;
@@ -119,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   WorkRing* ring = reinterpret_cast<WorkRing*>(smem + C::OFF_BAR + 256);
   static_assert(256 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
+  static_assert(C::SMEM <= 232448, "shared memory over the per-block limit");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -130,9 +135,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int s = 0; s < C::STAGES; ++s) {
+    for (int s = 0; s < C::KSTAGES; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(k_empty + s, 1);
+    }
+    for (int s = 0; s < C::VSTAGES; ++s) {
       mbar_init(v_full + s, 1);
       mbar_init(v_empty + s, 1);
     }
@@ -182,19 +189,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int jj = 0; jj < u.n; ++jj) {
           const int row = (u.kt_lo + jj) * kBN;
-          const int st = k_it % C::STAGES;
-          ok = mbar_wait(k_empty + st, ((k_it / C::STAGES) & 1) ^ 1, abort_flag, p.status);
+          const int st = k_it % C::KSTAGES;
+          ok = mbar_wait(k_empty + st, ((k_it / C::KSTAGES) & 1) ^ 1, abort_flag, p.status);
           if (!ok) break;
           mbar_arrive_expect_tx(k_full + st, C::KTILE);
           for (int j = 0; j < D / 64; ++j)
             tma_load_3d(smem + C::OFF_K + st * C::KTILE + j * 16384, &tmap_k, k_full + st, 64 * j,
                         row, plane);
           ++k_it;
-          ok = mbar_wait(v_empty + st, ((v_it / C::STAGES) & 1) ^ 1, abort_flag, p.status);
+          const int sv = v_it % C::VSTAGES;
+          ok = mbar_wait(v_empty + sv, ((v_it / C::VSTAGES) & 1) ^ 1, abort_flag, p.status);
           if (!ok) break;
-          mbar_arrive_expect_tx(v_full + st, C::KTILE);
+          mbar_arrive_expect_tx(v_full + sv, C::KTILE);
           for (int j = 0; j < D / 64; ++j)
-            tma_load_3d(smem + C::OFF_V + st * C::KTILE + j * 16384, &tmap_v, v_full + st, 64 * j,
+            tma_load_3d(smem + C::OFF_V + sv * C::KTILE + j * 16384, &tmap_v, v_full + sv, 64 * j,
                         row, plane);
           ++v_it;
         }
@@ -202,14 +210,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // teardown: every issued copy must land before the CTA's memory is released
       if (q_issued) drain_wait(q_full, (u_it - 1) & 1, p.status);
-      for (int st = 0; st < C::STAGES; ++st) {
+      for (int st = 0; st < C::KSTAGES; ++st) {
         if (k_it > static_cast<uint32_t>(st)) {
-          const uint32_t last = k_it - 1 - ((k_it - 1 - st) % C::STAGES);
-          drain_wait(k_full + st, (last / C::STAGES) & 1, p.status);
+          const uint32_t last = k_it - 1 - ((k_it - 1 - st) % C::KSTAGES);
+          drain_wait(k_full + st, (last / C::KSTAGES) & 1, p.status);
         }
+      }
+      for (int st = 0; st < C::VSTAGES; ++st) {
         if (v_it > static_cast<uint32_t>(st)) {
-          const uint32_t last = v_it - 1 - ((v_it - 1 - st) % C::STAGES);
-          drain_wait(v_full + st, (last / C::STAGES) & 1, p.status);
+          const uint32_t last = v_it - 1 - ((v_it - 1 - st) % C::VSTAGES);
+          drain_wait(v_full + st, (last / C::VSTAGES) & 1, p.status);
         }
       }
     }
@@ -246,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u.n <= 0) continue;
         ok = mbar_wait(q_full, u_it & 1, abort_flag, p.status);
         if (!ok) break;
-        int st = kv_it % C::STAGES;
-        ok = mbar_wait(k_full + st, (kv_it / C::STAGES) & 1, abort_flag, p.status);
+        int st = kv_it % C::KSTAGES;
+        ok = mbar_wait(k_full + st, (kv_it / C::KSTAGES) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
         issue_s(0, st);
@@ -259,20 +269,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u.n == 1) mma_commit(q_empty);
         for (int jj = 0; jj < u.n && ok; ++jj) {
           const uint32_t it = kv_it + jj;
-          const int stj = it % C::STAGES;
+          const int stj = it % C::KSTAGES, svj = it % C::VSTAGES;
           mma_commit(k_empty + stj);  // the S MMAs reading K_jj are all issued
-          ok = mbar_wait(v_full + stj, (it / C::STAGES) & 1, abort_flag, p.status);
+          ok = mbar_wait(v_full + svj, (it / C::VSTAGES) & 1, abort_flag, p.status);
           if (!ok) break;
           const bool last = (jj + 1 == u.n);
-          const int stn = (it + 1) % C::STAGES;
+          const int stn = (it + 1) % C::KSTAGES;
           for (int s = 0; s < 2 && ok; ++s) {
             ok = mbar_wait(p_full + s, t_it & 1, abort_flag, p.status);
             if (!ok) break;
             tc_fence_after();
-            issue_pv(s, stj, jj > 0);
+            issue_pv(s, svj, jj > 0);
             if (!last) {
               if (s == 0) {
-                ok = mbar_wait(k_full + stn, ((it + 1) / C::STAGES) & 1, abort_flag, p.status);
+                ok = mbar_wait(k_full + stn, ((it + 1) / C::KSTAGES) & 1, abort_flag, p.status);
                 if (!ok) break;
                 tc_fence_after();
               }
@@ -283,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_commit(o_full + s);
             }
           }
-          mma_commit(v_empty + stj);
+          mma_commit(v_empty + svj);
           ++t_it;
         }
         kv_it += u.n;

@@ -23,54 +23,36 @@ __device__ __forceinline__ int find_segment(const int32_t* __restrict__ seg, int
   return lo - 1;
 }
 
-__global__ void __launch_bounds__(256) plan_rows_kernel(const int32_t* __restrict__ seg_all,
-                                                        const int32_t* __restrict__ seg_ids_all,
-                                                        const int32_t* __restrict__ nseg, int L,
-                                                        int S, int seq_start, int Lpad, int Spad,
-                                                        int32_t* __restrict__ qlo,
-                                                        int32_t* __restrict__ kend,
-                                                        int32_t* __restrict__ sched) {
-  const int b = blockIdx.y;
-  const int x = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b == 0 && x < 8) sched[x] = 0;
-  const int32_t* seg = seg_all + (size_t)b * (S + 1);
-  const int32_t* sid = seg_ids_all + (size_t)b * S;
-  const int n = nseg[b];
-  if (x < Lpad) {
-    int32_t lo = kPadLo;
-    if (x < L) {
-      const int t = seq_start + x;
-      const int k = find_segment(seg, n, t);
-      if (sid[k] != 0) lo = seg[k];
-    }
-    qlo[(size_t)b * Lpad + x] = lo;
-  }
-  if (x < Spad) {
-    int32_t e = x;
-    if (x < S) {
-      const int k = find_segment(seg, n, x);
-      if (sid[k] != 0) e = seg[k + 1];
-    }
-    kend[(size_t)b * Spad + x] = e;
-  }
-}
-
-// One warp per forward query block or backward key tile.
-__global__ void __launch_bounds__(256) plan_tiles_kernel(const int32_t* __restrict__ qlo,
-                                                         const int32_t* __restrict__ kend, int B,
-                                                         int L, int seq_start, int NQB, int QROWS,
-                                                         int Lpad, int NKT, int Spad,
-                                                         int32_t* __restrict__ fwd_range,
-                                                         int32_t* __restrict__ bwd_range) {
+// One warp per forward query block or backward key tile.  The warp of a
+// query block first writes the mask bound qlo of each of its rows, the warp
+// of a key tile the segment end kend of each of its keys (both from a binary
+// search of the row's segment list), then reduces them to the block's
+// non-empty tile range.  Warp 0 also zeroes the work counters.
+__global__ void __launch_bounds__(256) plan_tiles_kernel(
+    const int32_t* __restrict__ seg_all, const int32_t* __restrict__ seg_ids_all,
+    const int32_t* __restrict__ nseg, int B, int L, int S, int seq_start, int NQB, int QROWS,
+    int Lpad, int NKT, int Spad, int32_t* __restrict__ qlo, int32_t* __restrict__ kend,
+    int32_t* __restrict__ fwd_range, int32_t* __restrict__ bwd_range,
+    int32_t* __restrict__ sched) {
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  if (w == 0 && lane < 8) sched[lane] = 0;
   const int nf = B * NQB;
   if (w < nf) {
     const int b = w / NQB, qb = w % NQB;
+    const int32_t* seg = seg_all + (size_t)b * (S + 1);
+    const int32_t* sid = seg_ids_all + (size_t)b * S;
+    const int n = nseg[b];
     int mn = 0x7fffffff, mx = -1;
     for (int r = lane; r < QROWS; r += 32) {
       const int i = qb * QROWS + r;
-      const int32_t lo = qlo[(size_t)b * Lpad + i];
+      int32_t lo = kPadLo;
+      if (i < L) {
+        const int t = seq_start + i;
+        const int k = find_segment(seg, n, t);
+        if (sid[k] != 0) lo = seg[k];
+      }
+      qlo[(size_t)b * Lpad + i] = lo;
       if (lo != kPadLo) {
         mn = min(mn, lo);
         mx = max(mx, seq_start + i);
@@ -89,10 +71,18 @@ __global__ void __launch_bounds__(256) plan_tiles_kernel(const int32_t* __restri
   } else if (w < nf + B * NKT) {
     const int u = w - nf;
     const int b = u / NKT, kt = u % NKT;
+    const int32_t* seg = seg_all + (size_t)b * (S + 1);
+    const int32_t* sid = seg_ids_all + (size_t)b * S;
+    const int n = nseg[b];
     int mn = 0x7fffffff, mx = -1;
     for (int r = lane; r < kBN; r += 32) {
       const int p = kt * kBN + r;
-      const int32_t e = kend[(size_t)b * Spad + p];
+      int32_t e = p;
+      if (p < S) {
+        const int k = find_segment(seg, n, p);
+        if (sid[k] != 0) e = seg[k + 1];
+      }
+      kend[(size_t)b * Spad + p] = e;
       if (e > p) {
         mn = min(mn, p);
         mx = max(mx, e);
@@ -119,18 +109,35 @@ __global__ void __launch_bounds__(256) plan_tiles_kernel(const int32_t* __restri
 // One CTA; bitonic sort of 64-bit keys in shared memory.
 constexpr int kSortThreads = 1024;
 
+// Key of entry i: cost descending, then index ascending (all keys distinct).
+__device__ __forceinline__ unsigned long long sort_key(const int32_t* __restrict__ range, int i) {
+  const int cost = max(0, range[2 * i + 1] - range[2 * i] + 1);
+  return (static_cast<unsigned long long>(0x7fffffffu - static_cast<unsigned>(cost)) << 32) |
+         static_cast<unsigned>(i);
+}
+
+// Lists of up to kRankSortMax entries: the position of an entry is the number
+// of smaller keys, one comparison pass per entry.
+constexpr int kRankSortMax = 2048;
+
 __device__ void sort_desc(const int32_t* __restrict__ range, int n, int32_t* __restrict__ order,
                           unsigned long long* keys) {
+  if (n <= kRankSortMax) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) keys[i] = sort_key(range, i);
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const unsigned long long ki = keys[i];
+      int rank = 0;
+      for (int j = 0; j < n; ++j) rank += keys[j] < ki;
+      order[rank] = i;
+    }
+    __syncthreads();
+    return;
+  }
   int np = 1;
   while (np < n) np <<= 1;
   for (int i = threadIdx.x; i < np; i += blockDim.x) {
-    unsigned long long key = ~0ull;
-    if (i < n) {
-      const int cost = max(0, range[2 * i + 1] - range[2 * i] + 1);
-      key = (static_cast<unsigned long long>(0x7fffffffu - static_cast<unsigned>(cost)) << 32) |
-            static_cast<unsigned>(i);
-    }
-    keys[i] = key;
+    keys[i] = i < n ? sort_key(range, i) : ~0ull;
   }
   __syncthreads();
   for (int size = 2; size <= np; size <<= 1) {
@@ -176,12 +183,10 @@ cudaError_t launch_plan(const int32_t* seg, const int32_t* seg_ids, const int32_
   int32_t* bo = reinterpret_cast<int32_t*>(base + pl.bwd_order);
   int32_t* sc = reinterpret_cast<int32_t*>(base + pl.sched);
 
-  dim3 g1(cdiv(max(pl.Lpad, pl.Spad), 256), B);
-  plan_rows_kernel<<<g1, 256, 0, stream>>>(seg, seg_ids, nseg, L, S, seq_start, pl.Lpad, pl.Spad,
-                                           qlo, kend, sc);
   const int warps = B * pl.NQB + B * pl.NKT;
   plan_tiles_kernel<<<cdiv(warps * 32, 256), 256, 0, stream>>>(
-      qlo, kend, B, L, seq_start, pl.NQB, pl.QROWS, pl.Lpad, pl.NKT, pl.Spad, fr, br);
+      seg, seg_ids, nseg, B, L, S, seq_start, pl.NQB, pl.QROWS, pl.Lpad, pl.NKT, pl.Spad, qlo,
+      kend, fr, br, sc);
   const int nf = B * pl.NQB, nb = B * pl.NKT;
   int np = 1;
   while (np < max(nf, nb)) np <<= 1;
