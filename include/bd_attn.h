@@ -88,6 +88,68 @@ int bd_segment_cu_seqlens(const int32_t* doc_ids, int B, int S, int32_t* seg, in
                           int32_t* nseg, bd_stream_t stream);
 
 /*
+ * Document ids from per-document lengths (page
+ * "nemo_automodel.components.models.glm5_next.cp", doc_ids_from_seq_lens:
+ * lengths [batch, documents] padded with padding_value, default -1000).
+ *   seq_lens       int32 [B, ndocs]; entries equal to padding_value are not
+ *                  documents and take no number; the others are numbered
+ *                  1..n in order (a zero-length document takes its number).
+ *   ndocs          0 .. 8192 (larger: BD_ERR_UNSUPPORTED).
+ *   doc_ids        int32 [B, S] output; positions past the last document are 0.
+ * A negative length other than padding_value, or a row total above S, zeroes
+ * that row and records BD_ERR_INVALID_ARG in *dev_status (first error wins).
+ */
+int bd_doc_ids_from_seq_lens(const int32_t* seq_lens, int B, int ndocs, int S, int padding_value,
+                             int32_t* doc_ids, int32_t* dev_status, bd_stream_t stream);
+
+/*
+ * Document positions and validity from document ids (page
+ * "nemo_automodel.components.models.inkling2.context_parallel",
+ * unpack_row_layout: integer positions and a padding mask [batch, sequence],
+ * padding decided from the document layout, never from token ids).
+ *   doc_ids    int32 [B, S]; a document is a maximal run of equal non-zero ids.
+ *   positions  int32 [B, S] output: 0, 1, 2, ... along each document; 0 on padding.
+ *   keep       uint8 [B, S] output: 1 on document tokens, 0 on padding.
+ */
+int bd_position_ids_from_doc_ids(const int32_t* doc_ids, int B, int S, int32_t* positions,
+                                 uint8_t* keep, bd_stream_t stream);
+
+/*
+ * Document-position check (page
+ * "nemo_automodel.components.models.inkling2.context_parallel",
+ * validate_document_positions: unit increments inside documents, zero at a
+ * new document; a shard may begin partway through a document; a gap cannot
+ * resume an old one).  Among the kept tokens of a row, in order: the first
+ * may carry any position >= 0; a later one must carry 0, or its
+ * predecessor's position + 1 when it directly follows the predecessor; after
+ * a gap it must carry 0.
+ *   keep       uint8 [B, S] (non-zero = valid token).
+ *   positions  int32 [B, S].
+ *   first_bad  int32 [B] output: first offending column of each row, or -1.
+ * Any offending row also records BD_ERR_INVALID_ARG in *dev_status.
+ */
+int bd_validate_document_positions(const uint8_t* keep, const int32_t* positions, int B, int S,
+                                   int32_t* first_bad, int32_t* dev_status, bd_stream_t stream);
+
+/*
+ * Key/value rows the local queries need (page
+ * "nemo_automodel.components.distributed.blockdiag_cp", cp_blockdiag_sdpa:
+ * K/V delivered by all-gather "or a needed-only halo/a2a exchange").  The
+ * local queries [seq_start, seq_start + L) attend, under the per-document
+ * causal mask, exactly the rows [lo, hi): lo = start of the segment of the
+ * first non-padding local query, hi = one past the last non-padding local
+ * query; lo = hi = seq_start when every local query is padding.
+ *   seg, seg_ids, nseg  as written by bd_segment_cu_seqlens for [B, S].
+ *   range       int32 [B, 2] output: (lo, hi) of each row.
+ *   shard_rows  int32 [B, ceil(S / L)] output, or NULL: rows of [lo, hi) in
+ *               each shard [r L, min((r + 1) L, S)) of the row (the counts an
+ *               all-to-all-v of shards of L rows would move).
+ */
+int bd_kv_needed_range(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg, int B,
+                       int S, int L, int seq_start, int32_t* range, int32_t* shard_rows,
+                       bd_stream_t stream);
+
+/*
  * Attention plan: per-row mask bounds, the non-empty tile ranges of every
  * query block (forward) and key tile (backward), and both work lists sorted
  * longest-first.  This is the "varlen metadata precompute" that the page

@@ -32,6 +32,10 @@ SIGNATURES = {
     "bd_version": (_c_int, []),
     "bd_doc_ids_from_cu_seqlens": (_c_int, [_vp, _vp, _c_int, _c_int, _vp, _vp, _vp]),
     "bd_segment_cu_seqlens": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp, _vp]),
+    "bd_doc_ids_from_seq_lens": (_c_int, [_vp] + [_c_int] * 4 + [_vp, _vp, _vp]),
+    "bd_position_ids_from_doc_ids": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp]),
+    "bd_validate_document_positions": (_c_int, [_vp, _vp, _c_int, _c_int, _vp, _vp, _vp]),
+    "bd_kv_needed_range": (_c_int, [_vp, _vp, _vp] + [_c_int] * 4 + [_vp, _vp, _vp]),
     "bd_attn_plan_size": (_c_size, [_c_int] * 5),
     "bd_attn_plan": (_c_int, [_vp, _vp, _vp] + [_c_int] * 6 + [_vp, _c_size, _vp]),
     "bd_attn_fwd_workspace_size": (_c_size, [_c_int] * 4),
@@ -130,6 +134,47 @@ def bd_segment_cu_seqlens(doc_ids, B: int, S: int, seg, seg_ids, nseg, stream=No
         _want(t, torch.int32, n)
     _check(lib().bd_segment_cu_seqlens(_ptr(doc_ids), B, S, _ptr(seg), _ptr(seg_ids), _ptr(nseg),
                                        _stream(stream)), "bd_segment_cu_seqlens")
+
+
+def bd_doc_ids_from_seq_lens(seq_lens, B: int, ndocs: int, S: int, padding_value: int, doc_ids,
+                             dev_status=None, stream=None) -> None:
+    for t, n in ((seq_lens, "seq_lens"), (doc_ids, "doc_ids")):
+        _want(t, torch.int32, n)
+    _check(lib().bd_doc_ids_from_seq_lens(_ptr(seq_lens), B, ndocs, S, int(padding_value),
+                                          _ptr(doc_ids), _ptr(dev_status), _stream(stream)),
+           "bd_doc_ids_from_seq_lens")
+
+
+def bd_position_ids_from_doc_ids(doc_ids, B: int, S: int, positions, keep, stream=None) -> None:
+    for t, n in ((doc_ids, "doc_ids"), (positions, "positions")):
+        _want(t, torch.int32, n)
+    if keep.dtype not in (torch.uint8, torch.bool):
+        raise ValueError(f"keep must be uint8 or bool, got {keep.dtype}")
+    _check(lib().bd_position_ids_from_doc_ids(_ptr(doc_ids), B, S, _ptr(positions), _ptr(keep),
+                                              _stream(stream)), "bd_position_ids_from_doc_ids")
+
+
+def bd_validate_document_positions(keep, positions, B: int, S: int, first_bad, dev_status=None,
+                                   stream=None) -> None:
+    if keep.dtype not in (torch.uint8, torch.bool):
+        raise ValueError(f"keep must be uint8 or bool, got {keep.dtype}")
+    for t, n in ((positions, "positions"), (first_bad, "first_bad")):
+        _want(t, torch.int32, n)
+    _check(lib().bd_validate_document_positions(_ptr(keep), _ptr(positions), B, S,
+                                                _ptr(first_bad), _ptr(dev_status),
+                                                _stream(stream)),
+           "bd_validate_document_positions")
+
+
+def bd_kv_needed_range(seg, seg_ids, nseg, B: int, S: int, L: int, seq_start: int, kv_range,
+                       shard_rows=None, stream=None) -> None:
+    for t, n in ((seg, "seg"), (seg_ids, "seg_ids"), (nseg, "nseg"), (kv_range, "range")):
+        _want(t, torch.int32, n)
+    if shard_rows is not None:
+        _want(shard_rows, torch.int32, "shard_rows")
+    _check(lib().bd_kv_needed_range(_ptr(seg), _ptr(seg_ids), _ptr(nseg), B, S, L, seq_start,
+                                    _ptr(kv_range), _ptr(shard_rows), _stream(stream)),
+           "bd_kv_needed_range")
 
 
 def bd_attn_plan_size(B: int, Hq: int, Hkv: int, L: int, S: int) -> int:

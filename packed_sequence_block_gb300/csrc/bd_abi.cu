@@ -149,6 +149,50 @@ int bd_segment_cu_seqlens(const int32_t* doc_ids, int B, int S, int32_t* seg, in
                                                                                   : BD_ERR_CUDA;
 }
 
+int bd_doc_ids_from_seq_lens(const int32_t* seq_lens, int B, int ndocs, int S, int padding_value,
+                             int32_t* doc_ids, int32_t* dev_status, bd_stream_t stream) {
+  if (doc_ids == nullptr || B < 1 || S < 1 || ndocs < 0 || (ndocs > 0 && seq_lens == nullptr))
+    return BD_ERR_INVALID_ARG;
+  if (S >= (1 << 30) || B > 65535 || ndocs > kMaxDocsPerRow) return BD_ERR_UNSUPPORTED;
+  return launch_doc_ids_from_lens(seq_lens, B, ndocs, S, padding_value, doc_ids, dev_status,
+                                  stream) == cudaSuccess
+             ? BD_OK
+             : BD_ERR_CUDA;
+}
+
+int bd_position_ids_from_doc_ids(const int32_t* doc_ids, int B, int S, int32_t* positions,
+                                 uint8_t* keep, bd_stream_t stream) {
+  if (doc_ids == nullptr || positions == nullptr || keep == nullptr || B < 1 || S < 1)
+    return BD_ERR_INVALID_ARG;
+  if (S >= (1 << 30)) return BD_ERR_UNSUPPORTED;
+  return launch_position_ids(doc_ids, B, S, positions, keep, stream) == cudaSuccess ? BD_OK
+                                                                                    : BD_ERR_CUDA;
+}
+
+int bd_validate_document_positions(const uint8_t* keep, const int32_t* positions, int B, int S,
+                                   int32_t* first_bad, int32_t* dev_status, bd_stream_t stream) {
+  if (keep == nullptr || positions == nullptr || first_bad == nullptr || B < 1 || S < 1)
+    return BD_ERR_INVALID_ARG;
+  if (S >= (1 << 30)) return BD_ERR_UNSUPPORTED;
+  return launch_validate_positions(keep, positions, B, S, first_bad, dev_status, stream) ==
+                 cudaSuccess
+             ? BD_OK
+             : BD_ERR_CUDA;
+}
+
+int bd_kv_needed_range(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg, int B,
+                       int S, int L, int seq_start, int32_t* range, int32_t* shard_rows,
+                       bd_stream_t stream) {
+  if (seg == nullptr || seg_ids == nullptr || nseg == nullptr || range == nullptr || B < 1 ||
+      S < 1 || L < 1 || seq_start < 0 || static_cast<long long>(seq_start) + L > S)
+    return BD_ERR_INVALID_ARG;
+  if (S >= (1 << 30)) return BD_ERR_UNSUPPORTED;
+  return launch_kv_range(seg, seg_ids, nseg, B, S, L, seq_start, range, shard_rows, stream) ==
+                 cudaSuccess
+             ? BD_OK
+             : BD_ERR_CUDA;
+}
+
 size_t bd_attn_plan_size(int B, int Hq, int Hkv, int L, int S) {
   if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || S < 1) return 0;
   return plan_layout(B, Hq, Hkv, L, S).total;

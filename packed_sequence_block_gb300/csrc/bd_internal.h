@@ -97,6 +97,18 @@ cudaError_t launch_doc_ids(const int32_t* cu, const int32_t* row_ptr, int B, int
                            int32_t* status, cudaStream_t stream);
 cudaError_t launch_segments(const int32_t* ids, int B, int S, int32_t* seg, int32_t* seg_ids,
                             int32_t* nseg, cudaStream_t stream);
+cudaError_t launch_doc_ids_from_lens(const int32_t* lens, int B, int ndocs, int S,
+                                     int padding_value, int32_t* ids, int32_t* status,
+                                     cudaStream_t stream);
+cudaError_t launch_position_ids(const int32_t* ids, int B, int S, int32_t* pos, uint8_t* keep,
+                                cudaStream_t stream);
+cudaError_t launch_validate_positions(const uint8_t* keep, const int32_t* pos, int B, int S,
+                                      int32_t* bad, int32_t* status, cudaStream_t stream);
+cudaError_t launch_kv_range(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg,
+                            int B, int S, int L, int seq_start, int32_t* range,
+                            int32_t* shard_rows, cudaStream_t stream);
+// Largest documents dimension bd_doc_ids_from_seq_lens accepts.
+constexpr int kMaxDocsPerRow = 8192;
 cudaError_t launch_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg, int B,
                         int Hq, int Hkv, int L, int S, int seq_start, void* plan,
                         cudaStream_t stream);

@@ -113,3 +113,18 @@ def test_bwd_and_plan_reject_bad_arguments(lib_):
     assert lib_.bd_segment_cu_seqlens(FAKE, 0, 8, FAKE, FAKE, FAKE, None) == 1
     host = ctypes.c_int32(0)
     assert lib_.bd_get_device_status(None, ctypes.addressof(host), None) == 1
+
+
+def test_layout_entry_points_reject_bad_arguments_on_the_host(lib_):
+    f = lib_.bd_doc_ids_from_seq_lens
+    assert f(FAKE, 1, 8193, 8, -1000, FAKE, None, None) == 2   # too many documents
+    assert f(FAKE, 0, 4, 8, -1000, FAKE, None, None) == 1      # no rows
+    assert f(None, 1, 4, 8, -1000, FAKE, None, None) == 1      # lengths missing
+    g = lib_.bd_position_ids_from_doc_ids
+    assert g(FAKE, 1, 0, FAKE, FAKE, None) == 1
+    assert g(FAKE, 1, 8, None, FAKE, None) == 1
+    h = lib_.bd_validate_document_positions
+    assert h(FAKE, FAKE, 1, 8, None, None, None) == 1
+    k = lib_.bd_kv_needed_range
+    assert k(FAKE, FAKE, FAKE, 1, 8, 4, 5, FAKE, None, None) == 1  # seq_start + L > S
+    assert k(FAKE, FAKE, FAKE, 1, 8, 0, 0, FAKE, None, None) == 1  # L < 1
