@@ -262,6 +262,73 @@ class HotPath:
             h.copy_(d, non_blocking=True)
 
 
+def time_layout_kernels(device, hbm_gbs, reps=20):
+    """Device times of the row-layout kernels at the 8192- and 131072-token rows.
+
+    Bytes are the algorithmic ones (each input read once, each output written
+    once); at these sizes the kernels are bound by launch latency, not HBM.
+    """
+    from packed_sequence_block_gb300 import _native as N
+    from packed_sequence_block_gb300.attention import device_status_word, segment_cu_seqlens
+    out = {}
+    for name in ("lognormal8k", "interval131k"):
+        wl = make_workload(name)
+        B, S, L = wl.B, wl.S, wl.L
+        lens_rows = [np.diff(np.asarray(c, np.int64)) for c in wl.cu]
+        nd = max(len(x) for x in lens_rows)
+        lens = np.full((B, nd), -1000, np.int32)
+        for b, x in enumerate(lens_rows):
+            lens[b, :len(x)] = x
+        lens_d = torch.from_numpy(lens).to(device)
+        ids = torch.empty((B, S), dtype=torch.int32, device=device)
+        pos = torch.empty((B, S), dtype=torch.int32, device=device)
+        keep = torch.empty((B, S), dtype=torch.bool, device=device)
+        bad = torch.empty((B,), dtype=torch.int32, device=device)
+        st = device_status_word(device)
+        N.bd_doc_ids_from_seq_lens(lens_d, B, nd, S, -1000, ids, st)
+        seg, sid, nseg = segment_cu_seqlens(ids)
+        rng_ = torch.empty((B, 2), dtype=torch.int32, device=device)
+        rows = torch.empty((B, -(-S // L)), dtype=torch.int32, device=device)
+        calls = {
+            "doc_ids_from_seq_lens": (lambda: N.bd_doc_ids_from_seq_lens(
+                lens_d, B, nd, S, -1000, ids, st), 4 * B * nd + 4 * B * S),
+            "position_ids_from_doc_ids": (lambda: N.bd_position_ids_from_doc_ids(
+                ids, B, S, pos, keep), 4 * B * S + 5 * B * S),
+            "validate_document_positions": (lambda: N.bd_validate_document_positions(
+                keep, pos, B, S, bad, st), 5 * B * S + 4 * B),
+            "kv_needed_range": (lambda: N.bd_kv_needed_range(
+                seg, sid, nseg, B, S, L, wl.seq_starts[-1], rng_, rows),
+                8 * B * nd + 8 * B + 4 * B * rows.shape[1]),
+        }
+        res = {}
+        for key, (fn, nbytes) in calls.items():
+            # ten back-to-back calls captured as one graph, so that host-side
+            # launch time stays out of the device time measured
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(10):
+                    fn()
+            g.replay()
+            ts = []
+            for _ in range(reps):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g.replay()
+                e1.record()
+                ts.append((e0, e1))
+            torch.cuda.synchronize()
+            us = statistics.median(a.elapsed_time(b) for a, b in ts) * 1e3 / 10
+            gbs = nbytes / (us * 1e-6) / 1e9
+            res[key] = {"us": round(us, 2), "bytes": nbytes, "GB/s": round(gbs, 1),
+                        "frac_of_hbm": round(gbs / hbm_gbs, 4)}
+        out[f"{name}: B={B}, S={S}"] = res
+    return out
+
+
 def flush_l2(buf):
     buf.add_(1)
 
@@ -458,6 +525,7 @@ def main():
     peak = float(peaks["bf16_tflops"])
     clocks = sampler.summary(local)
     traffic, traffic_src = profiled_traffic(args.workload, args.seed)
+    layout_times = time_layout_kernels(device, float(peaks["hbm_gbs"])) if rank == 0 else None
 
     if rank == 0:
         line = {
@@ -485,6 +553,9 @@ def main():
                          "peak_source": f"{peak_src} bf16_tflops (burst)",
                          "avg_launch_ms": main_avg},
             "clocks": clocks,
+            "layout_kernels": {"bound": "launch latency (KB-scale rows); HBM peak "
+                                        f"{float(peaks['hbm_gbs']):.0f} GB/s ({peak_src})",
+                               "timings": layout_times},
         }
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_oracle_sample(wl, args.cpu_budget,

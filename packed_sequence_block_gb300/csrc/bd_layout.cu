@@ -115,92 +115,110 @@ __global__ void __launch_bounds__(kLenThreads) doc_ids_from_lens_kernel(
   ids[(size_t)b * S + p] = id;
 }
 
-// One CTA per row, kScanItems consecutive positions a thread per chunk.  The
-// start of the run holding p is the largest run start <= p: a running
-// maximum carried across the chunks of the row.
+constexpr int kChunk = kScanThreads * kScanItems;
+
+// Largest q in [0, end) with pred(q), searched backwards one chunk at a time
+// by the whole block; -1 when there is none.
+template <typename Pred>
+__device__ __forceinline__ long long last_before(int end, long long* warp_part, Pred pred) {
+  for (int hi = end; hi > 0; hi -= kChunk) {
+    const int lo = hi > kChunk ? hi - kChunk : 0;
+    long long m = LLONG_MIN;
+    for (int q = lo + threadIdx.x; q < hi; q += kScanThreads)
+      if (pred(q)) m = q;
+    long long tot;
+    block_scan_excl<true>(m, warp_part, &tot);
+    if (tot >= 0) return tot;
+  }
+  return -1;
+}
+
+// Grid (ceil(S / kChunk), B): one chunk of one row per block.  The start of
+// the run holding p is the largest run start <= p: the chunk's own starts by
+// a block scan, the run start in force at the chunk's first position by a
+// backward search (position 0 always starts a run, so it ends).
 __global__ void __launch_bounds__(kScanThreads) position_ids_kernel(
     const int32_t* __restrict__ ids_all, int S, int32_t* __restrict__ pos_all,
     uint8_t* __restrict__ keep_all) {
   __shared__ long long warp_part[32];
-  const int b = blockIdx.x;
+  const int b = blockIdx.y;
   const int32_t* ids = ids_all + (size_t)b * S;
   int32_t* pos = pos_all + (size_t)b * S;
   uint8_t* keep = keep_all + (size_t)b * S;
-  long long carry = 0;  // run start in force at the start of the chunk (position 0 starts one)
-  for (int c0 = 0; c0 < S; c0 += kScanThreads * kScanItems) {
-    const int p0 = c0 + threadIdx.x * kScanItems;
-    int32_t id[kScanItems];
-    long long st[kScanItems];
-    long long m = LLONG_MIN;
+  const int c0 = blockIdx.x * kChunk;
+  const long long carry =
+      c0 == 0 ? 0 : last_before(c0, warp_part, [&](int q) { return q == 0 || ids[q] != ids[q - 1]; });
+  const int p0 = c0 + threadIdx.x * kScanItems;
+  int32_t id[kScanItems];
+  long long st[kScanItems];
+  long long m = LLONG_MIN;
 #pragma unroll
-    for (int u = 0; u < kScanItems; ++u) {
-      const int p = p0 + u;
-      id[u] = p < S ? ids[p] : 0;
-      if (p < S && (p == 0 || id[u] != (u > 0 ? id[u - 1] : ids[p - 1]))) m = p;
-      st[u] = m;
-    }
-    long long tot;
-    long long before = block_scan_excl<true>(m, warp_part, &tot);
-    if (carry > before) before = carry;
+  for (int u = 0; u < kScanItems; ++u) {
+    const int p = p0 + u;
+    id[u] = p < S ? ids[p] : 0;
+    if (p < S && (p == 0 || id[u] != (u > 0 ? id[u - 1] : ids[p - 1]))) m = p;
+    st[u] = m;
+  }
+  long long tot;
+  long long before = block_scan_excl<true>(m, warp_part, &tot);
+  if (carry > before) before = carry;
 #pragma unroll
-    for (int u = 0; u < kScanItems; ++u) {
-      const int p = p0 + u;
-      if (p < S) {
-        const long long rs = st[u] > before ? st[u] : before;
-        const bool k = id[u] != 0;
-        pos[p] = k ? static_cast<int32_t>(p - rs) : 0;
-        keep[p] = k ? 1 : 0;
-      }
+  for (int u = 0; u < kScanItems; ++u) {
+    const int p = p0 + u;
+    if (p < S) {
+      const long long rs = st[u] > before ? st[u] : before;
+      const bool k = id[u] != 0;
+      pos[p] = k ? static_cast<int32_t>(p - rs) : 0;
+      keep[p] = k ? 1 : 0;
     }
-    if (tot > carry) carry = tot;
   }
 }
 
-// One CTA per row: the previous kept column of p is the largest kept q < p,
-// a running maximum as above; the first offending column goes to bad[b].
+// Grid (ceil(S / kChunk), B).  The previous kept column of p is the largest
+// kept q < p: within the chunk by a block scan, before it by a backward
+// search.  The smallest offending column of the row goes to bad[b] (bad must
+// hold -1 or a column of the row; rows are reset by a preceding launch).
 __global__ void __launch_bounds__(kScanThreads) validate_positions_kernel(
     const uint8_t* __restrict__ keep_all, const int32_t* __restrict__ pos_all, int S,
     int32_t* __restrict__ bad_all, int32_t* status) {
   __shared__ long long warp_part[32];
   __shared__ int first_bad;
-  const int b = blockIdx.x;
+  const int b = blockIdx.y;
   const uint8_t* keep = keep_all + (size_t)b * S;
   const int32_t* pos = pos_all + (size_t)b * S;
   if (threadIdx.x == 0) first_bad = INT_MAX;
-  long long carry = -1;  // last kept column before the chunk, -1 if none
-  for (int c0 = 0; c0 < S; c0 += kScanThreads * kScanItems) {
-    const int p0 = c0 + threadIdx.x * kScanItems;
-    uint8_t k[kScanItems];
-    long long m = LLONG_MIN;
+  const int c0 = blockIdx.x * kChunk;
+  const long long carry =
+      c0 == 0 ? -1 : last_before(c0, warp_part, [&](int q) { return keep[q] != 0; });
+  const int p0 = c0 + threadIdx.x * kScanItems;
+  uint8_t k[kScanItems];
+  long long m = LLONG_MIN;
 #pragma unroll
-    for (int u = 0; u < kScanItems; ++u) {
-      const int p = p0 + u;
-      k[u] = p < S ? keep[p] : 0;
-      if (k[u]) m = p;
-    }
-    long long tot;
-    long long prev = block_scan_excl<true>(m, warp_part, &tot);
-    if (carry > prev) prev = carry;
+  for (int u = 0; u < kScanItems; ++u) {
+    const int p = p0 + u;
+    k[u] = p < S ? keep[p] : 0;
+    if (k[u]) m = p;
+  }
+  long long tot;
+  long long prev = block_scan_excl<true>(m, warp_part, &tot);
+  if (carry > prev) prev = carry;
 #pragma unroll
-    for (int u = 0; u < kScanItems; ++u) {
-      const int p = p0 + u;
-      if (p < S && k[u]) {
-        const int32_t x = pos[p];
-        bool ok;
-        if (prev < 0) ok = x >= 0;
-        else if (prev == p - 1) ok = x == 0 || x == pos[prev] + 1;
-        else ok = x == 0;
-        if (!ok) atomicMin(&first_bad, p);
-        prev = p;
-      }
+  for (int u = 0; u < kScanItems; ++u) {
+    const int p = p0 + u;
+    if (p < S && k[u]) {
+      const int32_t x = pos[p];
+      bool ok;
+      if (prev < 0) ok = x >= 0;
+      else if (prev == p - 1) ok = x == 0 || x == pos[prev] + 1;
+      else ok = x == 0;
+      if (!ok) atomicMin(&first_bad, p);
+      prev = p;
     }
-    if (tot > carry) carry = tot;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    const int fb = first_bad;
-    bad_all[b] = fb == INT_MAX ? -1 : fb;
-    if (fb != INT_MAX) set_status(status, BD_ERR_INVALID_ARG);
+  if (threadIdx.x == 0 && first_bad != INT_MAX) {
+    atomicMin(reinterpret_cast<unsigned int*>(bad_all + b), static_cast<unsigned int>(first_bad));
+    set_status(status, BD_ERR_INVALID_ARG);
   }
 }
 
@@ -276,13 +294,18 @@ cudaError_t launch_doc_ids_from_lens(const int32_t* lens, int B, int ndocs, int 
 
 cudaError_t launch_position_ids(const int32_t* ids, int B, int S, int32_t* pos, uint8_t* keep,
                                 cudaStream_t stream) {
-  position_ids_kernel<<<B, kScanThreads, 0, stream>>>(ids, S, pos, keep);
+  position_ids_kernel<<<dim3(cdiv(S, kChunk), B), kScanThreads, 0, stream>>>(ids, S, pos, keep);
   return cudaGetLastError();
 }
 
 cudaError_t launch_validate_positions(const uint8_t* keep, const int32_t* pos, int B, int S,
                                       int32_t* bad, int32_t* status, cudaStream_t stream) {
-  validate_positions_kernel<<<B, kScanThreads, 0, stream>>>(keep, pos, S, bad, status);
+  // -1 (all bits set) is the largest unsigned value, so the blocks' unsigned
+  // minimum leaves it only where no block found an offending column
+  cudaError_t e = cudaMemsetAsync(bad, 0xff, sizeof(int32_t) * B, stream);
+  if (e != cudaSuccess) return e;
+  validate_positions_kernel<<<dim3(cdiv(S, kChunk), B), kScanThreads, 0, stream>>>(keep, pos, S,
+                                                                                  bad, status);
   return cudaGetLastError();
 }
 
