@@ -50,7 +50,7 @@ def parse_args():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     return ap.parse_args()
 
 
@@ -211,19 +211,26 @@ class HotPath:
         # backward preprocess, main and dq conversion
         return 2 + len(self.wl.seq_starts) * 7
 
-    def step(self, time_main=False):
+    def _io(self):
+        """This object's own per-step inputs and outputs."""
+        return {"cu": self.cu, "rp": self.rp, "k": self.k, "v": self.v, "q": self.q_iv,
+                "do": self.do_iv, "out": self.out, "lse": self.lse, "dq": self.dq,
+                "dk": self.dk, "dv": self.dv}
+
+    def step(self, time_main=False, io=None):
         N, wl = self.N, self.wl
+        io = io if io is not None else self._io()
         B, S, L, Hq, Hkv, D = wl.B, wl.S, wl.L, wl.Hq, wl.Hkv, wl.D
-        N.bd_doc_ids_from_cu_seqlens(self.cu, self.rp, B, S, self.ids, self.status)
+        N.bd_doc_ids_from_cu_seqlens(io["cu"], io["rp"], B, S, self.ids, self.status)
         N.bd_segment_cu_seqlens(self.ids, B, S, self.seg, self.sid, self.nseg)
         for i, s0 in enumerate(wl.seq_starts):
             N.bd_attn_plan(self.seg, self.sid, self.nseg, B, Hq, Hkv, L, S, s0, self.plans[i])
-            N.bd_attn_fwd(self.q_iv[i], self.k, self.v, B, Hq, Hkv, L, S, D, s0, self.scale,
-                          self.gqa, self.plans[i], self.out[i], self.lse[i], self.out_lo[i],
+            N.bd_attn_fwd(io["q"][i], io["k"], io["v"], B, Hq, Hkv, L, S, D, s0, self.scale,
+                          self.gqa, self.plans[i], io["out"][i], io["lse"][i], self.out_lo[i],
                           self.fws, self.status)
-            args = (self.q_iv[i], self.k, self.v, self.out[i], self.lse[i], self.do_iv[i], B, Hq,
-                    Hkv, L, S, D, s0, self.scale, self.gqa, self.plans[i], self.dq[i], self.dk,
-                    self.dv, self.ws)
+            args = (io["q"][i], io["k"], io["v"], io["out"][i], io["lse"][i], io["do"][i], B, Hq,
+                    Hkv, L, S, D, s0, self.scale, self.gqa, self.plans[i], io["dq"][i],
+                    io["dk"], io["dv"], self.ws)
             N.bd_attn_bwd_stages(*args, out_lo=self.out_lo[i], dev_status=self.status,
                                  stages=1)
             if time_main:
@@ -238,28 +245,69 @@ class HotPath:
             N.bd_attn_bwd_stages(*args, out_lo=self.out_lo[i], dev_status=self.status,
                                  stages=4)
 
-    def e2e_buffers(self):
-        """Pinned host copies of the inputs and room for the results."""
+    def e2e_setup(self):
+        """Pinned host copies of the inputs, and two device/host buffer sets, so that a
+        step's copies in and out overlap the neighbouring steps' compute."""
         pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)  # noqa: E731
+        own = self._io()
+        in_keys, out_keys = ("cu", "rp", "k", "v", "q", "do"), ("out", "lse", "dq", "dk", "dv")
+
+        def flat(io, keys):
+            ts = []
+            for key in keys:
+                ts.extend(io[key] if isinstance(io[key], list) else [io[key]])
+            return ts
+
         self.h_in = []
-        for dev_t in [self.k, self.v, *self.q_iv, *self.do_iv]:
-            h = pin(dev_t)
-            h.copy_(dev_t)
-            self.h_in.append((h, dev_t))
-        self.h_out = [(pin(t), t) for t in [*self.out, *self.lse, *self.dq, self.dk, self.dv]]
-        h2d = sum(h.numel() * h.element_size() for h, _ in self.h_in)
-        h2d += self.cu_h.numel() * 4 + self.rp_h.numel() * 4
-        d2h = sum(h.numel() * h.element_size() for h, _ in self.h_out)
+        for t in flat(own, in_keys):
+            h = pin(t)
+            h.copy_(t)
+            self.h_in.append(h)
+        clone = {k: ([torch.empty_like(x) for x in t] if isinstance(t, list)
+                     else torch.empty_like(t)) for k, t in own.items()}
+        self.sets = []
+        for io in (own, clone):
+            self.sets.append({"io": io, "d_in": flat(io, in_keys), "d_out": flat(io, out_keys),
+                              "h_out": [pin(t) for t in flat(io, out_keys)],
+                              "ev": {n: torch.cuda.Event() for n in ("in", "done", "out")}})
+        self.s_in, self.s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        h2d = sum(h.numel() * h.element_size() for h in self.h_in)
+        d2h = sum(t.numel() * t.element_size() for t in self.sets[0]["d_out"])
         return h2d, d2h
 
-    def e2e_step(self):
-        self.cu.copy_(self.cu_h, non_blocking=True)
-        self.rp.copy_(self.rp_h, non_blocking=True)
-        for h, d in self.h_in:
-            d.copy_(h, non_blocking=True)
-        self.step()
-        for h, d in self.h_out:
-            h.copy_(d, non_blocking=True)
+    def e2e_run(self, n_steps):
+        """n_steps steps through the library with each step's inputs copied in from
+        pinned host memory and its results copied out; returns elapsed ms."""
+        cur = torch.cuda.current_stream()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(cur)
+        self.s_in.wait_event(t0)
+        self.s_out.wait_event(t0)
+        for i in range(n_steps):
+            st = self.sets[i % 2]
+            ev = st["ev"]
+            if i >= 2:
+                self.s_in.wait_event(ev["done"])  # step i-2 no longer reads this set
+            with torch.cuda.stream(self.s_in):
+                for h, d in zip(self.h_in, st["d_in"]):
+                    d.copy_(h, non_blocking=True)
+                ev["in"].record(self.s_in)
+            cur.wait_event(ev["in"])
+            if i >= 2:
+                cur.wait_event(ev["out"])  # step i-2's results have left this set
+            self.step(io=st["io"])
+            ev["done"].record(cur)
+            self.s_out.wait_event(ev["done"])
+            with torch.cuda.stream(self.s_out):
+                for h, d in zip(st["h_out"], st["d_out"]):
+                    h.copy_(d, non_blocking=True)
+                ev["out"].record(self.s_out)
+        for st in self.sets[:min(2, n_steps)]:
+            cur.wait_event(st["ev"]["out"])
+        t1.record(cur)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
 
 
 def time_layout_kernels(device, hbm_gbs, reps=20):
@@ -489,28 +537,16 @@ def main():
     check_device_status(device)
     main_ms = [a.elapsed_time(b) for a, b in hp.main_events]
 
-    # end to end through the public API with host buffers (copies inside the
-    # timed region), captured and replayed the same way
-    h2d, d2h = hp.e2e_buffers()
-    for _ in range(2):
-        hp.e2e_step()
+    # end to end through the public API with host buffers: every step copies its
+    # inputs in from pinned host memory and its results out inside the timed
+    # region, on two copy streams, double-buffered so that they overlap the
+    # neighbouring steps' compute
+    h2d, d2h = hp.e2e_setup()
+    hp.e2e_run(2)
     barrier()
-    e2e_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(e2e_graph):
-        hp.e2e_step()
-    e2e_graph.replay()
-    barrier()
-    e_ms = []
-    for _ in range(args.e2e_steps):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        e2e_graph.replay()
-        e1.record()
-        e_ms.append((e0, e1))
+    e2e_total = hp.e2e_run(args.e2e_steps)
     barrier()
     check_device_status(device)
-    e2e_total = sum(a.elapsed_time(b) for a, b in e_ms)
 
     t = torch.tensor([total_ms, e2e_total], dtype=torch.float64, device=device)
     if world > 1:
@@ -544,7 +580,12 @@ def main():
             "tokens_per_s": tok_s,
             "frac_of_bf16_peak": value / peak,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                    "ms_per_step": e2e_total / args.e2e_steps,
+                    "schedule": "each step's inputs copied in from pinned host memory and its "
+                                "results copied out inside the timed region, on two copy "
+                                "streams, double-buffered to overlap the neighbouring steps' "
+                                "compute"},
             "gpu_launches": hp.launches_per_step() * args.steps,
             "roofline": {"kernel": "bd_bwd_kernel (backward main)", "bound": "tensor",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
