@@ -431,6 +431,20 @@ def useful_pairs_interval(wl, s0):
     return total
 
 
+def max_over_ranks(values, world, device):
+    """Each value's maximum over the ranks (the slowest rank's time); one
+    collective on the timing numbers only, never on the data path."""
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_rate(units_per_rank_step, steps, slowest_ms, world):
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return world * units_per_rank_step * steps / (slowest_ms * 1e-3)
+
+
 def run_reference(args, wl, rank, world):
     if rank != 0:
         return
@@ -548,13 +562,10 @@ def main():
     barrier()
     check_device_status(device)
 
-    t = torch.tensor([total_ms, e2e_total], dtype=torch.float64, device=device)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    total_ms, e2e_total = float(t[0]), float(t[1])
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
-    e2e_value = world * flops_step * args.e2e_steps / (e2e_total * 1e-3) / 1e12
-    tok_s = world * tokens_step * args.steps / (total_ms * 1e-3)
+    total_ms, e2e_total = max_over_ranks([total_ms, e2e_total], world, device)
+    value = job_rate(flops_step, args.steps, total_ms, world) / 1e12
+    e2e_value = job_rate(flops_step, args.e2e_steps, e2e_total, world) / 1e12
+    tok_s = job_rate(tokens_step, args.steps, total_ms, world)
 
     main_avg = statistics.mean(main_ms)
     achieved = flops_bwd_main_step * args.steps / (sum(main_ms) * 1e-3) / 1e12
