@@ -35,12 +35,17 @@ P_ij = exp(s_ij - lse_i), dS_ij = P_ij (<dO_i, v_j> - Delta_i),
 dq_i = scale sum_j dS_ij k_j, dk_j = scale sum_i dS_ij q_i,
 dv_j = sum_i P_ij dO_i (sums over the query heads sharing key head j).
 
+Dropout (``dropout_p``, page "nemo_automodel.components.distributed.blockdiag_cp",
+cp_blockdiag_sdpa) follows oracle/dropout.py.
+
 Every segment is computed on its own with numpy fp64 matrix products; query
 rows of one segment are processed in slices only to bound memory.
 """
 from __future__ import annotations
 
 import numpy as np
+
+from .dropout import keep_mask
 
 PAD_DOC_ID = 0
 
@@ -108,11 +113,15 @@ def _row_slices(t0, t1, n_keys):
         t += step
 
 
-def blockdiag_sdpa_forward(q, k, v, doc_ids, seq_start=0, scale=None, enable_gqa=False):
+def blockdiag_sdpa_forward(q, k, v, doc_ids, seq_start=0, scale=None, enable_gqa=False,
+                           dropout_p=0.0, seed=0, offset=0):
     """out [B,Hq,L,D] and lse [B,Hq,L] in fp64 for block-diagonal causal attention.
 
     ``doc_ids`` is [B, S] (0 == padding).  Query i of q sits at global position
     seq_start + i and attends keys j <= seq_start + i of its own segment.
+    With ``dropout_p`` > 0 the weights P are masked by oracle.dropout.keep_mask
+    (``seed``, ``offset``) and kept ones scaled by 1 / (1 - dropout_p); lse is
+    the softmax's, before dropout.
     """
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
     B, Hq, Hkv, L, S, D = _check(q, k, v, seq_start, enable_gqa)
@@ -136,22 +145,29 @@ def blockdiag_sdpa_forward(q, k, v, doc_ids, seq_start=0, scale=None, enable_gqa
                     m = s.max(axis=1, keepdims=True)
                     row_lse = m + np.log(np.exp(s - m).sum(axis=1, keepdims=True))
                     p = np.exp(s - row_lse)
+                    if dropout_p > 0.0:
+                        p = p * keep_mask(b * Hq + h, np.arange(r0, r1), keys, seed, offset,
+                                          dropout_p) / (1.0 - dropout_p)
                     out[b, h, r0 - seq_start:r1 - seq_start] = p @ v[b, g, start:r1]
                     lse[b, h, r0 - seq_start:r1 - seq_start] = row_lse[:, 0]
     return out, lse
 
 
 def blockdiag_sdpa_backward(q, k, v, dout, doc_ids, seq_start=0, scale=None,
-                            enable_gqa=False, out=None, lse=None):
+                            enable_gqa=False, out=None, lse=None, dropout_p=0.0, seed=0,
+                            offset=0):
     """dq [B,Hq,L,D], dk and dv [B,Hkv,S,D] (fp64): gradient of sum(out * dout).
 
     ``out`` and ``lse`` default to this module's own forward pass.  dk/dv rows
-    of keys no query of the interval attends are 0.
+    of keys no query of the interval attends are 0.  With dropout (mask M,
+    r = 1 / (1 - p)): dv = (P o M r)^T dO and dS = P o (M r dP - Delta), where
+    Delta = <dO, out> still equals sum_j P_ij M_ij r dP_ij.
     """
     q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
     B, Hq, Hkv, L, S, D = _check(q, k, v, seq_start, enable_gqa)
     if out is None or lse is None:
-        out, lse = blockdiag_sdpa_forward(q, k, v, doc_ids, seq_start, scale, enable_gqa)
+        out, lse = blockdiag_sdpa_forward(q, k, v, doc_ids, seq_start, scale, enable_gqa,
+                                          dropout_p, seed, offset)
     ids = np.asarray(doc_ids).reshape(B, S)
     scale = D ** -0.5 if scale is None else float(scale)
     G = Hq // Hkv
@@ -174,8 +190,13 @@ def blockdiag_sdpa_backward(q, k, v, dout, doc_ids, seq_start=0, scale=None,
                     s = scale * (q[b, h, i0:i1] @ kk.T)
                     p = np.where(allowed, np.exp(s - lse[b, h, i0:i1, None]), 0.0)
                     dp = dout[b, h, i0:i1] @ vv.T
+                    pd = p
+                    if dropout_p > 0.0:
+                        mr = keep_mask(b * Hq + h, np.arange(r0, r1), keys, seed, offset,
+                                       dropout_p) / (1.0 - dropout_p)
+                        pd, dp = p * mr, dp * mr
                     ds = p * (dp - delta[b, h, i0:i1, None])
                     dq[b, h, i0:i1] = scale * (ds @ kk)
                     dk[b, g, start:r1] += scale * (ds.T @ q[b, h, i0:i1])
-                    dv[b, g, start:r1] += p.T @ dout[b, h, i0:i1]
+                    dv[b, g, start:r1] += pd.T @ dout[b, h, i0:i1]
     return dq, dk, dv

@@ -12,6 +12,7 @@ import types
 import numpy as np
 import pytest
 
+import test_oracle_dropout as dpins
 import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
@@ -29,10 +30,18 @@ MUTATIONS = {
     "dq_missing_scale": ("dq[b, h, i0:i1] = scale * (ds @ kk)", "dq[b, h, i0:i1] = ds @ kk"),
     "ds_sign": ("ds = p * (dp - delta[b, h, i0:i1, None])",
                 "ds = p * (dp + delta[b, h, i0:i1, None])"),
-    "dv_into_dk": ("dv[b, g, start:r1] += p.T @ dout[b, h, i0:i1]",
-                   "dk[b, g, start:r1] += p.T @ dout[b, h, i0:i1]"),
+    "dv_into_dk": ("dv[b, g, start:r1] += pd.T @ dout[b, h, i0:i1]",
+                   "dk[b, g, start:r1] += pd.T @ dout[b, h, i0:i1]"),
     "dk_uses_k": ("dk[b, g, start:r1] += scale * (ds.T @ q[b, h, i0:i1])",
                   "dk[b, g, start:r1] += scale * (ds.T @ q[b, h, i0:i1][:, ::-1])"),
+    "dropout_unscaled": ("dropout_p) / (1.0 - dropout_p)\n                    out[b, h",
+                         "dropout_p)\n                    out[b, h"),
+    "dropout_dv_undropped": ("dv[b, g, start:r1] += pd.T @ dout[b, h, i0:i1]",
+                             "dv[b, g, start:r1] += p.T @ dout[b, h, i0:i1]"),
+    "dropout_ds_unmasked": ("                        pd, dp = p * mr, dp * mr",
+                            "                        pd = p * mr"),
+    "dropout_mask_local_rows": ("p = p * keep_mask(b * Hq + h, np.arange(r0, r1), keys",
+                                "p = p * keep_mask(b * Hq + h, np.arange(r0, r1) - seq_start, keys"),
     "interval_offset": ("q[b, h, r0 - seq_start:r1 - seq_start] @ k[b, g, start:r1].T",
                         "q[b, h, r0:r1] @ k[b, g, start:r1].T"),
 }
@@ -43,12 +52,14 @@ def _mutant(name):
     old, new = MUTATIONS[name]
     assert src.count(old) >= 1, f"mutation site for {name} not found"
     mod = types.ModuleType(f"oracle_mutant_{name}")
-    exec(compile(src.replace(old, new), SRC, "exec"), mod.__dict__)
+    src = src.replace(old, new).replace("from .dropout import", "from oracle.dropout import")
+    exec(compile(src, SRC, "exec"), mod.__dict__)
     return mod
 
 
 def _pins(orc, monkeypatch):
     monkeypatch.setattr(pins, "orc", orc)
+    monkeypatch.setattr(dpins, "orc", orc)
     checks = [
         lambda: pins.test_golden_tiny_segments(),
         lambda: pins.test_golden_padded_small(),
@@ -59,6 +70,9 @@ def _pins(orc, monkeypatch):
         lambda: pins.test_single_document_is_torch_causal_sdpa(8),
         lambda: pins.test_packed_equals_documents_run_separately(),
         lambda: pins.test_backward_matches_finite_differences(),
+        lambda: dpins.test_dropout_forward_matches_dense_statement(dpins.CASES[1]),
+        lambda: dpins.test_dropout_backward_matches_finite_differences(),
+        lambda: dpins.test_dropout_intervals_concatenate_to_full_rows(),
     ]
     failed = 0
     for c in checks:
@@ -70,7 +84,7 @@ def _pins(orc, monkeypatch):
 
 
 def test_unmutated_oracle_passes_all(monkeypatch):
-    src = open(SRC).read()
+    src = open(SRC).read().replace("from .dropout import", "from oracle.dropout import")
     mod = types.ModuleType("oracle_copy")
     exec(compile(src, SRC, "exec"), mod.__dict__)
     assert _pins(mod, monkeypatch) == 0
