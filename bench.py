@@ -51,6 +51,8 @@ def parse_args():
                     help="seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--dropout-p", type=float, default=0.1,
+                    help="also time the step with attention dropout at this p (0: skip)")
     return ap.parse_args()
 
 
@@ -205,6 +207,7 @@ class HotPath:
         self.scale = D ** -0.5
         self.gqa = Hq != Hkv
         self.main_events = []
+        self.drop = None  # (p, seed, offset) to run the dropout entry points
 
     def launches_per_step(self):
         # ids, segments; per interval: 2 plan kernels, v conversion + forward,
@@ -225,6 +228,17 @@ class HotPath:
         N.bd_segment_cu_seqlens(self.ids, B, S, self.seg, self.sid, self.nseg)
         for i, s0 in enumerate(wl.seq_starts):
             N.bd_attn_plan(self.seg, self.sid, self.nseg, B, Hq, Hkv, L, S, s0, self.plans[i])
+            if self.drop is not None:
+                p, seed, off = self.drop
+                N.bd_attn_fwd_dropout(io["q"][i], io["k"], io["v"], B, Hq, Hkv, L, S, D, s0,
+                                      self.scale, self.gqa, self.plans[i], io["out"][i],
+                                      io["lse"][i], p, seed, off, self.out_lo[i], self.fws,
+                                      self.status)
+                N.bd_attn_bwd_dropout(io["q"][i], io["k"], io["v"], io["out"][i], io["lse"][i],
+                                      io["do"][i], B, Hq, Hkv, L, S, D, s0, self.scale,
+                                      self.gqa, self.plans[i], io["dq"][i], io["dk"], io["dv"],
+                                      self.ws, p, seed, off, self.out_lo[i], self.status)
+                continue
             N.bd_attn_fwd(io["q"][i], io["k"], io["v"], B, Hq, Hkv, L, S, D, s0, self.scale,
                           self.gqa, self.plans[i], io["out"][i], io["lse"][i], self.out_lo[i],
                           self.fws, self.status)
@@ -562,7 +576,34 @@ def main():
     barrier()
     check_device_status(device)
 
-    total_ms, e2e_total = max_over_ranks([total_ms, e2e_total], world, device)
+    # the same step with attention dropout (counter-based mask regenerated in
+    # the backward), graph-replayed like the timed steps above
+    drop_ms = 0.0
+    if args.dropout_p > 0.0:
+        hp.drop = (args.dropout_p, 0x9E3779B97F4A7C15, 0)
+        for _ in range(3):
+            hp.step()
+        drop_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(drop_graph):
+            hp.step()
+        drop_graph.replay()
+        barrier()
+        check_device_status(device)
+        ev = []
+        for _ in range(args.steps):
+            flush_l2(l2_buf)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            drop_graph.replay()
+            e1.record()
+            ev.append((e0, e1))
+        barrier()
+        check_device_status(device)
+        drop_ms = sum(a.elapsed_time(b) for a, b in ev)
+        hp.drop = None
+
+    total_ms, e2e_total, drop_ms = max_over_ranks([total_ms, e2e_total, drop_ms], world, device)
     value = job_rate(flops_step, args.steps, total_ms, world) / 1e12
     e2e_value = job_rate(flops_step, args.e2e_steps, e2e_total, world) / 1e12
     tok_s = job_rate(tokens_step, args.steps, total_ms, world)
@@ -609,6 +650,12 @@ def main():
                                         f"{float(peaks['hbm_gbs']):.0f} GB/s ({peak_src})",
                                "timings": layout_times},
         }
+        if args.dropout_p > 0.0:
+            dv_ = job_rate(flops_step, args.steps, drop_ms, world) / 1e12
+            line["dropout"] = {"p": args.dropout_p, "value": dv_, "unit": "TFLOP/s",
+                               "ms_per_step": drop_ms / args.steps,
+                               "frac_of_bf16_peak": dv_ / peak,
+                               "relative_to_no_dropout": dv_ / value}
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_oracle_sample(wl, args.cpu_budget,
                                                      oracle_inputs(wl, args.seed))

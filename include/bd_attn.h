@@ -233,6 +233,40 @@ int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
                 bd_stream_t stream);
 
 /*
+ * Forward and backward with attention dropout (page
+ * "nemo_automodel.components.distributed.blockdiag_cp", cp_blockdiag_sdpa's
+ * dropout_p, read as torch scaled_dot_product_attention's: dropout acts on
+ * the normalised attention weights, kept weights are scaled by 1 / (1 - p)).
+ * Same arguments and results as bd_attn_fwd / bd_attn_bwd plus
+ *   dropout_p    in [0, 1) (else BD_ERR_INVALID_ARG); 0 is no dropout.
+ *   seed         64-bit key of the generator.
+ *   offset       32-bit stream offset (a different offset draws a different
+ *                mask under the same seed, e.g. one per layer or step).
+ * The mask is a pure function of (seed, offset, batch row b, query head h,
+ * query position t, key position j): weight (t, j) of plane b * Hq + h is
+ * dropped iff word (j & 3) of Philox4x32-10 (Salmon et al., SC'11) at
+ * counter (j >> 2, t, b * Hq + h, offset) under key (seed mod 2^32,
+ * seed >> 32) is below floor(p * 2^32).  t is the global position
+ * (seq_start + i), so query intervals of one row draw the same mask as the
+ * whole row, and the backward regenerates the forward's mask from the same
+ * (seed, offset) with nothing stored in between.  lse stays the log-sum-exp
+ * of the undropped scores; out is the dropped output.  The backward must be
+ * given the forward's dropout_p, seed and offset.
+ */
+int bd_attn_fwd_dropout(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
+                        int L, int S, int D, int seq_start, float scale, int enable_gqa,
+                        void* plan, size_t plan_bytes, void* out, float* lse, void* out_lo,
+                        void* workspace, size_t workspace_bytes, double dropout_p,
+                        uint64_t seed, uint32_t offset, int32_t* dev_status,
+                        bd_stream_t stream);
+int bd_attn_bwd_dropout(const void* q, const void* k, const void* v, const void* out,
+                        const void* out_lo, const float* lse, const void* dout, int B, int Hq,
+                        int Hkv, int L, int S, int D, int seq_start, float scale, int enable_gqa,
+                        void* plan, size_t plan_bytes, void* dq, void* dk, void* dv,
+                        void* workspace, size_t workspace_bytes, double dropout_p, uint64_t seed,
+                        uint32_t offset, int32_t* dev_status, bd_stream_t stream);
+
+/*
  * The backward pass in separately launchable stages (same arguments as
  * bd_attn_bwd plus a bit mask).  Bit 1: per-row terms Delta_i = <dO_i, o_i>
  * and lse in log2 units, and zeroing of the fp32 dq accumulator (both in

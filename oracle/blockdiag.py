@@ -113,15 +113,22 @@ def _row_slices(t0, t1, n_keys):
         t += step
 
 
+def _mask_plane(mask_planes, b, h, Hq):
+    return b * Hq + h if mask_planes is None else int(np.asarray(mask_planes)[b, h])
+
+
 def blockdiag_sdpa_forward(q, k, v, doc_ids, seq_start=0, scale=None, enable_gqa=False,
-                           dropout_p=0.0, seed=0, offset=0):
+                           dropout_p=0.0, seed=0, offset=0, mask_planes=None, mask_pos0=0):
     """out [B,Hq,L,D] and lse [B,Hq,L] in fp64 for block-diagonal causal attention.
 
     ``doc_ids`` is [B, S] (0 == padding).  Query i of q sits at global position
     seq_start + i and attends keys j <= seq_start + i of its own segment.
     With ``dropout_p`` > 0 the weights P are masked by oracle.dropout.keep_mask
     (``seed``, ``offset``) and kept ones scaled by 1 / (1 - dropout_p); lse is
-    the softmax's, before dropout.
+    the softmax's, before dropout.  For a slice of a larger problem,
+    ``mask_planes`` [B, Hq] gives each (row, head) its plane in the whole and
+    ``mask_pos0`` the whole row's position of this row's position 0, so that
+    the slice draws the whole problem's mask.
     """
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
     B, Hq, Hkv, L, S, D = _check(q, k, v, seq_start, enable_gqa)
@@ -146,8 +153,9 @@ def blockdiag_sdpa_forward(q, k, v, doc_ids, seq_start=0, scale=None, enable_gqa
                     row_lse = m + np.log(np.exp(s - m).sum(axis=1, keepdims=True))
                     p = np.exp(s - row_lse)
                     if dropout_p > 0.0:
-                        p = p * keep_mask(b * Hq + h, np.arange(r0, r1), keys, seed, offset,
-                                          dropout_p) / (1.0 - dropout_p)
+                        p = p * keep_mask(_mask_plane(mask_planes, b, h, Hq),
+                                          np.arange(r0, r1) + mask_pos0, keys + mask_pos0,
+                                          seed, offset, dropout_p) / (1.0 - dropout_p)
                     out[b, h, r0 - seq_start:r1 - seq_start] = p @ v[b, g, start:r1]
                     lse[b, h, r0 - seq_start:r1 - seq_start] = row_lse[:, 0]
     return out, lse
@@ -155,19 +163,20 @@ def blockdiag_sdpa_forward(q, k, v, doc_ids, seq_start=0, scale=None, enable_gqa
 
 def blockdiag_sdpa_backward(q, k, v, dout, doc_ids, seq_start=0, scale=None,
                             enable_gqa=False, out=None, lse=None, dropout_p=0.0, seed=0,
-                            offset=0):
+                            offset=0, mask_planes=None, mask_pos0=0):
     """dq [B,Hq,L,D], dk and dv [B,Hkv,S,D] (fp64): gradient of sum(out * dout).
 
     ``out`` and ``lse`` default to this module's own forward pass.  dk/dv rows
     of keys no query of the interval attends are 0.  With dropout (mask M,
     r = 1 / (1 - p)): dv = (P o M r)^T dO and dS = P o (M r dP - Delta), where
-    Delta = <dO, out> still equals sum_j P_ij M_ij r dP_ij.
+    Delta = <dO, out> still equals sum_j P_ij M_ij r dP_ij.  ``mask_planes``
+    and ``mask_pos0`` as in the forward.
     """
     q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
     B, Hq, Hkv, L, S, D = _check(q, k, v, seq_start, enable_gqa)
     if out is None or lse is None:
         out, lse = blockdiag_sdpa_forward(q, k, v, doc_ids, seq_start, scale, enable_gqa,
-                                          dropout_p, seed, offset)
+                                          dropout_p, seed, offset, mask_planes, mask_pos0)
     ids = np.asarray(doc_ids).reshape(B, S)
     scale = D ** -0.5 if scale is None else float(scale)
     G = Hq // Hkv
@@ -192,8 +201,9 @@ def blockdiag_sdpa_backward(q, k, v, dout, doc_ids, seq_start=0, scale=None,
                     dp = dout[b, h, i0:i1] @ vv.T
                     pd = p
                     if dropout_p > 0.0:
-                        mr = keep_mask(b * Hq + h, np.arange(r0, r1), keys, seed, offset,
-                                       dropout_p) / (1.0 - dropout_p)
+                        mr = keep_mask(_mask_plane(mask_planes, b, h, Hq),
+                                       np.arange(r0, r1) + mask_pos0, keys + mask_pos0, seed,
+                                       offset, dropout_p) / (1.0 - dropout_p)
                         pd, dp = p * mr, dp * mr
                     ds = p * (dp - delta[b, h, i0:i1, None])
                     dq[b, h, i0:i1] = scale * (ds @ kk)

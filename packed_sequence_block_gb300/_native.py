@@ -25,6 +25,7 @@ BD_ERR_TIMEOUT = 4
 BD_ERR_WORKSPACE = 5
 
 _c_int, _c_size, _c_float, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p
+_c_double, _c_u64, _c_u32 = ctypes.c_double, ctypes.c_uint64, ctypes.c_uint32
 
 # name -> (restype, argtypes); mirrors include/bd_attn.h
 SIGNATURES = {
@@ -42,9 +43,15 @@ SIGNATURES = {
     "bd_attn_fwd": (_c_int, [_vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size,
                                                                _vp, _vp, _vp, _vp, _c_size,
                                                                _vp, _vp]),
+    "bd_attn_fwd_dropout": (_c_int, [_vp, _vp, _vp] + [_c_int] * 7 + [
+        _c_float, _c_int, _vp, _c_size, _vp, _vp, _vp, _vp, _c_size, _c_double, _c_u64, _c_u32,
+        _vp, _vp]),
     "bd_attn_bwd_workspace_size": (_c_size, [_c_int] * 6),
     "bd_attn_bwd": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size, _vp,
                                                          _vp, _vp, _vp, _c_size, _vp, _vp]),
+    "bd_attn_bwd_dropout": (_c_int, [_vp] * 7 + [_c_int] * 7 + [
+        _c_float, _c_int, _vp, _c_size, _vp, _vp, _vp, _vp, _c_size, _c_double, _c_u64, _c_u32,
+        _vp, _vp]),
     "bd_attn_bwd_stages": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size,
                                                                 _vp, _vp, _vp, _vp, _c_size, _vp,
                                                                 _c_int, _vp]),
@@ -208,6 +215,24 @@ def bd_attn_fwd(q, k, v, B: int, Hq: int, Hkv: int, L: int, S: int, D: int, seq_
                              _stream(stream)), "bd_attn_fwd")
 
 
+def bd_attn_fwd_dropout(q, k, v, B: int, Hq: int, Hkv: int, L: int, S: int, D: int,
+                        seq_start: int, scale: float, enable_gqa: bool, plan, out, lse,
+                        dropout_p: float, seed: int, offset: int = 0, out_lo=None,
+                        workspace=None, dev_status=None, stream=None) -> None:
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _want(t, torch.bfloat16, n)
+    if out_lo is not None:
+        _want(out_lo, torch.bfloat16, "out_lo")
+    _want(lse, torch.float32, "lse")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().bd_attn_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, L, S, D, seq_start,
+                                     float(scale), int(bool(enable_gqa)), _ptr(plan),
+                                     plan.numel() * plan.element_size(), _ptr(out), _ptr(lse),
+                                     _ptr(out_lo), _ptr(workspace), ws_bytes, float(dropout_p),
+                                     int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF,
+                                     _ptr(dev_status), _stream(stream)), "bd_attn_fwd_dropout")
+
+
 def bd_attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, L: int, S: int, D: int) -> int:
     return int(lib().bd_attn_bwd_workspace_size(B, Hq, Hkv, L, S, D))
 
@@ -226,6 +251,25 @@ def bd_attn_bwd(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: i
                              _ptr(dv), _ptr(workspace),
                              workspace.numel() * workspace.element_size(), _ptr(dev_status),
                              _stream(stream)), "bd_attn_bwd")
+
+
+def bd_attn_bwd_dropout(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: int,
+                        D: int, seq_start: int, scale: float, enable_gqa: bool, plan, dq, dk, dv,
+                        workspace, dropout_p: float, seed: int, offset: int = 0, out_lo=None,
+                        dev_status=None, stream=None) -> None:
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"),
+                 (dk, "dk"), (dv, "dv")):
+        _want(t, torch.bfloat16, n)
+    _want(lse, torch.float32, "lse")
+    _check(lib().bd_attn_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo),
+                                     _ptr(lse), _ptr(dout), B, Hq, Hkv, L, S, D, seq_start,
+                                     float(scale), int(bool(enable_gqa)), _ptr(plan),
+                                     plan.numel() * plan.element_size(), _ptr(dq), _ptr(dk),
+                                     _ptr(dv), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
+                                     float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF,
+                                     int(offset) & 0xFFFFFFFF, _ptr(dev_status),
+                                     _stream(stream)), "bd_attn_bwd_dropout")
 
 
 def bd_attn_bwd_stages(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: int,

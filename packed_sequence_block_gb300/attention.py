@@ -95,13 +95,15 @@ def _resolve_scale(scale, D):
 
 
 def attn_forward(q, k, v, plan, seq_start=0, scale=None, enable_gqa=False, residual=True,
-                 workspace=None):
+                 workspace=None, dropout_p: float = 0.0, seed: int = 0, offset: int = 0):
     """out [B,Hq,L,D] bf16, lse [B,Hq,L] fp32 and the rounding residual of out (no autograd).
 
     The residual (bf16, same shape as out, or None when ``residual`` is
     False) lets the backward form Delta = <dout, O> from O at ~16 bits.
     ``workspace`` (uint8, at least bd_attn_fwd_workspace_size bytes) is
-    allocated here when not given.
+    allocated here when not given.  ``dropout_p`` > 0 drops attention weights
+    with the counter-based mask of (seed, offset); the backward must be given
+    the same three values.
     """
     B, Hq, L, D = q.shape
     Hkv, S = k.shape[1], k.shape[2]
@@ -111,13 +113,19 @@ def attn_forward(q, k, v, plan, seq_start=0, scale=None, enable_gqa=False, resid
     out = torch.empty_like(q)
     out_lo = torch.empty_like(q) if residual else None
     lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device)
-    N.bd_attn_fwd(q, k, v, B, Hq, Hkv, L, S, D, seq_start, _resolve_scale(scale, D), enable_gqa,
-                  plan, out, lse, out_lo, workspace, device_status_word(q.device))
+    if dropout_p != 0.0:  # the library rejects p outside [0, 1)
+        N.bd_attn_fwd_dropout(q, k, v, B, Hq, Hkv, L, S, D, seq_start, _resolve_scale(scale, D),
+                              enable_gqa, plan, out, lse, dropout_p, seed, offset, out_lo,
+                              workspace, device_status_word(q.device))
+    else:
+        N.bd_attn_fwd(q, k, v, B, Hq, Hkv, L, S, D, seq_start, _resolve_scale(scale, D),
+                      enable_gqa, plan, out, lse, out_lo, workspace, device_status_word(q.device))
     return out, lse, out_lo
 
 
 def attn_backward(q, k, v, out, lse, dout, plan, seq_start=0, scale=None, enable_gqa=False,
-                  workspace=None, out_lo=None):
+                  workspace=None, out_lo=None, dropout_p: float = 0.0, seed: int = 0,
+                  offset: int = 0):
     """dq, dk, dv (bf16) for the forward above (no autograd)."""
     B, Hq, L, D = q.shape
     Hkv, S = k.shape[1], k.shape[2]
@@ -127,9 +135,14 @@ def attn_backward(q, k, v, out, lse, dout, plan, seq_start=0, scale=None, enable
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
-    N.bd_attn_bwd(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, seq_start,
-                  _resolve_scale(scale, D), enable_gqa, plan, dq, dk, dv, workspace, out_lo,
-                  device_status_word(q.device))
+    if dropout_p != 0.0:
+        N.bd_attn_bwd_dropout(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, seq_start,
+                              _resolve_scale(scale, D), enable_gqa, plan, dq, dk, dv, workspace,
+                              dropout_p, seed, offset, out_lo, device_status_word(q.device))
+    else:
+        N.bd_attn_bwd(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, seq_start,
+                      _resolve_scale(scale, D), enable_gqa, plan, dq, dk, dv, workspace, out_lo,
+                      device_status_word(q.device))
     return dq, dk, dv
 
 
@@ -137,30 +150,44 @@ class BlockdiagAttention(torch.autograd.Function):
     """Autograd wrapper: forward and backward both run the library's kernels."""
 
     @staticmethod
-    def forward(ctx, q, k, v, plan, seq_start, scale, enable_gqa):
+    def forward(ctx, q, k, v, plan, seq_start, scale, enable_gqa, dropout_p=0.0, seed=0,
+                offset=0):
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
-        out, lse, out_lo = attn_forward(q, k, v, plan, seq_start, scale, enable_gqa)
+        out, lse, out_lo = attn_forward(q, k, v, plan, seq_start, scale, enable_gqa,
+                                        dropout_p=dropout_p, seed=seed, offset=offset)
         ctx.save_for_backward(q, k, v, out, lse, plan, out_lo)
-        ctx.args = (seq_start, scale, enable_gqa)
+        ctx.args = (seq_start, scale, enable_gqa, dropout_p, seed, offset)
         ctx.mark_non_differentiable(lse)
         return out, lse
 
     @staticmethod
     def backward(ctx, dout, _dlse):
         q, k, v, out, lse, plan, out_lo = ctx.saved_tensors
-        seq_start, scale, enable_gqa = ctx.args
+        seq_start, scale, enable_gqa, dropout_p, seed, offset = ctx.args
         dq, dk, dv = attn_backward(q, k, v, out, lse, dout.contiguous(), plan, seq_start, scale,
-                                   enable_gqa, out_lo=out_lo)
-        return dq, dk, dv, None, None, None, None
+                                   enable_gqa, out_lo=out_lo, dropout_p=dropout_p, seed=seed,
+                                   offset=offset)
+        return dq, dk, dv, None, None, None, None, None, None, None
+
+
+def _draw_seed() -> int:
+    """A 64-bit dropout seed from torch's default CPU generator (no device sync)."""
+    return int(torch.randint(0, 2 ** 62, (1,), dtype=torch.int64).item())
 
 
 def blockdiag_attention(q, k, v, *, cu_seqlens=None, doc_ids=None, seq_start: int = 0,
-                        scale=None, enable_gqa: bool = False, return_lse: bool = False):
+                        scale=None, enable_gqa: bool = False, return_lse: bool = False,
+                        dropout_p: float = 0.0, dropout_seed=None, dropout_offset: int = 0):
     """Block-diagonal causal attention of q [B,Hq,L,D] against k, v [B,Hkv,S,D].
 
     The mask comes from ``doc_ids`` [B, S] (0 == padding) or, when those are
     not given, from ``cu_seqlens`` (one row's boundaries or a list of rows).
+    ``dropout_p`` in [0, 1) drops attention weights (kept ones scaled by
+    1 / (1 - p)); the mask is a function of (dropout_seed, dropout_offset) and
+    the positions, and the seed is drawn from torch's generator when None.
     """
+    if not 0.0 <= float(dropout_p) < 1.0:
+        raise ValueError("dropout_p must lie in [0, 1)")
     S = k.shape[2]
     if doc_ids is None:
         if cu_seqlens is None:
@@ -170,25 +197,33 @@ def blockdiag_attention(q, k, v, *, cu_seqlens=None, doc_ids=None, seq_start: in
     if seg_ids.shape[0] != q.shape[0]:
         raise ValueError("document ids must have one row per batch row")
     plan = make_plan(seg, seg_ids, nseg, q.shape[1], k.shape[1], q.shape[2], seq_start)
-    out, lse = BlockdiagAttention.apply(q, k, v, plan, seq_start, scale, enable_gqa)
+    seed = 0
+    if dropout_p > 0.0:
+        seed = _draw_seed() if dropout_seed is None else int(dropout_seed)
+    out, lse = BlockdiagAttention.apply(q, k, v, plan, seq_start, scale, enable_gqa,
+                                        float(dropout_p), seed, int(dropout_offset))
     return (out, lse) if return_lse else out
 
 
 def cp_blockdiag_sdpa(query, key, value, attn_mask=None, dropout_p: float = 0.0,
                       is_causal: bool = False, scale=None, enable_gqa: bool = False, *,
-                      doc_ids=None, cu_seqlens=None, seq_start: int = 0, **kwargs):
+                      doc_ids=None, cu_seqlens=None, seq_start: int = 0, dropout_seed=None,
+                      dropout_offset: int = 0, **kwargs):
     """SDPA-shaped entry: local queries against delivered K/V, per-document causal mask.
 
     As on the page "nemo_automodel.components.distributed.blockdiag_cp",
     ``attn_mask`` and ``is_causal`` are ignored (the mask is rebuilt from the
     document ids), ``scale`` None means D**-0.5, and extra keyword arguments
-    are accepted and ignored.  Dropout is not implemented: ``dropout_p`` must be 0.
+    are accepted and ignored.  ``dropout_p`` acts as in torch's SDPA (on the
+    normalised weights, kept ones scaled by 1 / (1 - p), applied whenever it
+    is > 0); ``dropout_seed`` / ``dropout_offset`` fix the mask (the seed is
+    drawn from torch's generator when None).
     """
     del attn_mask, is_causal, kwargs
-    if dropout_p != 0.0:
-        raise ValueError("dropout_p > 0 is not supported")
     return blockdiag_attention(query, key, value, cu_seqlens=cu_seqlens, doc_ids=doc_ids,
-                               seq_start=seq_start, scale=scale, enable_gqa=enable_gqa)
+                               seq_start=seq_start, scale=scale, enable_gqa=enable_gqa,
+                               dropout_p=dropout_p, dropout_seed=dropout_seed,
+                               dropout_offset=dropout_offset)
 
 
 def useful_pairs(cu_rows, seq_start: int, L: int) -> int:

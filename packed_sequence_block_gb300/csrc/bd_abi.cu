@@ -62,11 +62,28 @@ int check_plan_lists(int B, int Hq, int Hkv, int L, int S) {
 }
 
 AttnDims resolve(int B, int Hq, int Hkv, int L, int S, int D, int seq_start, float scale) {
-  AttnDims d{B, Hq, Hkv, L, S, D, seq_start, scale, 0.f};
+  AttnDims d{B, Hq, Hkv, L, S, D, seq_start, scale, 0.f, DropoutArgs{}};
   if (!(scale > 0.f) || !std::isfinite(scale)) d.scale = 1.0f / std::sqrt(static_cast<float>(D));
   d.scale_log2 = d.scale * 1.4426950408889634f;
   return d;
 }
+
+// Dropout arguments: p in [0, 1); an element is kept iff its 32-bit Philox
+// word is >= floor(p * 2^32); p == 0 turns dropout off.
+int make_dropout(double p, uint64_t seed, uint32_t offset, DropoutArgs* out) {
+  if (!(p >= 0.0 && p < 1.0)) return BD_ERR_INVALID_ARG;
+  DropoutArgs d;
+  d.on = p > 0.0;
+  const double thr = std::floor(p * 4294967296.0);
+  d.threshold = thr >= 4294967295.0 ? 0xffffffffu : static_cast<uint32_t>(thr);
+  d.rp = static_cast<float>(1.0 / (1.0 - p));
+  d.k0 = static_cast<uint32_t>(seed & 0xffffffffu);
+  d.k1 = static_cast<uint32_t>(seed >> 32);
+  d.offset = offset;
+  *out = d;
+  return BD_OK;
+}
+
 
 }  // namespace
 
@@ -221,10 +238,15 @@ size_t bd_attn_fwd_workspace_size(int B, int Hkv, int S, int D) {
   return align256(2 * (size_t)B * Hkv * S * D);
 }
 
-int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L, int S,
-                int D, int seq_start, float scale, int enable_gqa, void* plan,
-                size_t plan_bytes, void* out, float* lse, void* out_lo, void* workspace,
-                size_t workspace_bytes, int32_t* dev_status, bd_stream_t stream) {
+}  // extern "C"
+
+namespace bd {
+namespace {
+
+int fwd_impl(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L, int S,
+             int D, int seq_start, float scale, int enable_gqa, void* plan, size_t plan_bytes,
+             void* out, float* lse, void* out_lo, void* workspace, size_t workspace_bytes,
+             const DropoutArgs& drop, int32_t* dev_status, cudaStream_t stream) {
   if (q == nullptr || k == nullptr || v == nullptr || plan == nullptr || out == nullptr ||
       lse == nullptr || workspace == nullptr)
     return BD_ERR_INVALID_ARG;
@@ -238,7 +260,8 @@ int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int 
   if (st != BD_OK) return st;
   if (plan_bytes < plan_layout(B, Hq, Hkv, L, S).total) return BD_ERR_WORKSPACE;
   if (workspace_bytes < bd_attn_fwd_workspace_size(B, Hkv, S, D)) return BD_ERR_WORKSPACE;
-  const AttnDims d = resolve(B, Hq, Hkv, L, S, D, seq_start, scale);
+  AttnDims d = resolve(B, Hq, Hkv, L, S, D, seq_start, scale);
+  d.drop = drop;
   // the P V product reads v through its fp16 copy in the workspace
   CUtensorMap tq, tk, tv;
   if (!make_tmap_bf16(&tq, q, B * Hq, L, D) || !make_tmap_bf16(&tk, k, B * Hkv, S, D) ||
@@ -252,18 +275,11 @@ int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int 
              : BD_ERR_CUDA;
 }
 
-size_t bd_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int S, int D) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || S < 1 || D < 1) return 0;
-  return bwd_layout(B, Hq, Hkv, L, S, D).total;
-}
-
-int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* out,
-                       const void* out_lo, const float* lse, const void* dout, int B, int Hq,
-                       int Hkv, int L, int S,
-                       int D, int seq_start, float scale, int enable_gqa, void* plan,
-                       size_t plan_bytes, void* dq, void* dk, void* dv, void* workspace,
-                       size_t workspace_bytes, int32_t* dev_status, int stages,
-                       bd_stream_t stream) {
+int bwd_impl(const void* q, const void* k, const void* v, const void* out, const void* out_lo,
+             const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S, int D,
+             int seq_start, float scale, int enable_gqa, void* plan, size_t plan_bytes, void* dq,
+             void* dk, void* dv, void* workspace, size_t workspace_bytes, const DropoutArgs& drop,
+             int32_t* dev_status, int stages, cudaStream_t stream) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || lse == nullptr ||
       dout == nullptr || plan == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
       workspace == nullptr)
@@ -281,7 +297,8 @@ int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* 
   if (plan_bytes < plan_layout(B, Hq, Hkv, L, S).total) return BD_ERR_WORKSPACE;
   const BwdLayout wl = bwd_layout(B, Hq, Hkv, L, S, D);
   if (workspace_bytes < wl.total) return BD_ERR_WORKSPACE;
-  const AttnDims d = resolve(B, Hq, Hkv, L, S, D, seq_start, scale);
+  AttnDims d = resolve(B, Hq, Hkv, L, S, D, seq_start, scale);
+  d.drop = drop;
   CUtensorMap tq, tk, tv, tdo, tdq;
   char* ws = static_cast<char*>(workspace);
   if (!make_tmap_bf16(&tq, q, B * Hq, L, D) || !make_tmap_bf16(&tk, k, B * Hkv, S, D) ||
@@ -296,6 +313,49 @@ int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* 
              : BD_ERR_CUDA;
 }
 
+}  // namespace
+}  // namespace bd
+
+extern "C" {
+
+int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L, int S,
+                int D, int seq_start, float scale, int enable_gqa, void* plan,
+                size_t plan_bytes, void* out, float* lse, void* out_lo, void* workspace,
+                size_t workspace_bytes, int32_t* dev_status, bd_stream_t stream) {
+  return fwd_impl(q, k, v, B, Hq, Hkv, L, S, D, seq_start, scale, enable_gqa, plan, plan_bytes,
+                  out, lse, out_lo, workspace, workspace_bytes, DropoutArgs{}, dev_status, stream);
+}
+
+int bd_attn_fwd_dropout(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
+                        int L, int S, int D, int seq_start, float scale, int enable_gqa,
+                        void* plan, size_t plan_bytes, void* out, float* lse, void* out_lo,
+                        void* workspace, size_t workspace_bytes, double dropout_p,
+                        uint64_t seed, uint32_t offset, int32_t* dev_status,
+                        bd_stream_t stream) {
+  DropoutArgs drop;
+  const int st = make_dropout(dropout_p, seed, offset, &drop);
+  if (st != BD_OK) return st;
+  return fwd_impl(q, k, v, B, Hq, Hkv, L, S, D, seq_start, scale, enable_gqa, plan, plan_bytes,
+                  out, lse, out_lo, workspace, workspace_bytes, drop, dev_status, stream);
+}
+
+size_t bd_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int S, int D) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || S < 1 || D < 1) return 0;
+  return bwd_layout(B, Hq, Hkv, L, S, D).total;
+}
+
+int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* out,
+                       const void* out_lo, const float* lse, const void* dout, int B, int Hq,
+                       int Hkv, int L, int S,
+                       int D, int seq_start, float scale, int enable_gqa, void* plan,
+                       size_t plan_bytes, void* dq, void* dk, void* dv, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, int stages,
+                       bd_stream_t stream) {
+  return bwd_impl(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
+                  enable_gqa, plan, plan_bytes, dq, dk, dv, workspace, workspace_bytes,
+                  DropoutArgs{}, dev_status, stages, stream);
+}
+
 int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* out_lo,
                 const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S, int D,
                 int seq_start,
@@ -305,6 +365,20 @@ int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
   return bd_attn_bwd_stages(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
                             enable_gqa, plan, plan_bytes, dq, dk, dv, workspace, workspace_bytes,
                             dev_status, kBwdPrepare | kBwdMain | kBwdFinish, stream);
+}
+
+int bd_attn_bwd_dropout(const void* q, const void* k, const void* v, const void* out,
+                        const void* out_lo, const float* lse, const void* dout, int B, int Hq,
+                        int Hkv, int L, int S, int D, int seq_start, float scale, int enable_gqa,
+                        void* plan, size_t plan_bytes, void* dq, void* dk, void* dv,
+                        void* workspace, size_t workspace_bytes, double dropout_p, uint64_t seed,
+                        uint32_t offset, int32_t* dev_status, bd_stream_t stream) {
+  DropoutArgs drop;
+  const int st = make_dropout(dropout_p, seed, offset, &drop);
+  if (st != BD_OK) return st;
+  return bwd_impl(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
+                  enable_gqa, plan, plan_bytes, dq, dk, dv, workspace, workspace_bytes, drop,
+                  dev_status, kBwdPrepare | kBwdMain | kBwdFinish, stream);
 }
 
 int bd_get_device_status(const int32_t* dev_status, int32_t* host_status, bd_stream_t stream) {

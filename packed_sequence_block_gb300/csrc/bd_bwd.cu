@@ -65,6 +65,7 @@ struct BwdParams {
   __nv_bfloat16* dv;
   int32_t* status;
   int* ctr;  // work counters in the plan: [next unit, finished CTAs]
+  DropoutArgs drop;
 };
 
 struct BUnit {
@@ -91,6 +92,37 @@ __device__ __forceinline__ BUnit decode_bunit(const BwdParams& p, int w) {
 // in L2.
 __device__ __forceinline__ int unit_qtile(const BUnit& u, int i) {
   return u.qt_lo + u.nq - 1 - i % u.nq;
+}
+
+// Dropout keep bits of one key row against 64 consecutive queries (bit c:
+// the query at global position t0 + c), for a thread whose key is `key`.
+// The element (query t, key j) keeps iff word j & 3 of Philox4x32-10 at
+// counter (j >> 2, t, plane, offset) reaches the threshold.  The four lanes
+// of a quad hold the four keys of one counter, so each lane draws the blocks
+// of 16 of the queries (one block serves all four keys) and the quad then
+// exchanges the bits: lane a's 4-bit group g holds the four keys' bits of
+// query 4 g + a.
+__device__ __forceinline__ uint64_t keep_bits64(int key, uint32_t t0, uint32_t plane,
+                                                const DropoutArgs& d, int lane) {
+  const int a = lane & 3;
+  uint64_t nib = 0;
+#pragma unroll
+  for (int g = 0; g < 16; ++g) {
+    const uint4 w = philox4x32_10(static_cast<uint32_t>(key) >> 2, t0 + 4 * g + a, plane,
+                                  d.offset, d.k0, d.k1);
+    const uint32_t n = static_cast<uint32_t>(w.x >= d.threshold) |
+                       (static_cast<uint32_t>(w.y >= d.threshold) << 1) |
+                       (static_cast<uint32_t>(w.z >= d.threshold) << 2) |
+                       (static_cast<uint32_t>(w.w >= d.threshold) << 3);
+    nib |= static_cast<uint64_t>(n) << (4 * g);
+  }
+  uint64_t out = 0;
+#pragma unroll
+  for (int src = 0; src < 4; ++src) {
+    const uint64_t x = __shfl_sync(0xffffffffu, nib, (lane & ~3) | src);
+    out |= ((x >> a) & 0x1111111111111111ull) << src;  // key a's bit of query 4 g + src
+  }
+  return out;
 }
 
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
@@ -199,7 +231,11 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
 // hands to the dV MMA (32 registers) and forms dS = P (dP - Delta) in fp32
 // from them.
 
-template <int D>
+// kDrop: attention dropout (p.drop).  With the mask M regenerated from the
+// counters the forward used: dV = rp (P o M)^T dO, where the P^T tile carries
+// P o M and rp = 1 / (1 - p) joins dV's epilogue; dS = P o (rp M o dP - Delta),
+// Delta = <dO, O> of the dropped output.
+template <int D, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     bd_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_k,
@@ -481,6 +517,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < u.n_it; ++i) {
         const int qt = unit_qtile(u, i);
         const int st = st_it & 1;
+        uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;  // dropout keep bits of the 64 columns
+        if constexpr (kDrop) {
+          // drawn before the S^T wait: they depend only on the positions
+          const uint32_t plane = static_cast<uint32_t>(u.b * p.Hq + u.g * p.G + i / u.nq);
+          const uint64_t kb = keep_bits64(
+              key, static_cast<uint32_t>(p.seq_start + qt * kBM + c0), plane, p.drop, lane);
+          keep_lo = static_cast<uint32_t>(kb);
+          keep_hi = static_cast<uint32_t>(kb >> 32);
+        }
         // ---- phase P: P^T = exp2(S^T * scale * log2 e - lse * log2 e), masked
         ok = mbar_wait_warp(s_full, it_g & 1, abort_flag, p.status);
         if (!ok) break;
@@ -520,9 +565,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             pk[c * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
             pk[c * 16 + (e >> 1) + 1] = pack_bf16x2(p2, p3);
+            if constexpr (kDrop) {
+              // P o M for dV: a dropped weight's bf16 half becomes 0
+              const uint32_t kb = (c == 0 ? keep_lo : keep_hi) >> e;
+              tmp[e >> 1] = pk[c * 16 + (e >> 1)] & ((kb & 1u ? 0x0000ffffu : 0u) |
+                                                     (kb & 2u ? 0xffff0000u : 0u));
+              tmp[(e >> 1) + 1] = pk[c * 16 + (e >> 1) + 1] & ((kb & 4u ? 0x0000ffffu : 0u) |
+                                                               (kb & 8u ? 0xffff0000u : 0u));
+            }
           }
+          if constexpr (!kDrop) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) tmp[e] = pk[c * 16 + e];
+            for (int e = 0; e < 16; ++e) tmp[e] = pk[c * 16 + e];
+          }
           tmem_st16(tS + c * 16, tmp);
         }
         tmem_wait_st();
@@ -541,6 +596,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; e += 4) {
             const float4 x = dl4[(c * 32 + e) >> 2];  // Delta of four columns
             const uint32_t pa = pk[c * 16 + (e >> 1)], pb = pk[c * 16 + (e >> 1) + 1];
+            if constexpr (kDrop) {
+              // dS = P (rp M dP - Delta)
+              const uint32_t kb = (c == 0 ? keep_lo : keep_hi) >> e;
+              const float rp = p.drop.rp;
+              const float d0 = (kb & 1u) ? fmaf(rp, __uint_as_float(dv[e]), -x.x) : -x.x;
+              const float d1 = (kb & 2u) ? fmaf(rp, __uint_as_float(dv[e + 1]), -x.y) : -x.y;
+              const float d2 = (kb & 4u) ? fmaf(rp, __uint_as_float(dv[e + 2]), -x.z) : -x.z;
+              const float d3 = (kb & 8u) ? fmaf(rp, __uint_as_float(dv[e + 3]), -x.w) : -x.w;
+              dk[e >> 1] = pack_bf16x2(__uint_as_float(pa << 16) * d0,
+                                       __uint_as_float(pa & 0xffff0000u) * d1);
+              dk[(e >> 1) + 1] = pack_bf16x2(__uint_as_float(pb << 16) * d2,
+                                             __uint_as_float(pb & 0xffff0000u) * d3);
+              continue;
+            }
             dk[e >> 1] = pack_bf16x2(__uint_as_float(pa << 16) * (__uint_as_float(dv[e]) - x.x),
                                     __uint_as_float(pa & 0xffff0000u) *
                                         (__uint_as_float(dv[e + 1]) - x.y));
@@ -571,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       {
         const uint32_t tsrc = tmem + lane_off + hf * 128;
-        const float mul = hf == 0 ? p.scale : 1.f;
+        const float mul = hf == 0 ? p.scale : (kDrop ? p.drop.rp : 1.f);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t v[32];
@@ -700,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) ring_retire(p.ctr);
 }
 
-template <int D>
+template <int D, bool kDrop>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const CUtensorMap& tdo,
                                 const CUtensorMap& tdq,
@@ -714,7 +783,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(bd_bwd_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(bd_bwd_kernel<D, kDrop>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
@@ -731,7 +800,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
   }
   const int grid = p.n_units < num_sms ? p.n_units : num_sms;
   if ((stages & kBwdMain) && grid > 0) {
-    bd_bwd_kernel<D><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
+    bd_bwd_kernel<D, kDrop><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -777,11 +846,19 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.status = status;
   p.ctr = reinterpret_cast<int*>(base + pl.sched) + 2;
+  p.drop = d.drop;
+  if (d.drop.on) {
+    if (d.D == 64)
+      return launch_bwd_t<64, true>(tq, tk, tv, tdo, tdq, p, out, out_lo, lse, dout, dq, stages,
+                                    num_sms, stream);
+    return launch_bwd_t<128, true>(tq, tk, tv, tdo, tdq, p, out, out_lo, lse, dout, dq, stages,
+                                   num_sms, stream);
+  }
   if (d.D == 64)
-    return launch_bwd_t<64>(tq, tk, tv, tdo, tdq, p, out, out_lo, lse, dout, dq, stages, num_sms,
-                            stream);
-  return launch_bwd_t<128>(tq, tk, tv, tdo, tdq, p, out, out_lo, lse, dout, dq, stages, num_sms,
-                           stream);
+    return launch_bwd_t<64, false>(tq, tk, tv, tdo, tdq, p, out, out_lo, lse, dout, dq, stages,
+                                   num_sms, stream);
+  return launch_bwd_t<128, false>(tq, tk, tv, tdo, tdq, p, out, out_lo, lse, dout, dq, stages,
+                                  num_sms, stream);
 }
 
 }  // namespace bd

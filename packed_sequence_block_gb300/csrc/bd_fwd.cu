@@ -58,6 +58,7 @@ struct FwdParams {
   float* lse;
   int32_t* status;
   int* ctr;  // work counters in the plan: [next unit, finished CTAs]
+  DropoutArgs drop;
 };
 
 struct Unit {
@@ -101,7 +102,11 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int32
 
 }  // namespace
 
-template <int D>
+// kDrop: attention dropout on the weights that feed P V (p.drop): a dropped
+// weight is written as 0 into the P tile and the kept ones are scaled by
+// 1 / (1 - p) with 1 / l in the epilogue; the row sum and the log-sum-exp stay
+// those of the undropped softmax.
+template <int D, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     bd_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_k,
@@ -322,6 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i = qt * kBM + r;  // local query row
       const bool in_range = i < p.L;
       const int t = p.seq_start + i;
+      const uint32_t tpos = static_cast<uint32_t>(t);  // dropout counter word 1
+      const uint32_t plane = static_cast<uint32_t>(u.b * p.Hq + h);
       const int32_t lo = in_range ? p.qlo[(size_t)u.b * p.Lpad + i] : kPadLo;
       const size_t row = static_cast<size_t>(u.b * p.Hq + h) * p.L + i;
       if (u.n <= 0) {
@@ -396,13 +403,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
+          uint4 w = make_uint4(0, 0, 0, 0);  // Philox words of the current four keys
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const float2 t = ffma2(make_float2(__uint_as_float(v[c * 32 + e]),
                                                __uint_as_float(v[c * 32 + e + 1])), sc2, nm2);
             const float2 x = make_float2(fast_exp2(t.x), fast_exp2(t.y));
             l4[(e >> 1) & 3] = fadd2(l4[(e >> 1) & 3], x);
-            pk[e >> 1] = pack_f16x2(x.x, x.y);
+            if constexpr (kDrop) {
+              // key j = k0 + c*32 + e: counter (j >> 2, t, plane, offset), word j & 3
+              if ((e & 3) == 0)
+                w = philox4x32_10(static_cast<uint32_t>((k0 + c * 32 + e) >> 2), tpos, plane,
+                                  p.drop.offset, p.drop.k0, p.drop.k1);
+              const uint32_t wa = (e & 3) == 0 ? w.x : w.z, wb = (e & 3) == 0 ? w.y : w.w;
+              pk[e >> 1] = pack_f16x2(wa >= p.drop.threshold ? x.x : 0.f,
+                                      wb >= p.drop.threshold ? x.y : 0.f);
+            } else {
+              pk[e >> 1] = pack_f16x2(x.x, x.y);
+            }
           }
           tmem_st16(tS + c * 16, pk);
         }
@@ -435,7 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ++o_it;
       tc_fence_after();
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      // the kept weights enter P V unscaled; 1 / (1 - p) joins 1 / l here
+      const float inv = (l > 0.f) ? (kDrop ? p.drop.rp : 1.f) / l : 0.f;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
@@ -478,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) ring_retire(p.ctr);
 }
 
-template <int D>
+template <int D, bool kDrop>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const FwdParams& p, int num_sms,
                                 cudaStream_t stream) {
@@ -487,14 +506,14 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(bd_fwd_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(bd_fwd_kernel<D, kDrop>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const int grid = p.n_units < num_sms ? p.n_units : num_sms;
   if (grid <= 0) return cudaSuccess;
-  bd_fwd_kernel<D><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, p);
+  bd_fwd_kernel<D, kDrop><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -546,8 +565,13 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.lse = lse;
   p.status = status;
   p.ctr = reinterpret_cast<int*>(base + pl.sched);
-  if (d.D == 64) return launch_fwd_t<64>(tq, tk, tv, p, num_sms, stream);
-  return launch_fwd_t<128>(tq, tk, tv, p, num_sms, stream);
+  p.drop = d.drop;
+  if (d.drop.on) {
+    if (d.D == 64) return launch_fwd_t<64, true>(tq, tk, tv, p, num_sms, stream);
+    return launch_fwd_t<128, true>(tq, tk, tv, p, num_sms, stream);
+  }
+  if (d.D == 64) return launch_fwd_t<64, false>(tq, tk, tv, p, num_sms, stream);
+  return launch_fwd_t<128, false>(tq, tk, tv, p, num_sms, stream);
 }
 
 }  // namespace bd

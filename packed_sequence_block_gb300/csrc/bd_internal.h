@@ -85,10 +85,21 @@ inline BwdLayout bwd_layout(int B, int Hq, int Hkv, int L, int S, int D) {
   return w;
 }
 
+// Attention dropout: element (plane, query position t, key position j) is kept
+// iff word j & 3 of Philox4x32-10(counter (j >> 2, t, plane, offset), key
+// (k0, k1)) is >= threshold = floor(p * 2^32); kept weights are scaled by rp.
+struct DropoutArgs {
+  bool on = false;
+  uint32_t threshold = 0;
+  float rp = 1.f;  // 1 / (1 - p)
+  uint32_t k0 = 0, k1 = 0, offset = 0;
+};
+
 struct AttnDims {
   int B, Hq, Hkv, L, S, D, seq_start;
   float scale;        // softmax scale (resolved, > 0)
   float scale_log2;   // scale * log2(e)
+  DropoutArgs drop;
 };
 
 // ---- launchers (each enqueues on `stream`; returns the launch error) ----

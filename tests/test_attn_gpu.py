@@ -17,7 +17,8 @@ import numpy as np
 import pytest
 import torch
 
-from _gpu_common import assert_close, assert_lse, gpu_forward_backward, rand_bf16, to64
+from _gpu_common import (assert_close, assert_lse, gpu_forward_backward, rand_bf16,
+                         sampled_checks, to64)
 from oracle import blockdiag as orc
 from packed_sequence_block_gb300.workloads import make_qkv_do, make_workload
 
@@ -121,7 +122,7 @@ def test_autograd_api_matches_oracle(cuda_lib):
     assert_close("dk", to64(ka.grad), edk)
     assert_close("dv", to64(va.grad), edv)
     with pytest.raises(ValueError):
-        cp_blockdiag_sdpa(q, k, v, dropout_p=0.1, enable_gqa=True, cu_seqlens=cu)
+        cp_blockdiag_sdpa(q, k, v, dropout_p=1.0, enable_gqa=True, cu_seqlens=cu)
 
 
 def test_repeat_calls_are_stable(cuda_lib):
@@ -143,56 +144,6 @@ def test_workload_full(cuda_lib, name):
     _run_and_compare(_ids(wl.cu, wl.S), q, k, v, do, 0, None, name)
 
 
-def _sub_oracle_rows(q, k, v, do, b, hq_list, G, a, r0, r1, D):
-    """Oracle on one document [a, r1) restricted to query rows [r0, r1) (all in the doc)."""
-    qs = to64(q[b:b + 1, hq_list, r0:r1])
-    dos = to64(do[b:b + 1, hq_list, r0:r1])
-    kv_heads = sorted({h // G for h in hq_list})
-    ks = to64(k[b:b + 1, kv_heads, a:r1])
-    vs = to64(v[b:b + 1, kv_heads, a:r1])
-    ids = np.ones((1, r1 - a), np.int32)
-    Gs = len(hq_list) // len(kv_heads)
-    eo, el = orc.blockdiag_sdpa_forward(qs, ks, vs, ids, r0 - a, None, Gs > 1)
-    edq, edk, edv = orc.blockdiag_sdpa_backward(qs, ks, vs, dos, ids, r0 - a, None, Gs > 1,
-                                                out=eo, lse=el)
-    return eo, el, edq, edk, edv
-
-
-def _sampled_checks(wl, q, k, v, do, out, lse, dq, dk, dv, s0, L, b, heads_fwd, group, rng):
-    """Rows near each document's start/end and tile boundaries; dk/dv of each doc's last keys."""
-    G = wl.G
-    cu = [int(x) for x in wl.cu[b]]
-    last = cu[-1]
-    for a, e in zip(cu[:-1], cu[1:]):
-        lo, hi = max(a, s0), min(e, s0 + L)
-        if lo >= hi:
-            continue
-        starts = {lo, max(lo, hi - 64), lo + (((hi - lo) // 2) // 128) * 128}
-        starts.add(min(hi - 1, max(lo, int(rng.integers(lo, hi)))))
-        for r0 in sorted(starts):
-            r1 = min(hi, r0 + 64)
-            if r1 <= r0:
-                continue
-            eo, el, edq, _, _ = _sub_oracle_rows(q, k, v, do, b, heads_fwd, G, a, r0, r1, wl.D)
-            sl = slice(r0 - s0, r1 - s0)
-            assert_close(f"out[{r0}:{r1}]", to64(out[b, heads_fwd, sl])[None], eo)
-            assert_lse(f"lse[{r0}:{r1}]", to64(lse[b, heads_fwd, sl])[None], el)
-            assert_close(f"dq[{r0}:{r1}]", to64(dq[b, heads_fwd, sl])[None], edq)
-        # dk/dv of the last keys attended inside the interval: need only queries after them
-        j0 = max(lo, hi - 128)
-        heads = list(range(group * G, (group + 1) * G))
-        _, _, _, edk, edv = _sub_oracle_rows(q, k, v, do, b, heads, G, a, j0, hi, wl.D)
-        assert_close(f"dk[{j0}:{hi}]", to64(dk[b, group, j0:hi])[None, None], edk[:, :, j0 - a:])
-        assert_close(f"dv[{j0}:{hi}]", to64(dv[b, group, j0:hi])[None, None], edv[:, :, j0 - a:])
-    # padding rows and keys no query of the interval attends
-    if last < s0 + L:
-        pad = slice(max(last, s0) - s0, L)
-        assert torch.all(out[b, :, pad] == 0) and torch.all(dq[b, :, pad] == 0)
-        assert torch.all(torch.isneginf(lse[b, :, pad]))
-    assert torch.all(dk[b, :, s0 + L:] == 0) and torch.all(dv[b, :, s0 + L:] == 0)
-    assert torch.all(dk[b, :, last:] == 0) and torch.all(dv[b, :, last:] == 0)
-
-
 def test_causal64k_sampled(cuda_lib):
     wl = make_workload("causal64k", 0)
     q, k, v, do = make_qkv_do(wl, device="cuda", generator_device="cuda")
@@ -200,7 +151,7 @@ def test_causal64k_sampled(cuda_lib):
     out, lse, dq, dk, dv = gpu_forward_backward(q, k, v, do, ids)
     rng = np.random.default_rng(0)
     for b in range(wl.B):
-        _sampled_checks(wl, q, k, v, do, out, lse, dq, dk, dv, 0, wl.L, b, [0, wl.Hq - 1],
+        sampled_checks(wl, q, k, v, do, out, lse, dq, dk, dv, 0, wl.L, b, [0, wl.Hq - 1],
                         b % wl.Hkv, rng)
 
 
@@ -217,5 +168,5 @@ def test_interval131k_sampled(cuda_lib, interval):
     # embed the interval's query-side tensors at their global rows for the sampler
     full = lambda t: torch.nn.functional.pad(t, (0, 0, s0, wl.S - s0 - L))  # noqa: E731
     rng = np.random.default_rng(interval)
-    _sampled_checks(wl, full(qi), k, v, full(doi), out, lse, dq, dk, dv, s0, L, 0, [0, 37, 63],
+    sampled_checks(wl, full(qi), k, v, full(doi), out, lse, dq, dk, dv, s0, L, 0, [0, 37, 63],
                     interval % wl.Hkv, rng)

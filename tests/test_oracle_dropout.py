@@ -175,3 +175,39 @@ def test_dropout_intervals_concatenate_to_full_rows():
     parts = [orc.blockdiag_sdpa_forward(q[:, :, s:s + 4], k, v, ids, s, None, True, 0.4, 5, 1)[0]
              for s in (0, 4, 8)]
     np.testing.assert_allclose(np.concatenate(parts, axis=2), full, rtol=0, atol=1e-14)
+
+
+def test_dropout_slice_draws_the_whole_problems_mask():
+    """A document and a subset of heads, cut out with their planes and positions,
+    give the whole problem's values (the slice form the sampled checks use)."""
+    rng = np.random.default_rng(36)
+    B, Hq, Hkv, S, D = 2, 4, 2, 14, 3
+    ids = np.array([[1] * 5 + [2] * 6 + [0] * 3, [3] * 9 + [4] * 5], np.int32)
+    q, do = _rand((B, Hq, S, D), rng), _rand((B, Hq, S, D), rng)
+    k, v = _rand((B, Hkv, S, D), rng), _rand((B, Hkv, S, D), rng)
+    p, seed, off = 0.4, (7 << 40) | 3, 2
+    out, lse = orc.blockdiag_sdpa_forward(q, k, v, ids, 0, None, True, p, seed, off)
+    dq, dk, dv = orc.blockdiag_sdpa_backward(q, k, v, do, ids, 0, None, True, out=out, lse=lse,
+                                             dropout_p=p, seed=seed, offset=off)
+    b, a, e, heads = 0, 5, 11, [2, 3]  # document 2 of row 0, kv head 1
+    r0 = 7
+    sl = (slice(b, b + 1), heads)
+    planes = [[b * Hq + h for h in heads]]
+    ones = np.ones((1, e - a), np.int32)
+    so, sls = orc.blockdiag_sdpa_forward(q[sl][:, :, r0:e], k[b:b + 1, 1:2, a:e],
+                                         v[b:b + 1, 1:2, a:e], ones, r0 - a, None, True, p, seed,
+                                         off, mask_planes=planes, mask_pos0=a)
+    np.testing.assert_allclose(so, out[sl][:, :, r0:e], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(sls, lse[sl][:, :, r0:e], rtol=0, atol=1e-13)
+    # dk/dv of the document's keys from all of its queries
+    _, sdk, sdv = orc.blockdiag_sdpa_backward(q[sl][:, :, a:e], k[b:b + 1, 1:2, a:e],
+                                              v[b:b + 1, 1:2, a:e], do[sl][:, :, a:e], ones, 0,
+                                              None, True, dropout_p=p, seed=seed, offset=off,
+                                              mask_planes=planes, mask_pos0=a)
+    np.testing.assert_allclose(sdk[0, 0], dk[b, 1, a:e], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(sdv[0, 0], dv[b, 1, a:e], rtol=0, atol=1e-12)
+    # and a wrong plane draws another mask
+    wrong, _ = orc.blockdiag_sdpa_forward(q[sl][:, :, r0:e], k[b:b + 1, 1:2, a:e],
+                                          v[b:b + 1, 1:2, a:e], ones, r0 - a, None, True, p,
+                                          seed, off, mask_planes=[[0, 1]], mask_pos0=a)
+    assert np.abs(wrong - out[sl][:, :, r0:e]).max() > 1e-3

@@ -40,8 +40,11 @@ MUTATIONS = {
                              "dv[b, g, start:r1] += p.T @ dout[b, h, i0:i1]"),
     "dropout_ds_unmasked": ("                        pd, dp = p * mr, dp * mr",
                             "                        pd = p * mr"),
-    "dropout_mask_local_rows": ("p = p * keep_mask(b * Hq + h, np.arange(r0, r1), keys",
-                                "p = p * keep_mask(b * Hq + h, np.arange(r0, r1) - seq_start, keys"),
+    "dropout_mask_local_rows": (
+        "p = p * keep_mask(_mask_plane(mask_planes, b, h, Hq),\n"
+        "                                          np.arange(r0, r1) + mask_pos0",
+        "p = p * keep_mask(_mask_plane(mask_planes, b, h, Hq),\n"
+        "                                          np.arange(r0, r1) - seq_start + mask_pos0"),
     "interval_offset": ("q[b, h, r0 - seq_start:r1 - seq_start] @ k[b, g, start:r1].T",
                         "q[b, h, r0:r1] @ k[b, g, start:r1].T"),
 }
