@@ -45,7 +45,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .dropout import keep_mask
+from .dropout import keep_mask, keep_scale
 
 PAD_DOC_ID = 0
 
@@ -124,7 +124,8 @@ def blockdiag_sdpa_forward(q, k, v, doc_ids, seq_start=0, scale=None, enable_gqa
     ``doc_ids`` is [B, S] (0 == padding).  Query i of q sits at global position
     seq_start + i and attends keys j <= seq_start + i of its own segment.
     With ``dropout_p`` > 0 the weights P are masked by oracle.dropout.keep_mask
-    (``seed``, ``offset``) and kept ones scaled by 1 / (1 - dropout_p); lse is
+    (``seed``, ``offset``) and kept ones scaled by oracle.dropout.keep_scale
+    (1 / (1 - p') for p' = dropout_p rounded down to a multiple of 2^-16); lse is
     the softmax's, before dropout.  For a slice of a larger problem,
     ``mask_planes`` [B, Hq] gives each (row, head) its plane in the whole and
     ``mask_pos0`` the whole row's position of this row's position 0, so that
@@ -155,7 +156,7 @@ def blockdiag_sdpa_forward(q, k, v, doc_ids, seq_start=0, scale=None, enable_gqa
                     if dropout_p > 0.0:
                         p = p * keep_mask(_mask_plane(mask_planes, b, h, Hq),
                                           np.arange(r0, r1) + mask_pos0, keys + mask_pos0,
-                                          seed, offset, dropout_p) / (1.0 - dropout_p)
+                                          seed, offset, dropout_p) * keep_scale(dropout_p)
                     out[b, h, r0 - seq_start:r1 - seq_start] = p @ v[b, g, start:r1]
                     lse[b, h, r0 - seq_start:r1 - seq_start] = row_lse[:, 0]
     return out, lse
@@ -168,7 +169,7 @@ def blockdiag_sdpa_backward(q, k, v, dout, doc_ids, seq_start=0, scale=None,
 
     ``out`` and ``lse`` default to this module's own forward pass.  dk/dv rows
     of keys no query of the interval attends are 0.  With dropout (mask M,
-    r = 1 / (1 - p)): dv = (P o M r)^T dO and dS = P o (M r dP - Delta), where
+    r = keep_scale(p)): dv = (P o M r)^T dO and dS = P o (M r dP - Delta), where
     Delta = <dO, out> still equals sum_j P_ij M_ij r dP_ij.  ``mask_planes``
     and ``mask_pos0`` as in the forward.
     """
@@ -203,7 +204,7 @@ def blockdiag_sdpa_backward(q, k, v, dout, doc_ids, seq_start=0, scale=None,
                     if dropout_p > 0.0:
                         mr = keep_mask(_mask_plane(mask_planes, b, h, Hq),
                                        np.arange(r0, r1) + mask_pos0, keys + mask_pos0, seed,
-                                       offset, dropout_p) / (1.0 - dropout_p)
+                                       offset, dropout_p) * keep_scale(dropout_p)
                         pd, dp = p * mr, dp * mr
                     ds = p * (dp - delta[b, h, i0:i1, None])
                     dq[b, h, i0:i1] = scale * (ds @ kk)

@@ -8,10 +8,10 @@ What it follows:
 
 * Page "nemo_automodel.components.distributed.blockdiag_cp",
   ``cp_blockdiag_sdpa(..., dropout_p: float = 0.0, ...)``: a drop-in for torch
-  scaled_dot_product_attention, "dropout_p: Dropout probability".  Reading
-  (SDPA's convention): dropout acts on the normalised attention weights P; a
-  kept weight is scaled by 1 / (1 - p), a dropped one is 0; the returned
-  log-sum-exp is the softmax's, before dropout.
+  scaled_dot_product_attention, where dropout_p is the dropout probability.
+  Reading (SDPA's convention): dropout acts on the normalised attention
+  weights P; a kept weight is scaled by 1 / (1 - p), a dropped one is 0; the
+  returned log-sum-exp is the softmax's, before dropout.
 * The random bits: Philox4x32-10, the counter-based generator of Salmon,
   Moraes, Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3"
   (SC'11): ten rounds on a 128-bit counter (four 32-bit words) under a 64-bit
@@ -21,12 +21,16 @@ What it follows:
   0x9E3779B9 and 0xBB67AE85.  The same generator is written independently on
   the device from that definition.
 
-Reading for the mask (no page fixes one): element (plane = b Hq + h, query at
-global position t, key at position j) uses counter (j >> 2, t, plane, offset)
-under key (seed & 0xffffffff, seed >> 32) and output word j & 3; it is kept
-iff that word >= floor(p * 2**32).  The query's global position (not its
-local row) enters the counter, so a row split into query intervals draws the
-same mask as the whole row.
+Reading for the mask (no page fixes one): each weight draws a 16-bit value.
+Element (plane = b Hq + h, query at global position t, key at position j)
+uses counter (j >> 3, t, plane, offset) under key (seed & 0xffffffff,
+seed >> 32); of the four output words, word (j & 7) >> 1 holds its value, in
+the low 16 bits for even j and the high 16 bits for odd j.  It is kept iff
+that value >= floor(p * 2**16).  The drop probability is therefore p rounded
+down to a multiple of 2**-16, p' = floor(p * 2**16) / 2**16, and kept weights
+are scaled by 1 / (1 - p'), which keeps the expectation exact.  The query's
+global position (not its local row) enters the counter, so a row split into
+query intervals draws the same mask as the whole row.
 
 Parity unpinned for the exact Philox stream: the published known-answer
 vectors are not at hand, so the generator is pinned only by properties
@@ -61,17 +65,23 @@ def philox4x32_10(c0, c1, c2, c3, seed: int):
 
 
 def drop_threshold(p: float) -> int:
-    """Words below floor(p * 2**32) drop their element (p in [0, 1))."""
+    """16-bit values below floor(p * 2**16) drop their element (p in [0, 1))."""
     if not 0.0 <= p < 1.0:
         raise ValueError("dropout_p must lie in [0, 1)")
-    return int(np.floor(float(p) * 4294967296.0))
+    return int(np.floor(float(p) * 65536.0))
+
+
+def keep_scale(p: float) -> float:
+    """1 / (1 - p') for the drop probability p' = drop_threshold(p) / 2**16."""
+    return 1.0 / (1.0 - drop_threshold(p) / 65536.0)
 
 
 def keep_mask(plane: int, t, j, seed: int, offset: int, p: float) -> np.ndarray:
     """Boolean keep mask [len(t), len(j)] of query positions t against key positions j."""
     t = np.asarray(t, dtype=np.int64)[:, None]
     j = np.asarray(j, dtype=np.int64)[None, :]
-    words = philox4x32_10(j >> 2, t, np.int64(plane), np.int64(offset), seed)
-    sel = np.broadcast_to(j & 3, np.broadcast_shapes(t.shape, j.shape))
-    w = np.choose(sel, words)
-    return w >= np.uint32(drop_threshold(p)) if p > 0.0 else np.ones(w.shape, bool)
+    words = philox4x32_10(j >> 3, t, np.int64(plane), np.int64(offset), seed)
+    shape = np.broadcast_shapes(t.shape, j.shape)
+    w = np.choose(np.broadcast_to((j & 7) >> 1, shape), words)
+    half = (w >> np.broadcast_to(((j & 1) * 16).astype(np.uint32), shape)) & np.uint32(0xFFFF)
+    return half >= np.uint32(drop_threshold(p)) if p > 0.0 else np.ones(half.shape, bool)

@@ -2,7 +2,8 @@
 
 Page "nemo_automodel.components.distributed.blockdiag_cp", cp_blockdiag_sdpa
 (dropout_p).  The generator (Philox4x32-10, Salmon et al., SC'11) is pinned by
-properties only (bijectivity, uniform words, the drop rate); the dropout
+properties only (bijectivity, uniform words, the drop rate, independent
+neighbouring keys); the dropout
 arithmetic by exact reductions: p = 0, a dense element-by-element restatement
 with the mask written out, the expectation over masks, finite differences
 with the mask fixed, and interval invariance.
@@ -53,10 +54,29 @@ def test_drop_rate(p):
 
 def test_threshold_and_p_zero():
     assert dro.drop_threshold(0.0) == 0
-    assert dro.drop_threshold(0.5) == 1 << 31
+    assert dro.drop_threshold(0.5) == 1 << 15
+    assert dro.drop_threshold(0.3) == 19660  # 0.3 * 65536 = 19660.8
+    assert dro.drop_threshold(2.0 ** -17) == 0  # below the 16-bit grain: nothing drops
+    assert dro.keep_scale(0.25) == 4.0 / 3.0
+    assert dro.keep_scale(0.3) == 1.0 / (1.0 - 19660 / 65536)
     assert dro.keep_mask(0, np.arange(5), np.arange(9), 1, 0, 0.0).all()
+    assert dro.keep_mask(0, np.arange(5), np.arange(9), 1, 0, 2.0 ** -17).all()
     with pytest.raises(ValueError):
         dro.drop_threshold(1.0)
+
+
+def test_neighbouring_keys_are_independent():
+    """Each key of an 8-key block draws its own 16 bits: two keys sharing a
+    value (or a word's half used twice) would correlate their decisions."""
+    p = 0.5
+    keep = dro.keep_mask(2, np.arange(256), np.arange(512), 7, 1, p)
+    for d in range(1, 9):
+        both = (keep[:, :-d] & keep[:, d:]).mean()
+        n = keep[:, d:].size
+        assert abs(both - 0.25) < 5 * math.sqrt(0.25 * 0.75 / n), d
+    # the same key across neighbouring queries too
+    both = (keep[:-1] & keep[1:]).mean()
+    assert abs(both - 0.25) < 5 * math.sqrt(0.25 * 0.75 / keep[1:].size)
 
 
 # ---------------------------------------------------------------- attention with dropout
@@ -83,7 +103,8 @@ def _dense_dropout_forward(q, k, v, ids, s0, scale, G, p, seed, offset):
                 z = sum(math.exp(x) for x in s.values())
                 for j in allowed:
                     keep = dro.keep_mask(b * Hq + h, [t], [j], seed, offset, p)[0, 0]
-                    w = math.exp(s[j]) / z * (1.0 / (1.0 - p) if keep else 0.0)
+                    p_eff = math.floor(p * 65536) / 65536  # p on the 16-bit grain
+                    w = math.exp(s[j]) / z * (1.0 / (1.0 - p_eff) if keep else 0.0)
                     out[b, h, i] += w * v[b, g, j]
     return out
 

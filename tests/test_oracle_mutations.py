@@ -34,7 +34,7 @@ MUTATIONS = {
                    "dk[b, g, start:r1] += pd.T @ dout[b, h, i0:i1]"),
     "dk_uses_k": ("dk[b, g, start:r1] += scale * (ds.T @ q[b, h, i0:i1])",
                   "dk[b, g, start:r1] += scale * (ds.T @ q[b, h, i0:i1][:, ::-1])"),
-    "dropout_unscaled": ("dropout_p) / (1.0 - dropout_p)\n                    out[b, h",
+    "dropout_unscaled": ("dropout_p) * keep_scale(dropout_p)\n                    out[b, h",
                          "dropout_p)\n                    out[b, h"),
     "dropout_dv_undropped": ("dv[b, g, start:r1] += pd.T @ dout[b, h, i0:i1]",
                              "dv[b, g, start:r1] += p.T @ dout[b, h, i0:i1]"),
