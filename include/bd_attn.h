@@ -236,7 +236,8 @@ int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
  * Forward and backward with attention dropout (page
  * "nemo_automodel.components.distributed.blockdiag_cp", cp_blockdiag_sdpa's
  * dropout_p, read as torch scaled_dot_product_attention's: dropout acts on
- * the normalised attention weights, kept weights are scaled by 1 / (1 - p)).
+ * the normalised attention weights and kept ones are scaled up; p is taken
+ * on a 16-bit grain, below).
  * Same arguments and results as bd_attn_fwd / bd_attn_bwd plus
  *   dropout_p    in [0, 1) (else BD_ERR_INVALID_ARG); 0 is no dropout.
  *   seed         64-bit key of the generator.
@@ -244,9 +245,14 @@ int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
  *                mask under the same seed, e.g. one per layer or step).
  * The mask is a pure function of (seed, offset, batch row b, query head h,
  * query position t, key position j): weight (t, j) of plane b * Hq + h is
- * dropped iff word (j & 3) of Philox4x32-10 (Salmon et al., SC'11) at
- * counter (j >> 2, t, b * Hq + h, offset) under key (seed mod 2^32,
- * seed >> 32) is below floor(p * 2^32).  t is the global position
+ * dropped iff its 16-bit value is below floor(p * 2^16), where the value is
+ * the low (j even) or high (j odd) half of word (j & 7) >> 1 of
+ * Philox4x32-10 (Salmon et al., SC'11) at counter (j >> 3, t, b * Hq + h,
+ * offset) under key (seed mod 2^32, seed >> 32).  The drop probability is
+ * thus p' = floor(p * 2^16) / 2^16 (p rounded down to the 16-bit grain;
+ * below 2^-16 nothing is dropped) and kept weights are scaled by
+ * 1 / (1 - p'), so the output's expectation is the undropped one.
+ * t is the global position
  * (seq_start + i), so query intervals of one row draw the same mask as the
  * whole row, and the backward regenerates the forward's mask from the same
  * (seed, offset) with nothing stored in between.  lse stays the log-sum-exp

@@ -182,9 +182,10 @@ def blockdiag_attention(q, k, v, *, cu_seqlens=None, doc_ids=None, seq_start: in
 
     The mask comes from ``doc_ids`` [B, S] (0 == padding) or, when those are
     not given, from ``cu_seqlens`` (one row's boundaries or a list of rows).
-    ``dropout_p`` in [0, 1) drops attention weights (kept ones scaled by
-    1 / (1 - p)); the mask is a function of (dropout_seed, dropout_offset) and
-    the positions, and the seed is drawn from torch's generator when None.
+    ``dropout_p`` in [0, 1) drops attention weights with probability p',
+    p rounded down to a multiple of 2^-16 (kept ones scaled by 1 / (1 - p'));
+    the mask is a function of (dropout_seed, dropout_offset) and the
+    positions, and the seed is drawn from torch's generator when None.
     """
     if not 0.0 <= float(dropout_p) < 1.0:
         raise ValueError("dropout_p must lie in [0, 1)")
@@ -215,9 +216,10 @@ def cp_blockdiag_sdpa(query, key, value, attn_mask=None, dropout_p: float = 0.0,
     ``attn_mask`` and ``is_causal`` are ignored (the mask is rebuilt from the
     document ids), ``scale`` None means D**-0.5, and extra keyword arguments
     are accepted and ignored.  ``dropout_p`` acts as in torch's SDPA (on the
-    normalised weights, kept ones scaled by 1 / (1 - p), applied whenever it
-    is > 0); ``dropout_seed`` / ``dropout_offset`` fix the mask (the seed is
-    drawn from torch's generator when None).
+    normalised weights, applied whenever it is > 0), with p rounded down to a
+    multiple of 2^-16 and kept weights scaled by 1 / (1 - p') for that p';
+    ``dropout_seed`` / ``dropout_offset`` fix the mask (the seed is drawn
+    from torch's generator when None).
     """
     del attn_mask, is_causal, kwargs
     return blockdiag_attention(query, key, value, cu_seqlens=cu_seqlens, doc_ids=doc_ids,

@@ -68,17 +68,25 @@ AttnDims resolve(int B, int Hq, int Hkv, int L, int S, int D, int seq_start, flo
   return d;
 }
 
-// Dropout arguments: p in [0, 1); an element is kept iff its 32-bit Philox
-// word is >= floor(p * 2^32); p == 0 turns dropout off.
+// Dropout arguments: p in [0, 1); an element is kept iff its 16-bit Philox
+// value is >= floor(p * 2^16), so the drop probability is p' = that
+// threshold / 2^16 and kept weights are scaled by 1 / (1 - p').  A p below
+// 2^-16 drops nothing and runs the kernels without dropout.
 int make_dropout(double p, uint64_t seed, uint32_t offset, DropoutArgs* out) {
   if (!(p >= 0.0 && p < 1.0)) return BD_ERR_INVALID_ARG;
   DropoutArgs d;
-  d.on = p > 0.0;
-  const double thr = std::floor(p * 4294967296.0);
-  d.threshold = thr >= 4294967295.0 ? 0xffffffffu : static_cast<uint32_t>(thr);
-  d.rp = static_cast<float>(1.0 / (1.0 - p));
-  d.k0 = static_cast<uint32_t>(seed & 0xffffffffu);
-  d.k1 = static_cast<uint32_t>(seed >> 32);
+  const double thr = std::floor(p * 65536.0);
+  d.threshold = thr >= 65535.0 ? 65535u : static_cast<uint32_t>(thr);
+  d.on = d.threshold > 0;
+  d.rp = static_cast<float>(1.0 / (1.0 - d.threshold / 65536.0));
+  uint32_t k0 = static_cast<uint32_t>(seed & 0xffffffffu);
+  uint32_t k1 = static_cast<uint32_t>(seed >> 32);
+  for (int r = 0; r < 10; ++r) {  // the Philox key schedule
+    d.rk[2 * r] = k0;
+    d.rk[2 * r + 1] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
   d.offset = offset;
   *out = d;
   return BD_OK;

@@ -96,31 +96,36 @@ __device__ __forceinline__ int unit_qtile(const BUnit& u, int i) {
 
 // Dropout keep bits of one key row against 64 consecutive queries (bit c:
 // the query at global position t0 + c), for a thread whose key is `key`.
-// The element (query t, key j) keeps iff word j & 3 of Philox4x32-10 at
-// counter (j >> 2, t, plane, offset) reaches the threshold.  The four lanes
-// of a quad hold the four keys of one counter, so each lane draws the blocks
-// of 16 of the queries (one block serves all four keys) and the quad then
-// exchanges the bits: lane a's 4-bit group g holds the four keys' bits of
-// query 4 g + a.
+// The element (query t, key j) keeps iff the 16-bit half j & 1 of word
+// (j & 7) >> 1 of Philox4x32-10 at counter (j >> 3, t, plane, offset)
+// reaches the threshold.  The eight lanes of an octet hold the eight keys of
+// one counter, so each lane draws the blocks of 8 of the queries (one block
+// serves all eight keys) and the octet then exchanges the bits: byte g of
+// lane a holds the eight keys' bits of query 8 g + a.
 __device__ __forceinline__ uint64_t keep_bits64(int key, uint32_t t0, uint32_t plane,
                                                 const DropoutArgs& d, int lane) {
-  const int a = lane & 3;
-  uint64_t nib = 0;
+  const int a = lane & 7;
+  const uint32_t thr = d.threshold;
+  uint64_t bytes = 0;
 #pragma unroll
-  for (int g = 0; g < 16; ++g) {
-    const uint4 w = philox4x32_10(static_cast<uint32_t>(key) >> 2, t0 + 4 * g + a, plane,
-                                  d.offset, d.k0, d.k1);
-    const uint32_t n = static_cast<uint32_t>(w.x >= d.threshold) |
-                       (static_cast<uint32_t>(w.y >= d.threshold) << 1) |
-                       (static_cast<uint32_t>(w.z >= d.threshold) << 2) |
-                       (static_cast<uint32_t>(w.w >= d.threshold) << 3);
-    nib |= static_cast<uint64_t>(n) << (4 * g);
+  for (int g = 0; g < 8; ++g) {
+    const uint4 w = philox4x32_10(static_cast<uint32_t>(key) >> 3, t0 + 8 * g + a, plane,
+                                  d.offset, d.rk);
+    const uint32_t n = static_cast<uint32_t>((w.x & 0xffffu) >= thr) |
+                       (static_cast<uint32_t>((w.x >> 16) >= thr) << 1) |
+                       (static_cast<uint32_t>((w.y & 0xffffu) >= thr) << 2) |
+                       (static_cast<uint32_t>((w.y >> 16) >= thr) << 3) |
+                       (static_cast<uint32_t>((w.z & 0xffffu) >= thr) << 4) |
+                       (static_cast<uint32_t>((w.z >> 16) >= thr) << 5) |
+                       (static_cast<uint32_t>((w.w & 0xffffu) >= thr) << 6) |
+                       (static_cast<uint32_t>((w.w >> 16) >= thr) << 7);
+    bytes |= static_cast<uint64_t>(n) << (8 * g);
   }
   uint64_t out = 0;
 #pragma unroll
-  for (int src = 0; src < 4; ++src) {
-    const uint64_t x = __shfl_sync(0xffffffffu, nib, (lane & ~3) | src);
-    out |= ((x >> a) & 0x1111111111111111ull) << src;  // key a's bit of query 4 g + src
+  for (int src = 0; src < 8; ++src) {
+    const uint64_t x = __shfl_sync(0xffffffffu, bytes, (lane & ~7) | src);
+    out |= ((x >> a) & 0x0101010101010101ull) << src;  // key a's bit of query 8 g + src
   }
   return out;
 }
@@ -241,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v,
                   const __grid_constant__ CUtensorMap tmap_do,
-                  const __grid_constant__ CUtensorMap tmap_dq, const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tmap_dq, const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);

@@ -110,7 +110,7 @@ template <int D, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     bd_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_k,
-                  const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
-          uint4 w = make_uint4(0, 0, 0, 0);  // Philox words of the current four keys
+          uint4 w = make_uint4(0, 0, 0, 0);  // Philox words of the current eight keys
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const float2 t = ffma2(make_float2(__uint_as_float(v[c * 32 + e]),
@@ -411,13 +411,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 x = make_float2(fast_exp2(t.x), fast_exp2(t.y));
             l4[(e >> 1) & 3] = fadd2(l4[(e >> 1) & 3], x);
             if constexpr (kDrop) {
-              // key j = k0 + c*32 + e: counter (j >> 2, t, plane, offset), word j & 3
-              if ((e & 3) == 0)
-                w = philox4x32_10(static_cast<uint32_t>((k0 + c * 32 + e) >> 2), tpos, plane,
-                                  p.drop.offset, p.drop.k0, p.drop.k1);
-              const uint32_t wa = (e & 3) == 0 ? w.x : w.z, wb = (e & 3) == 0 ? w.y : w.w;
-              pk[e >> 1] = pack_f16x2(wa >= p.drop.threshold ? x.x : 0.f,
-                                      wb >= p.drop.threshold ? x.y : 0.f);
+              // key j = k0 + c*32 + e: counter (j >> 3, t, plane, offset); keys e and
+              // e + 1 take the low and high halves of word (j & 7) >> 1
+              if ((e & 7) == 0)
+                w = philox4x32_10(static_cast<uint32_t>((k0 + c * 32 + e) >> 3), tpos, plane,
+                                  p.drop.offset, p.drop.rk);
+              const uint32_t wd = (e & 7) == 0 ? w.x : (e & 7) == 2 ? w.y : (e & 7) == 4 ? w.z : w.w;
+              pk[e >> 1] = pack_f16x2((wd & 0xffffu) >= p.drop.threshold ? x.x : 0.f,
+                                      (wd >> 16) >= p.drop.threshold ? x.y : 0.f);
             } else {
               pk[e >> 1] = pack_f16x2(x.x, x.y);
             }

@@ -86,13 +86,18 @@ inline BwdLayout bwd_layout(int B, int Hq, int Hkv, int L, int S, int D) {
 }
 
 // Attention dropout: element (plane, query position t, key position j) is kept
-// iff word j & 3 of Philox4x32-10(counter (j >> 2, t, plane, offset), key
-// (k0, k1)) is >= threshold = floor(p * 2^32); kept weights are scaled by rp.
+// iff the 16-bit half j & 1 of word (j & 7) >> 1 of Philox4x32-10(counter
+// (j >> 3, t, plane, offset), key (k0, k1)) is >= threshold = floor(p * 2^16);
+// kept weights are scaled by rp = 1 / (1 - threshold / 2^16).
+// rk holds the key schedule, round r's key words at rk[2r], rk[2r + 1]
+// (k0 + r 0x9E3779B9, k1 + r 0xBB67AE85), read by the kernels from their
+// parameter space.
 struct DropoutArgs {
   bool on = false;
   uint32_t threshold = 0;
   float rp = 1.f;  // 1 / (1 - p)
-  uint32_t k0 = 0, k1 = 0, offset = 0;
+  uint32_t offset = 0;
+  uint32_t rk[20] = {};
 };
 
 struct AttnDims {

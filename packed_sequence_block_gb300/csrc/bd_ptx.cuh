@@ -138,21 +138,21 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
 // as 1, 2, 3", SC'11): ten rounds on the counter (c0, c1, c2, c3) under the key
 // (k0, k1).  A round multiplies c0 and c2 by 0xD2511F53 and 0xCD9E8D57 and maps
 // the counter to (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0));
-// the key words then grow by 0x9E3779B9 and 0xBB67AE85.
+// the key words then grow by 0x9E3779B9 and 0xBB67AE85.  `rk` is that key
+// schedule precomputed (round r: rk[2r], rk[2r + 1]); kept in a kernel's
+// parameter space, each round's key words are constant operands of its xors.
 __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2,
-                                               uint32_t c3, uint32_t k0, uint32_t k1) {
+                                               uint32_t c3, const uint32_t (&rk)[20]) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
     const uint64_t m0 = static_cast<uint64_t>(c0) * 0xD2511F53u;  // one wide multiply each
     const uint64_t m1 = static_cast<uint64_t>(c2) * 0xCD9E8D57u;
-    const uint32_t n0 = static_cast<uint32_t>(m1 >> 32) ^ c1 ^ k0;
-    const uint32_t n2 = static_cast<uint32_t>(m0 >> 32) ^ c3 ^ k1;
+    const uint32_t n0 = static_cast<uint32_t>(m1 >> 32) ^ c1 ^ rk[2 * r];
+    const uint32_t n2 = static_cast<uint32_t>(m0 >> 32) ^ c3 ^ rk[2 * r + 1];
     c0 = n0;
     c1 = static_cast<uint32_t>(m1);
     c2 = n2;
     c3 = static_cast<uint32_t>(m0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
   }
   return make_uint4(c0, c1, c2, c3);
 }

@@ -153,6 +153,17 @@ def test_dropout_zero_is_the_plain_path(cuda_lib):
     assert torch.equal(out, a[0]) and torch.equal(lse, a[1])
 
 
+def test_dropout_below_the_grain_is_the_plain_path(cuda_lib):
+    """p < 2^-16 rounds to no dropout: bit-identical to the plain path."""
+    wl = make_workload("tiny", 0)
+    q, k, v, do = make_qkv_do(wl, device="cuda")
+    ids = torch.from_numpy(_ids(wl.cu, wl.S)).cuda()
+    r0 = gpu_forward_backward(q, k, v, do, ids)
+    r1 = gpu_forward_backward(q, k, v, do, ids, dropout=(2.0 ** -17, 9, 0))
+    for i in (0, 1, 3, 4):
+        assert torch.equal(r0[i], r1[i])
+
+
 def test_dropout_masks_follow_seed_and_offset(cuda_lib):
     wl = make_workload("tiny", 0)
     q, k, v, do = make_qkv_do(wl, device="cuda")
