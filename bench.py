@@ -77,6 +77,14 @@ def describe(wl):
             f"{wl.L}, seed {wl.seed}")
 
 
+def doc_boundaries(wl):
+    """The workload's document boundaries per row, or their SHA-256 when there are many."""
+    rows = [[int(x) for x in c] for c in wl.cu]
+    if sum(len(r) for r in rows) <= 64:
+        return rows
+    return "sha256:" + hashlib.sha256(json.dumps(rows).encode()).hexdigest()
+
+
 def profiled_traffic(workload, seed):
     """DRAM bytes per launch of the backward main kernel from the committed ncu
     summary, or None when the kernel sources differ from the profiled ones or
@@ -624,6 +632,7 @@ def main():
             "data": "synthetic",
             "config": {"workload": describe(wl), "B": wl.B, "S": wl.S, "L": wl.L, "Hq": Hq,
                        "Hkv": wl.Hkv, "D": D, "useful_pairs": pairs,
+                       "cu_seqlens": doc_boundaries(wl),
                        "useful_tflop_per_step": flops_step / 1e12,
                        "strict_12D_tflops": value * 12.0 / 14.0,
                        "l2": "flushed between timed steps (256 MiB write, outside the events)",
