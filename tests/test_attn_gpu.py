@@ -9,7 +9,8 @@ grouping the kernels distinguish (G even, G odd, G = 1), head dims 64 and
 all-padding rows and one-token documents.  The benchmark workloads run at
 full size: the 8192- and 4x16384-token ones compared in full, the two large
 ones on sampled rows the oracle computes on their own (rows are independent;
-dk/dv of the last keys of a document need only the queries after them).
+dk/dv of the last keys of a document need only the queries after them).  One
+case sits at the largest work lists the library accepts (16384 entries).
 """
 import zlib
 
@@ -170,3 +171,31 @@ def test_interval131k_sampled(cuda_lib, interval):
     rng = np.random.default_rng(interval)
     sampled_checks(wl, full(qi), k, v, full(doi), out, lse, dq, dk, dv, s0, L, 0, [0, 37, 63],
                     interval % wl.Hkv, rng)
+
+
+def test_longest_work_lists_sampled(cuda_lib):
+    """B * ceil(S / 128) at the library's 16384-entry limit for both work lists
+    (8 rows x 262144 tokens, Hq = 2 so that a forward block is one 128-row tile),
+    which the plan sorts with its bitonic path (the other cases stay under 2048
+    entries and use the rank sort); checked on sampled rows of two rows."""
+    from packed_sequence_block_gb300.workloads import Workload
+    rng = np.random.default_rng(77)
+    B, S = 8, 262144
+    cus = []
+    for _ in range(B):
+        lens, used = [], 0
+        while True:
+            x = int(np.clip(np.rint(np.exp(rng.normal(np.log(8192.0), 1.0))), 16, 65536))
+            if used + x > S - 1000:
+                break
+            lens.append(x)
+            used += x
+        cus.append(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32))
+    wl = Workload("longest_lists", B, S, S, 2, 1, 64, cus, [0], 5)
+    assert B * (S // 128) == 16384
+    q, k, v, do = make_qkv_do(wl, device="cuda", generator_device="cuda")
+    ids = torch.from_numpy(_ids(wl.cu, wl.S)).cuda()
+    out, lse, dq, dk, dv = gpu_forward_backward(q, k, v, do, ids)
+    srng = np.random.default_rng(3)
+    for b in (0, B - 1):
+        sampled_checks(wl, q, k, v, do, out, lse, dq, dk, dv, 0, wl.L, b, [0, 1], 0, srng)
