@@ -56,6 +56,9 @@ SMALL = {
     "all_pad_row": ([[0, 90, 256], [0]], 256, 256, 0, 2, 1, 128),
     "one_token_docs": ([list(range(0, 257))], 256, 256, 0, 2, 2, 64),
     "many_zero_len": ([[0, 0, 5, 5, 5, 200, 200, 333]], 384, 384, 0, 4, 4, 128),
+    "single_token_row": ([[0, 1]], 1, 1, 0, 2, 1, 64),
+    "last_query_only": ([[0, 200, 333]], 333, 1, 332, 4, 2, 128),
+    "first_query_only_padded": ([[0, 1], [0]], 300, 1, 0, 3, 1, 64),
 }
 
 
