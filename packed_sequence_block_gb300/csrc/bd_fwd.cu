@@ -31,14 +31,16 @@ struct FwdCfg {
   static constexpr int QTILE = kBM * D * 2;  // bytes of one 128-row bf16 tile
   static constexpr int KTILE = kBN * D * 2;
   // A K stage frees once the S products of its tile are done, a V stage only
-  // once the P V products are: V gets one stage more, so that a V tile loads
-  // over about two periods.
+  // once the P V products are.  At D = 128 a third V stage measured no faster
+  // than two, and its 32 KB stage the epilogue's stores instead.
   static constexpr int KSTAGES = (D == 64) ? 3 : 2;
-  static constexpr int VSTAGES = KSTAGES + 1;
+  static constexpr int VSTAGES = (D == 64) ? 4 : 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + 2 * QTILE;
   static constexpr int OFF_V = OFF_K + KSTAGES * KTILE;
-  static constexpr int OFF_BAR = OFF_V + VSTAGES * KTILE;
+  // epilogue staging: per softmax warp 32 rows x 64 B of out, then of out_lo
+  static constexpr int OFF_STG = OFF_V + VSTAGES * KTILE;
+  static constexpr int OFF_BAR = OFF_STG + 8 * 4096;
   static constexpr int SMEM = OFF_BAR + 512;
   static constexpr uint32_t IDESC_S = make_idesc_bf16(128, 128, 0, 0);
   // P V runs with fp16 operands (V from its fp16 copy, P <= 2^8 by the
@@ -60,6 +62,21 @@ struct FwdParams {
   int* ctr;  // work counters in the plan: [next unit, finished CTAs]
   DropoutArgs drop;
 };
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                       uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
 
 struct Unit {
   int b, h0, h1, qt0, qt1, kt_lo, n, g;
@@ -456,6 +473,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // the kept weights enter P V unscaled; 1 / (1 - p) joins 1 / l here
       const float inv = (l > 0.f) ? (kDrop ? p.drop.rp : 1.f) / l : 0.f;
+      // Each 32-column chunk goes through this warp's staging area: a thread
+      // writes its row's 64 bytes (16-byte pieces swizzled by row so that
+      // neither side conflicts on banks), then four lanes per row store 64
+      // contiguous bytes, eight rows an instruction, instead of 32 rows' 16
+      // bytes each.
+      const uint32_t stg = smem_u32(smem + C::OFF_STG) + (warp - 4) * 4096;
+      const int rr0 = lane >> 2, jj = lane & 3;  // read-back: row within 8, piece of the row
+      const size_t row0 = row - lane;            // the warp's first row
+      const int i0 = i - lane;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
@@ -468,18 +494,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           pl[e] = pack_bf16x2(a - __uint_as_float(pk[e] << 16),
                               b - __uint_as_float(pk[e] & 0xffff0000u));
         }
-        if (in_range) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + row * D + c * 32);
-          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
-          dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
-          if (p.out_lo != nullptr) {
-            uint4* dl = reinterpret_cast<uint4*>(p.out_lo + row * D + c * 32);
-            dl[0] = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-            dl[1] = make_uint4(pl[4], pl[5], pl[6], pl[7]);
-            dl[2] = make_uint4(pl[8], pl[9], pl[10], pl[11]);
-            dl[3] = make_uint4(pl[12], pl[13], pl[14], pl[15]);
+        __syncwarp();  // the previous chunk's read-back is done
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t a = stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
+          sts128(a, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          sts128(a + 2048, pl[4 * j], pl[4 * j + 1], pl[4 * j + 2], pl[4 * j + 3]);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int rr = 8 * k + rr0;
+          const uint32_t a = stg + rr * 64 + ((jj ^ ((rr >> 1) & 3)) << 4);
+          if (i0 + rr < p.L) {
+            const size_t off = (row0 + rr) * D + c * 32 + jj * 8;
+            *reinterpret_cast<uint4*>(p.out + off) = lds128(a);
+            if (p.out_lo != nullptr) *reinterpret_cast<uint4*>(p.out_lo + off) = lds128(a + 2048);
           }
         }
       }
