@@ -140,6 +140,15 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int32
   }
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -646,6 +655,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const uint32_t tsrc = tmem + lane_off + hf * 128;
         const float mul = hf == 0 ? p.scale : (kDrop ? p.drop.rp : 1.f);
+        // Each 32-column chunk goes through shared memory so that four lanes
+        // per row store 64 contiguous bytes, eight rows an instruction.  The
+        // staging is this warp's 4 KB of its group's half of the dS tile: every
+        // product of the unit has completed (dkdv_full), and only this group
+        // writes that half again, in its next dS phase.  16-byte pieces are
+        // swizzled by row pair, so neither side conflicts on banks; two 2 KB
+        // slots alternate.
+        const uint32_t stg = smem_u32(smem + C::OFF_DS) + hf * 16384 + q4 * 4096;
+        const int key0 = u.kt * kBN + q4 * 32;  // the warp's first key row
+        __nv_bfloat16* const gbase =
+            (hf == 0 ? p.dk : p.dv) + ((size_t)(u.b * p.Hkv + u.g) * p.S + key0) * D;
+        const int rr0 = lane >> 2, jj = lane & 3;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t v[32];
@@ -655,14 +676,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 16; ++e)
             pk2[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul,
                                  __uint_as_float(v[2 * e + 1]) * mul);
-          if (key < p.S) {
-            uint4* d4 = reinterpret_cast<uint4*>(grad + c * 32);
-            d4[0] = make_uint4(pk2[0], pk2[1], pk2[2], pk2[3]);
-            d4[1] = make_uint4(pk2[4], pk2[5], pk2[6], pk2[7]);
-            d4[2] = make_uint4(pk2[8], pk2[9], pk2[10], pk2[11]);
-            d4[3] = make_uint4(pk2[12], pk2[13], pk2[14], pk2[15]);
+          const uint32_t slot = stg + (c & 1) * 2048;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            st_shared_v4(slot + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), pk2[4 * j],
+                         pk2[4 * j + 1], pk2[4 * j + 2], pk2[4 * j + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int rr = 8 * k + rr0;
+            if (key0 + rr < p.S)
+              *reinterpret_cast<uint4*>(gbase + (size_t)rr * D + c * 32 + jj * 8) =
+                  ld_shared_v4(slot + rr * 64 + ((jj ^ ((rr >> 1) & 3)) << 4));
           }
         }
+        __syncwarp();
       }
       tc_fence_before();
     }
