@@ -130,6 +130,21 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int planes, int rows, in
   return make_tmap_16bit(map, base, planes, rows, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 }
 
+bool make_tmap_out(CUtensorMap* map, const void* base, int planes, int rows, int D) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                           static_cast<cuuint64_t>(rows) * D * 2};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_tmap_f16(CUtensorMap* map, const void* base, int planes, int rows, int D) {
   return make_tmap_16bit(map, base, planes, rows, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
 }
@@ -271,13 +286,16 @@ int fwd_impl(const void* q, const void* k, const void* v, int B, int Hq, int Hkv
   AttnDims d = resolve(B, Hq, Hkv, L, S, D, seq_start, scale);
   d.drop = drop;
   // the P V product reads v through its fp16 copy in the workspace
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to, tol;
+  if (!make_tmap_out(&to, out, B * Hq, L, D) ||
+      !make_tmap_out(&tol, out_lo != nullptr ? out_lo : out, B * Hq, L, D))
+    return BD_ERR_CUDA;
   if (!make_tmap_bf16(&tq, q, B * Hq, L, D) || !make_tmap_bf16(&tk, k, B * Hkv, S, D) ||
       !make_tmap_f16(&tv, workspace, B * Hkv, S, D))
     return BD_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return BD_ERR_CUDA;
-  return launch_fwd(tq, tk, tv, d, plan, v, workspace, out, out_lo, lse, dev_status, sms,
+  return launch_fwd(tq, tk, tv, to, tol, d, plan, v, workspace, out, out_lo, lse, dev_status, sms,
                     stream) == cudaSuccess
              ? BD_OK
              : BD_ERR_CUDA;

@@ -69,13 +69,16 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
                "r"(d)
                : "memory");
 }
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
+
+// TMA store of a shared-memory box into global memory (rows past the
+// tensor's extent are not written).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t smem_src, int c0,
+                                             int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
 }
 
 struct Unit {
@@ -127,7 +130,10 @@ template <int D, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     bd_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_k,
-                  const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ FwdParams p) {
+                  const __grid_constant__ CUtensorMap tmap_v,
+                  const __grid_constant__ CUtensorMap tmap_o,
+                  const __grid_constant__ CUtensorMap tmap_olo,
+                  const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -176,6 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
+    prefetch_tmap(&tmap_o);
+    prefetch_tmap(&tmap_olo);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -473,15 +481,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // the kept weights enter P V unscaled; 1 / (1 - p) joins 1 / l here
       const float inv = (l > 0.f) ? (kDrop ? p.drop.rp : 1.f) / l : 0.f;
-      // Each 32-column chunk goes through this warp's staging area: a thread
-      // writes its row's 64 bytes (16-byte pieces swizzled by row so that
-      // neither side conflicts on banks), then four lanes per row store 64
-      // contiguous bytes, eight rows an instruction, instead of 32 rows' 16
-      // bytes each.
+      // Each 32-column chunk of this warp's 32 rows goes through its staging
+      // area in the TMA box layout (64-byte rows, 16-byte pieces swizzled by
+      // row pair, which also keeps the writes free of bank conflicts), and
+      // lane 0 hands it to the TMA unit as one store per output: the global
+      // writes then leave the warp's path.  The area is reused once the TMA has
+      // read the previous chunk.
       const uint32_t stg = smem_u32(smem + C::OFF_STG) + (warp - 4) * 4096;
-      const int rr0 = lane >> 2, jj = lane & 3;  // read-back: row within 8, piece of the row
-      const size_t row0 = row - lane;            // the warp's first row
-      const int i0 = i - lane;
+      const int i0 = i - lane;  // the warp's first row
+      const int plane_o = u.b * p.Hq + h;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
@@ -494,28 +502,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           pl[e] = pack_bf16x2(a - __uint_as_float(pk[e] << 16),
                               b - __uint_as_float(pk[e] & 0xffff0000u));
         }
-        __syncwarp();  // the previous chunk's read-back is done
+        if (lane == 0) bulk_wait_read_all();  // the TMA has read the previous chunk
+        __syncwarp();
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint32_t a = stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
           sts128(a, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
           sts128(a + 2048, pl[4 * j], pl[4 * j + 1], pl[4 * j + 2], pl[4 * j + 3]);
         }
+        fence_async_smem();
         __syncwarp();
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int rr = 8 * k + rr0;
-          const uint32_t a = stg + rr * 64 + ((jj ^ ((rr >> 1) & 3)) << 4);
-          if (i0 + rr < p.L) {
-            const size_t off = (row0 + rr) * D + c * 32 + jj * 8;
-            *reinterpret_cast<uint4*>(p.out + off) = lds128(a);
-            if (p.out_lo != nullptr) *reinterpret_cast<uint4*>(p.out_lo + off) = lds128(a + 2048);
-          }
+        if (lane == 0) {
+          tma_store_3d(&tmap_o, stg, c * 32, i0, plane_o);
+          if (p.out_lo != nullptr) tma_store_3d(&tmap_olo, stg + 2048, c * 32, i0, plane_o);
+          bulk_commit_group();
         }
       }
       if (in_range) p.lse[row] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
       tc_fence_before();
     }
+    if (lane == 0) bulk_wait_all();  // this warp's output stores are done
+    __syncwarp();
   }
 
   // ------------------------------------------------------------ teardown
@@ -530,7 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool kDrop>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
-                                const CUtensorMap& tv, const FwdParams& p, int num_sms,
+                                const CUtensorMap& tv, const CUtensorMap& to,
+                                const CUtensorMap& tol, const FwdParams& p, int num_sms,
                                 cudaStream_t stream) {
   using C = FwdCfg<D>;
   static bool attr_set[64] = {};
@@ -544,7 +552,7 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
   }
   const int grid = p.n_units < num_sms ? p.n_units : num_sms;
   if (grid <= 0) return cudaSuccess;
-  bd_fwd_kernel<D, kDrop><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, p);
+  bd_fwd_kernel<D, kDrop><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, tol, p);
   return cudaGetLastError();
 }
 
@@ -560,7 +568,7 @@ __global__ void __launch_bounds__(256) v_to_f16_kernel(const uint4* __restrict__
 }
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const AttnDims& d, void* plan, const void* v, void* v16, void* out,
+                       const CUtensorMap& to, const CUtensorMap& tol, const AttnDims& d, void* plan, const void* v, void* v16, void* out,
                        void* out_lo, float* lse, int32_t* status, int num_sms,
                        cudaStream_t stream) {
   {
@@ -598,11 +606,11 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.ctr = reinterpret_cast<int*>(base + pl.sched);
   p.drop = d.drop;
   if (d.drop.on) {
-    if (d.D == 64) return launch_fwd_t<64, true>(tq, tk, tv, p, num_sms, stream);
-    return launch_fwd_t<128, true>(tq, tk, tv, p, num_sms, stream);
+    if (d.D == 64) return launch_fwd_t<64, true>(tq, tk, tv, to, tol, p, num_sms, stream);
+    return launch_fwd_t<128, true>(tq, tk, tv, to, tol, p, num_sms, stream);
   }
-  if (d.D == 64) return launch_fwd_t<64, false>(tq, tk, tv, p, num_sms, stream);
-  return launch_fwd_t<128, false>(tq, tk, tv, p, num_sms, stream);
+  if (d.D == 64) return launch_fwd_t<64, false>(tq, tk, tv, to, tol, p, num_sms, stream);
+  return launch_fwd_t<128, false>(tq, tk, tv, to, tol, p, num_sms, stream);
 }
 
 }  // namespace bd

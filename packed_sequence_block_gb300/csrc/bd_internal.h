@@ -132,6 +132,8 @@ cudaError_t launch_plan(const int32_t* seg, const int32_t* seg_ids, const int32_
 // Tensor maps for q/k/v-like tensors [planes, rows, D] (bf16, 128-byte swizzle,
 // box 64 x 128 x 1).  Returns false when the driver rejects the map.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int planes, int rows, int D);
+// bf16 [planes, rows, D] written by TMA stores of 32 x 32 boxes (64-byte swizzle).
+bool make_tmap_out(CUtensorMap* map, const void* base, int planes, int rows, int D);
 // The same for fp16 data.
 bool make_tmap_f16(CUtensorMap* map, const void* base, int planes, int rows, int D);
 // Tensor map for the fp32 dq accumulator [planes, rows, D] (128-byte swizzle,
@@ -140,6 +142,7 @@ bool make_tmap_dqacc(CUtensorMap* map, void* base, int planes, int rows, int D);
 
 // Converts v to fp16 into v16 (the map tv describes v16), then runs the forward.
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& to, const CUtensorMap& tol,
                        const AttnDims& d, void* plan, const void* v, void* v16, void* out,
                        void* out_lo, float* lse, int32_t* status, int num_sms,
                        cudaStream_t stream);
