@@ -128,3 +128,25 @@ def test_layout_entry_points_reject_bad_arguments_on_the_host(lib_):
     k = lib_.bd_kv_needed_range
     assert k(FAKE, FAKE, FAKE, 1, 8, 4, 5, FAKE, None, None) == 1  # seq_start + L > S
     assert k(FAKE, FAKE, FAKE, 1, 8, 0, 0, FAKE, None, None) == 1  # L < 1
+
+
+@pytest.mark.parametrize("p", [1.0, 1.5, -0.1, float("nan")])
+def test_dropout_entry_points_reject_bad_p_on_the_host(lib_, p):
+    """dropout_p outside [0, 1) is refused before any shape check or launch."""
+    f = lib_.bd_attn_fwd_dropout
+    assert f(FAKE, FAKE, FAKE, 1, 4, 2, 256, 256, 64, 0, 0.0, 1, FAKE, 1 << 30, FAKE, FAKE, None,
+             FAKE, 1 << 30, p, 7, 0, None, None) == 1
+    g = lib_.bd_attn_bwd_dropout
+    assert g(*([FAKE] * 7), 1, 4, 2, 256, 256, 64, 0, 0.0, 1, FAKE, 1 << 30, FAKE, FAKE, FAKE,
+             FAKE, 1 << 30, p, 7, 0, None, None) == 1
+
+
+def test_dropout_entry_points_check_shapes_like_the_plain_ones(lib_):
+    f = lib_.bd_attn_fwd_dropout
+    assert f(FAKE, FAKE, FAKE, 1, 4, 2, 256, 256, 96, 0, 0.0, 1, FAKE, 1 << 30, FAKE, FAKE, None,
+             FAKE, 1 << 30, 0.1, 7, 0, None, None) == 2   # D = 96 unsupported
+    assert f(FAKE, FAKE, FAKE, 1, 4, 2, 256, 256, 64, 0, 0.0, 1, FAKE, 1 << 30, FAKE, FAKE, None,
+             FAKE, 16, 0.1, 7, 0, None, None) == 5        # workspace too small
+    g = lib_.bd_attn_bwd_dropout
+    assert g(*([FAKE] * 7), 1, 4, 2, 256, 256, 64, 0, 0.0, 1, FAKE, 1 << 30, FAKE, FAKE, FAKE,
+             FAKE, 8, 0.1, 7, 0, None, None) == 5         # workspace too small
