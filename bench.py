@@ -22,6 +22,7 @@ import hashlib
 import json
 import os
 import statistics
+import tempfile
 import subprocess
 import sys
 import time
@@ -545,9 +546,11 @@ def main():
     check_device_status(device)
 
     peaks, peak_src = read_peaks()
-    sampler = ClockSampler(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
-                           if os.path.isdir(os.path.join(ROOT, "gpurun_out"))
-                           else f"/tmp/bd_clocks_{os.getpid()}.csv")
+    # the raw samples go to BD_CLOCKS_DIR when it is set (the JSON line carries the summary)
+    clocks_dir = os.environ.get("BD_CLOCKS_DIR")
+    sampler = ClockSampler(os.path.join(clocks_dir, f"clocks_rank{rank}.csv") if clocks_dir
+                           else os.path.join(tempfile.gettempdir(),
+                                             f"bd_clocks_{os.getpid()}_{rank}.csv"))
     step_ms = []
     barrier()
     with sampler:
