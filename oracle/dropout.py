@@ -32,11 +32,13 @@ are scaled by 1 / (1 - p'), which keeps the expectation exact.  The query's
 global position (not its local row) enters the counter, so a row split into
 query intervals draws the same mask as the whole row.
 
-Parity unpinned for the exact Philox stream: the published known-answer
-vectors are not at hand, so the generator is pinned only by properties
-(bijectivity, uniform words, the drop rate); the dropout arithmetic itself is
-pinned by exact reductions (p = 0, expectation over masks, finite
-differences with the mask fixed).
+Pins: the generator's words equal those of an independent implementation,
+cuRAND's device Philox4_32_10 (tests/test_oracle_philox_gpu.py, run on a
+GPU), for random seeds and counters; on the CPU it is held by properties
+(bijectivity, uniform words, the drop rate, independent neighbouring keys).
+The dropout arithmetic is pinned by exact reductions (p = 0, a dense
+restatement, the expectation over masks, finite differences with the mask
+fixed).
 """
 from __future__ import annotations
 

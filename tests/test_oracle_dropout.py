@@ -1,9 +1,10 @@
 """Pins for attention dropout in the oracle.
 
 Page "nemo_automodel.components.distributed.blockdiag_cp", cp_blockdiag_sdpa
-(dropout_p).  The generator (Philox4x32-10, Salmon et al., SC'11) is pinned by
-properties only (bijectivity, uniform words, the drop rate, independent
-neighbouring keys); the dropout
+(dropout_p).  The generator (Philox4x32-10, Salmon et al., SC'11) is pinned here by
+properties (bijectivity, uniform words, the drop rate, independent
+neighbouring keys) and, on a GPU, word for word against cuRAND's
+implementation (test_oracle_philox_gpu.py); the dropout
 arithmetic by exact reductions: p = 0, a dense element-by-element restatement
 with the mask written out, the expectation over masks, finite differences
 with the mask fixed, and interval invariance.
