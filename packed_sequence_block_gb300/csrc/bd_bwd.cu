@@ -554,6 +554,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           cb = min(kend, p.seq_start + p.L) - q0 - 1;
         }
         const bool full = __all_sync(0xffffffffu, ca <= c0 && cb >= c0 + 63);
+        uint32_t mw[2];  // allowed columns of this group's 64, 32 per word
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          const int lo = max(ca - c0 - 32 * w, 0), hi = min(cb - c0 - 32 * w, 31);
+          mw[w] = (lo > hi) ? 0u
+                            : ((0xffffffffu >> (31 - max(hi, 0))) & (0xffffffffu << min(lo, 31)));
+        }
         // the stage holds lse*log2(e) of the tile's 128 queries, then their Delta
         const float4* lse4 =
             reinterpret_cast<const float4*>(smem + C::OFF_LSED + st * 1024) + (c0 >> 2);
@@ -571,11 +578,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             float p2 = fast_exp2(fmaf(__uint_as_float(sv[e + 2]), p.scale_log2, -x.z));
             float p3 = fast_exp2(fmaf(__uint_as_float(sv[e + 3]), p.scale_log2, -x.w));
             if (!full) {
-              const int col = c0 + c * 32 + e;
-              p0 = (col >= ca && col <= cb) ? p0 : 0.f;
-              p1 = (col + 1 >= ca && col + 1 <= cb) ? p1 : 0.f;
-              p2 = (col + 2 >= ca && col + 2 <= cb) ? p2 : 0.f;
-              p3 = (col + 3 >= ca && col + 3 <= cb) ? p3 : 0.f;
+              const uint32_t m = mw[c] >> e;
+              p0 = (m & 1u) ? p0 : 0.f;
+              p1 = (m & 2u) ? p1 : 0.f;
+              p2 = (m & 4u) ? p2 : 0.f;
+              p3 = (m & 8u) ? p3 : 0.f;
             }
             pk[c * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
             pk[c * 16 + (e >> 1) + 1] = pack_bf16x2(p2, p3);

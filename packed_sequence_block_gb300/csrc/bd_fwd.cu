@@ -389,9 +389,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[128];
         tmem_ld128(tS, v);
         if (!full) {
+          uint32_t mw[4];  // allowed columns [ca, cb], 32 per word
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int lo = max(ca - 32 * w, 0), hi = min(cb - 32 * w, 31);
+            mw[w] = (lo > hi) ? 0u
+                              : ((0xffffffffu >> (31 - max(hi, 0))) & (0xffffffffu << min(lo, 31)));
+          }
 #pragma unroll
           for (int e = 0; e < kBN; ++e)
-            v[e] = (e >= ca && e <= cb) ? v[e] : 0xff800000u;
+            v[e] = ((mw[e >> 5] >> (e & 31)) & 1u) ? v[e] : 0xff800000u;
         }
         // row max over four independent chains of three-input maxima
         float m4[4];
