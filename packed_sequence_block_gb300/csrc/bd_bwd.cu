@@ -5,7 +5,7 @@
 // dS = P * (dP - Delta), dq = scale dS K, dk = scale dS^T Q, dv = P^T dO.
 //
 // Kernels:
-//  bwd_pre    Delta per row, lse in log2 units, zero the fp32 dq accumulator
+//  bwd_pre    -Delta and -lse (log2 units) per row, zero the fp32 dq accumulator
 //  bd_bwd     persistent; one work unit = one 128-key tile of one K/V head,
 //             looping over the G query heads of the group and the query tiles
 //             the plan marks non-empty.  Per iteration (tcgen05, TMEM):
@@ -58,8 +58,9 @@ struct BwdParams {
   const int32_t* kend;
   const int32_t* bwd_range;
   const int32_t* bwd_order;
-  const float* lse2;   // lse * log2(e) per query row, +inf where the row attends nothing
-  const float* delta;  // Delta = <dO, O> per query row
+  // negated so that the P and dS phases add them with paired fp32 arithmetic
+  const float* nlse2;   // -lse * log2(e) per query row, -inf where the row attends nothing
+  const float* ndelta;  // -Delta = -<dO, O> per query row
   float* dqacc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -160,13 +161,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 // ------------------------------------------------------------------ preprocess
 
-// One thread per 8 elements of a query row: Delta, lse in log2 units and the
+// One thread per 8 elements of a query row: -Delta, -lse in log2 units and the
 // zeroed dq accumulator.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(
     const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ out_lo,
     const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse, int planes, int L,
-    int Lq, float* __restrict__ lse2o, float* __restrict__ deltao, float* __restrict__ dqacc) {
+    int Lq, float* __restrict__ nlse2o, float* __restrict__ ndeltao, float* __restrict__ dqacc) {
   constexpr int TPR = D / 8;  // threads per row (a power of two dividing 32)
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (tid >= (long long)planes * Lq * TPR) return;  // a multiple of 32: whole warps leave
@@ -200,16 +201,16 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(
 #pragma unroll
   for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, TPR);
   if (part == 0) {
-    float l2 = INFINITY, dl = 0.f;
+    float nl2 = -INFINITY, ndl = 0.f;
     if (i < L) {
       const float x = lse[(size_t)plane * L + i];
       if (x != -INFINITY) {
-        l2 = x * kLog2e;
-        dl = acc;
+        nl2 = -(x * kLog2e);
+        ndl = -acc;
       }
     }
-    lse2o[(size_t)plane * Lq + i] = l2;
-    deltao[(size_t)plane * Lq + i] = dl;
+    nlse2o[(size_t)plane * Lq + i] = nl2;
+    ndeltao[(size_t)plane * Lq + i] = ndl;
   }
 }
 
@@ -360,8 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(smem + C::OFF_Q + st * C::TILE + j * 16384, &tmap_q, st_full + st, 64 * j,
                         qt * kBM, qplane);
           const size_t ro = (size_t)qplane * p.Lq + qt * kBM;
-          bulk_load(smem + C::OFF_LSED + st * 1024, p.lse2 + ro, 512, st_full + st);
-          bulk_load(smem + C::OFF_LSED + st * 1024 + 512, p.delta + ro, 512, st_full + st);
+          bulk_load(smem + C::OFF_LSED + st * 1024, p.nlse2 + ro, 512, st_full + st);
+          bulk_load(smem + C::OFF_LSED + st * 1024 + 512, p.ndelta + ro, 512, st_full + st);
           ++st_it;
           // dO_i after dV_{i-1}; Q_{i+1} (next round) waits for dK_{i-1}, which follows dV_{i-1}
           ok = mbar_wait(do_empty, (do_it & 1) ^ 1, abort_flag, p.status);
@@ -561,10 +562,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mw[w] = (lo > hi) ? 0u
                             : ((0xffffffffu >> (31 - max(hi, 0))) & (0xffffffffu << min(lo, 31)));
         }
-        // the stage holds lse*log2(e) of the tile's 128 queries, then their Delta
-        const float4* lse4 =
+        // the stage holds -lse*log2(e) of the tile's 128 queries, then their -Delta
+        const float4* nlse4 =
             reinterpret_cast<const float4*>(smem + C::OFF_LSED + st * 1024) + (c0 >> 2);
-        const float4* dl4 = lse4 + 32;
+        const float4* ndl4 = nlse4 + 32;
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
         uint32_t pk[32];  // P^T of this key row as bf16 pairs (the dV MMA's operand), kept for dS
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -572,11 +574,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tS + c * 32, sv);
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
-            const float4 x = lse4[(c * 32 + e) >> 2];  // lse*log2(e) of four columns
-            float p0 = fast_exp2(fmaf(__uint_as_float(sv[e]), p.scale_log2, -x.x));
-            float p1 = fast_exp2(fmaf(__uint_as_float(sv[e + 1]), p.scale_log2, -x.y));
-            float p2 = fast_exp2(fmaf(__uint_as_float(sv[e + 2]), p.scale_log2, -x.z));
-            float p3 = fast_exp2(fmaf(__uint_as_float(sv[e + 3]), p.scale_log2, -x.w));
+            const float4 x = nlse4[(c * 32 + e) >> 2];  // -lse*log2(e) of four columns
+            const float2 t01 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                     sc2, make_float2(x.x, x.y));
+            const float2 t23 =
+                ffma2(make_float2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), sc2,
+                      make_float2(x.z, x.w));
+            float p0 = fast_exp2(t01.x);
+            float p1 = fast_exp2(t01.y);
+            float p2 = fast_exp2(t23.x);
+            float p3 = fast_exp2(t23.y);
             if (!full) {
               const uint32_t m = mw[c] >> e;
               p0 = (m & 1u) ? p0 : 0.f;
@@ -615,28 +622,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t dk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
-            const float4 x = dl4[(c * 32 + e) >> 2];  // Delta of four columns
+            const float4 x = ndl4[(c * 32 + e) >> 2];  // -Delta of four columns
             const uint32_t pa = pk[c * 16 + (e >> 1)], pb = pk[c * 16 + (e >> 1) + 1];
             if constexpr (kDrop) {
               // dS = P (rp M dP - Delta)
               const uint32_t kb = (c == 0 ? keep_lo : keep_hi) >> e;
               const float rp = p.drop.rp;
-              const float d0 = (kb & 1u) ? fmaf(rp, __uint_as_float(dv[e]), -x.x) : -x.x;
-              const float d1 = (kb & 2u) ? fmaf(rp, __uint_as_float(dv[e + 1]), -x.y) : -x.y;
-              const float d2 = (kb & 4u) ? fmaf(rp, __uint_as_float(dv[e + 2]), -x.z) : -x.z;
-              const float d3 = (kb & 8u) ? fmaf(rp, __uint_as_float(dv[e + 3]), -x.w) : -x.w;
+              const float d0 = (kb & 1u) ? fmaf(rp, __uint_as_float(dv[e]), x.x) : x.x;
+              const float d1 = (kb & 2u) ? fmaf(rp, __uint_as_float(dv[e + 1]), x.y) : x.y;
+              const float d2 = (kb & 4u) ? fmaf(rp, __uint_as_float(dv[e + 2]), x.z) : x.z;
+              const float d3 = (kb & 8u) ? fmaf(rp, __uint_as_float(dv[e + 3]), x.w) : x.w;
               dk[e >> 1] = pack_bf16x2(__uint_as_float(pa << 16) * d0,
                                        __uint_as_float(pa & 0xffff0000u) * d1);
               dk[(e >> 1) + 1] = pack_bf16x2(__uint_as_float(pb << 16) * d2,
                                              __uint_as_float(pb & 0xffff0000u) * d3);
               continue;
             }
-            dk[e >> 1] = pack_bf16x2(__uint_as_float(pa << 16) * (__uint_as_float(dv[e]) - x.x),
-                                    __uint_as_float(pa & 0xffff0000u) *
-                                        (__uint_as_float(dv[e + 1]) - x.y));
-            dk[(e >> 1) + 1] =
-                pack_bf16x2(__uint_as_float(pb << 16) * (__uint_as_float(dv[e + 2]) - x.z),
-                           __uint_as_float(pb & 0xffff0000u) * (__uint_as_float(dv[e + 3]) - x.w));
+            // dS = P (dP + (-Delta)), in pairs
+            const float2 s01 = fmul2(
+                make_float2(__uint_as_float(pa << 16), __uint_as_float(pa & 0xffff0000u)),
+                fadd2(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
+                      make_float2(x.x, x.y)));
+            const float2 s23 = fmul2(
+                make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xffff0000u)),
+                fadd2(make_float2(__uint_as_float(dv[e + 2]), __uint_as_float(dv[e + 3])),
+                      make_float2(x.z, x.w)));
+            dk[e >> 1] = pack_bf16x2(s01.x, s01.y);
+            dk[(e >> 1) + 1] = pack_bf16x2(s23.x, s23.y);
           }
           // dS (queries contiguous) into the 128-byte-swizzled tile that is the K-major
           // A operand of dK = dS^T Q and the MN-major A operand of dQ = dS K
@@ -834,7 +846,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
     bwd_pre_kernel<D><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(out_lo),
         static_cast<const __nv_bfloat16*>(dout), lse, planes, p.L, p.Lq,
-        const_cast<float*>(p.lse2), const_cast<float*>(p.delta), p.dqacc);
+        const_cast<float*>(p.nlse2), const_cast<float*>(p.ndelta), p.dqacc);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -879,8 +891,8 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.kend = reinterpret_cast<const int32_t*>(base + pl.kend);
   p.bwd_range = reinterpret_cast<const int32_t*>(base + pl.bwd_range);
   p.bwd_order = reinterpret_cast<const int32_t*>(base + pl.bwd_order);
-  p.lse2 = reinterpret_cast<const float*>(ws + wl.lsed);
-  p.delta = p.lse2 + (size_t)d.B * d.Hq * wl.Lq;
+  p.nlse2 = reinterpret_cast<const float*>(ws + wl.lsed);
+  p.ndelta = p.nlse2 + (size_t)d.B * d.Hq * wl.Lq;
   p.dqacc = reinterpret_cast<float*>(ws + wl.dqacc);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);

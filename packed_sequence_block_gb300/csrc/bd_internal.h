@@ -69,7 +69,7 @@ inline PlanLayout plan_layout(int B, int Hq, int Hkv, int L, int S) {
 }
 
 // Backward workspace: fp32 dq accumulator [B,Hq,L,D], then per-row
-// lse * log2 e [B,Hq,Lq] followed by Delta [B,Hq,Lq] (Lq = ceil(L/128)*128).
+// -lse * log2 e [B,Hq,Lq] followed by -Delta [B,Hq,Lq] (Lq = ceil(L/128)*128).
 struct BwdLayout {
   int Lq;
   size_t dqacc, lsed, total;
