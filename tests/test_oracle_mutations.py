@@ -14,6 +14,7 @@ import pytest
 
 import test_oracle_dropout as dpins
 import test_oracle_pins as pins
+import test_oracle_row_slices as spins
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                    "oracle", "blockdiag.py")
@@ -47,6 +48,16 @@ MUTATIONS = {
         "                                          np.arange(r0, r1) - seq_start + mask_pos0"),
     "interval_offset": ("q[b, h, r0 - seq_start:r1 - seq_start] @ k[b, g, start:r1].T",
                         "q[b, h, r0:r1] @ k[b, g, start:r1].T"),
+    # mistakes that only show once a segment is cut into several row slices
+    "slices_overlap": ("yield t, min(t1, t + step)", "yield t, min(t1, t + step + 1)"),
+    "slice_rows_from_first_slice": (
+        "q[b, h, r0 - seq_start:r1 - seq_start] @ k[b, g, start:r1].T",
+        "q[b, h, t0 - seq_start:t0 - seq_start + r1 - r0] @ k[b, g, start:r1].T"),
+    "slice_dropout_rows_from_first_slice": (
+        "p = p * keep_mask(_mask_plane(mask_planes, b, h, Hq),\n"
+        "                                          np.arange(r0, r1) + mask_pos0",
+        "p = p * keep_mask(_mask_plane(mask_planes, b, h, Hq),\n"
+        "                                          np.arange(t0, t0 + r1 - r0) + mask_pos0"),
 }
 
 
@@ -76,6 +87,9 @@ def _pins(orc, monkeypatch):
         lambda: dpins.test_dropout_forward_matches_dense_statement(dpins.CASES[1]),
         lambda: dpins.test_dropout_backward_matches_finite_differences(),
         lambda: dpins.test_dropout_intervals_concatenate_to_full_rows(),
+    ] + [
+        (lambda n=n, b=b: spins.check_sliced_oracle(orc, n, b))
+        for n in sorted(spins.CASES) for b in (5, 256)
     ]
     failed = 0
     for c in checks:
