@@ -2,9 +2,10 @@
 """Benchmark of the block-diagonal causal attention hot path on GB300.
 
 One step = the whole path on one synthetic packed batch, every call through
-the C ABI: doc ids from cu_seqlens -> segments -> plan (tile classifier and
-longest-first lists) -> forward -> backward (per-row terms, main kernel, dq
-conversion).  Default workload: 1 row x 8192 tokens, Hq=32, Hkv=8, D=128,
+the C ABI's single-call entry points: bd_attn_fwd (the plan -- mask bounds
+and longest-first tile lists -- from cu_seqlens, the fp16 copy of v, the
+forward kernel) then bd_attn_bwd (the plan again with the per-row terms, the
+main kernel, the dq conversion), for every query interval.  Default workload: 1 row x 8192 tokens, Hq=32, Hkv=8, D=128,
 lognormal(1024, 1.0) document lengths (seed 0).
 
 Metric: useful TFLOP/s = 14 * D * (unmasked query/key pairs) * Hq per step
@@ -37,7 +38,11 @@ from packed_sequence_block_gb300.workloads import make_qkv_do, make_workload  # 
 
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+                "utilization.gpu")
+# seconds of back-to-back step replays right before the timed steps, with the
+# clock sampler running, so that it records the clocks under this load
+SOAK_S = 1.5
 
 
 def parse_args():
@@ -54,6 +59,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--dropout-p", type=float, default=0.1,
                     help="also time the step with attention dropout at this p (0: skip)")
+    ap.add_argument("--soak", type=float, default=SOAK_S,
+                    help="seconds of step replays before the timed steps, under the clock sampler")
     return ap.parse_args()
 
 
@@ -88,30 +95,27 @@ def doc_boundaries(wl):
 
 def profiled_traffic(workload, seed):
     """DRAM bytes per launch of the backward main kernel from the committed ncu
-    summary, or None when the kernel sources differ from the profiled ones or
-    the workload is not the profiled one."""
-    if workload != "lognormal8k" or seed != 0:
-        return None, "no capture for this workload"
-    path = os.path.join(ROOT, "profiles", "bd_bwd_kernel_lognormal8k.md")
+    figures (profiles/bd_bwd_kernel_lognormal8k.json), or None when the kernel
+    sources differ from the profiled ones or the workload is not the profiled one."""
+    path = os.path.join(ROOT, "profiles", "bd_bwd_kernel_lognormal8k.json")
     try:
-        lines = open(path).read().splitlines()
-    except OSError:
+        with open(path) as f:
+            fig = json.load(f)
+    except (OSError, ValueError):
         return None, "no capture"
-    traffic, shas = None, {}
-    for ln in lines:
-        ln = ln.strip()
-        if ln.startswith("traffic_bytes_per_launch:"):
-            traffic = int(ln.split(":", 1)[1])
-        elif ln.startswith("source_sha256:"):
-            name, digest = ln.split(":", 1)[1].split()
-            shas[name] = digest
-    if traffic is None or not shas:
+    if workload != fig.get("workload") or seed != fig.get("seed"):
+        return None, "no capture for this workload"
+    traffic, shas = fig.get("traffic_bytes_per_launch"), fig.get("source_sha256") or {}
+    if not isinstance(traffic, int) or not shas:
         return None, "no capture"
     csrc = os.path.join(ROOT, "packed_sequence_block_gb300", "csrc")
     for name, digest in shas.items():
-        with open(os.path.join(csrc, name), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != digest:
-                return None, f"{name} changed since the ncu capture"
+        try:
+            with open(os.path.join(csrc, name), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None, f"{name} changed since the ncu capture"
+        except OSError:
+            return None, f"{name} changed since the ncu capture"
     return traffic, "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch"
 
 
@@ -127,9 +131,10 @@ def read_peaks():
 class ClockSampler:
     """nvidia-smi samples every 200 ms while the timed region runs."""
 
-    def __init__(self, path):
+    def __init__(self, path, soak=SOAK_S):
         self.path = path
         self.proc = None
+        self.soak = soak
 
     def __enter__(self):
         try:
@@ -152,29 +157,34 @@ class ClockSampler:
             self.f.close()
 
     def summary(self, gpu_index):
+        """Median SM clock over the samples taken under load (GPU utilisation >= 50%),
+        the maximum clock, and every throttle reason seen while under load."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, mx, reasons = [], [], set()
-        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
-                 "sw_power_cap"]
+        sm_all, sm_load, mx, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
                     if int(parts[0]) != gpu_index:
                         continue
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
+                    mhz, top, util = float(parts[1]), float(parts[2]), float(parts[9])
                 except ValueError:
                     continue
-                for n, val in zip(names[1:], parts[5:9]):
-                    if val.lower() == "active":
-                        reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
+                sm_all.append(mhz)
+                mx.append(top)
+                if util >= 50.0:
+                    sm_load.append(mhz)
+                    for n, val in zip(names, parts[5:9]):
+                        if val.lower() == "active":
+                            reasons.add(n)
+        return {"sm_mhz": statistics.median(sm_load) if sm_load else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm_all), "samples_under_load": len(sm_load),
+                "window": f"{self.soak} s of back-to-back step replays, then the timed steps"}
 
 
 class HotPath:
@@ -195,23 +205,16 @@ class HotPath:
         self.q_iv = [q[:, :, s:s + L].contiguous() for s in wl.seq_starts]
         self.do_iv = [do[:, :, s:s + L].contiguous() for s in wl.seq_starts]
         del q, do
-        self.ids = torch.empty((B, S), dtype=torch.int32, device=device)
-        self.seg = torch.empty((B, S + 1), dtype=torch.int32, device=device)
-        self.sid = torch.empty((B, S), dtype=torch.int32, device=device)
-        self.nseg = torch.empty((B,), dtype=torch.int32, device=device)
-        self.plans = [torch.empty(N.bd_attn_plan_size(B, Hq, Hkv, L, S), dtype=torch.uint8,
-                                  device=device) for _ in wl.seq_starts]
         self.out = [torch.empty_like(x) for x in self.q_iv]
-        self.out_lo = [torch.empty_like(x) for x in self.q_iv]
         self.lse = [torch.empty((B, Hq, L), dtype=torch.float32, device=device)
                     for _ in wl.seq_starts]
         self.dq = [torch.empty_like(x) for x in self.q_iv]
         self.dk = torch.empty_like(k)
         self.dv = torch.empty_like(v)
-        self.fws = torch.empty(N.bd_attn_fwd_workspace_size(B, Hkv, S, D), dtype=torch.uint8,
-                               device=device)
-        self.ws = torch.empty(N.bd_attn_bwd_workspace_size(B, Hq, Hkv, L, S, D),
-                              dtype=torch.uint8, device=device)
+        # one workspace serves every interval: each interval's forward and
+        # backward run back to back on the stream
+        self.ws = torch.empty(N.bd_attn_workspace_size(B, Hq, Hkv, L, S, D), dtype=torch.uint8,
+                              device=device)
         self.status = device_status_word(device)
         self.scale = D ** -0.5
         self.gqa = Hq != Hkv
@@ -219,9 +222,8 @@ class HotPath:
         self.drop = None  # (p, seed, offset) to run the dropout entry points
 
     def launches_per_step(self):
-        # ids, segments; per interval: 2 plan kernels, v conversion + forward,
-        # backward preprocess, main and dq conversion
-        return 2 + len(self.wl.seq_starts) * 7
+        # per interval: plan + fp16 v, forward, plan + row terms, backward main, dq conversion
+        return len(self.wl.seq_starts) * 5
 
     def _io(self):
         """This object's own per-step inputs and outputs."""
@@ -230,43 +232,39 @@ class HotPath:
                 "dk": self.dk, "dv": self.dv}
 
     def step(self, time_main=False, io=None):
+        """One pass of the hot path: every query interval's forward and backward
+        through the single-call entry points (boundaries in, gradients out)."""
         N, wl = self.N, self.wl
         io = io if io is not None else self._io()
         B, S, L, Hq, Hkv, D = wl.B, wl.S, wl.L, wl.Hq, wl.Hkv, wl.D
-        N.bd_doc_ids_from_cu_seqlens(io["cu"], io["rp"], B, S, self.ids, self.status)
-        N.bd_segment_cu_seqlens(self.ids, B, S, self.seg, self.sid, self.nseg)
+        cu, rp, st = io["cu"], io["rp"], self.status
         for i, s0 in enumerate(wl.seq_starts):
-            N.bd_attn_plan(self.seg, self.sid, self.nseg, B, Hq, Hkv, L, S, s0, self.plans[i])
             if self.drop is not None:
                 p, seed, off = self.drop
-                N.bd_attn_fwd_dropout(io["q"][i], io["k"], io["v"], B, Hq, Hkv, L, S, D, s0,
-                                      self.scale, self.gqa, self.plans[i], io["out"][i],
-                                      io["lse"][i], p, seed, off, self.out_lo[i], self.fws,
-                                      self.status)
+                N.bd_attn_fwd_dropout(io["q"][i], io["k"], io["v"], B, Hq, Hkv, L, S, D, cu, rp,
+                                      s0, self.scale, self.gqa, io["out"][i], io["lse"][i],
+                                      self.ws, p, seed, off, st)
                 N.bd_attn_bwd_dropout(io["q"][i], io["k"], io["v"], io["out"][i], io["lse"][i],
-                                      io["do"][i], B, Hq, Hkv, L, S, D, s0, self.scale,
-                                      self.gqa, self.plans[i], io["dq"][i], io["dk"], io["dv"],
-                                      self.ws, p, seed, off, self.out_lo[i], self.status)
+                                      io["do"][i], B, Hq, Hkv, L, S, D, cu, rp, s0, self.scale,
+                                      self.gqa, io["dq"][i], io["dk"], io["dv"], self.ws, p,
+                                      seed, off, st)
                 continue
-            N.bd_attn_fwd(io["q"][i], io["k"], io["v"], B, Hq, Hkv, L, S, D, s0, self.scale,
-                          self.gqa, self.plans[i], io["out"][i], io["lse"][i], self.out_lo[i],
-                          self.fws, self.status)
+            N.bd_attn_fwd(io["q"][i], io["k"], io["v"], B, Hq, Hkv, L, S, D, cu, rp, s0,
+                          self.scale, self.gqa, io["out"][i], io["lse"][i], self.ws, st)
             args = (io["q"][i], io["k"], io["v"], io["out"][i], io["lse"][i], io["do"][i], B, Hq,
-                    Hkv, L, S, D, s0, self.scale, self.gqa, self.plans[i], io["dq"][i],
-                    io["dk"], io["dv"], self.ws)
-            N.bd_attn_bwd_stages(*args, out_lo=self.out_lo[i], dev_status=self.status,
-                                 stages=1)
-            if time_main:
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record()
-            N.bd_attn_bwd_stages(*args, out_lo=self.out_lo[i], dev_status=self.status,
-                                 stages=2)
-            if time_main:
-                e1.record()
-                self.main_events.append((e0, e1))
-            N.bd_attn_bwd_stages(*args, out_lo=self.out_lo[i], dev_status=self.status,
-                                 stages=4)
+                    Hkv, L, S, D, cu, rp, s0, self.scale, self.gqa, io["dq"][i], io["dk"],
+                    io["dv"], self.ws)
+            if not time_main:
+                N.bd_attn_bwd(*args, dev_status=st)
+                continue
+            N.bd_attn_bwd_stages(*args, dev_status=st, stages=1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            N.bd_attn_bwd_stages(*args, dev_status=st, stages=2)
+            e1.record()
+            self.main_events.append((e0, e1))
+            N.bd_attn_bwd_stages(*args, dev_status=st, stages=4)
 
     def e2e_setup(self):
         """Pinned host copies of the inputs, and two device/host buffer sets, so that a
@@ -550,10 +548,16 @@ def main():
     clocks_dir = os.environ.get("BD_CLOCKS_DIR")
     sampler = ClockSampler(os.path.join(clocks_dir, f"clocks_rank{rank}.csv") if clocks_dir
                            else os.path.join(tempfile.gettempdir(),
-                                             f"bd_clocks_{os.getpid()}_{rank}.csv"))
+                                             f"bd_clocks_{os.getpid()}_{rank}.csv"),
+                           args.soak)
     step_ms = []
     barrier()
     with sampler:
+        t_end = time.perf_counter() + args.soak
+        while time.perf_counter() < t_end:
+            for _ in range(50):
+                step_graph.replay()
+            torch.cuda.synchronize()
         for _ in range(args.steps):
             flush_l2(l2_buf)
             e0 = torch.cuda.Event(enable_timing=True)

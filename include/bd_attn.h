@@ -54,7 +54,7 @@ typedef enum {
 /* Human-readable text for a status code (static storage, never NULL). */
 const char* bd_status_string(int status);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor): 200. */
 int bd_version(void);
 
 /*
@@ -161,7 +161,7 @@ int bd_kv_needed_range(const int32_t* seg, const int32_t* seg_ids, const int32_t
  *                       whether Hq / Hkv is even).
  *   L, seq_start        query rows are global positions seq_start .. +L-1.
  *   plan                device buffer of bd_attn_plan_size() bytes, 256-byte
- *                       aligned, used by bd_attn_fwd / bd_attn_bwd, which must
+ *                       aligned, used by bd_attn_fwd_planned / bd_attn_bwd_planned, which must
  *                       be given the same B, Hq, Hkv, L, S, seq_start.  It also
  *                       holds the work counters those kernels take units from
  *                       (longest first) and leave at zero when they finish, so
@@ -176,61 +176,85 @@ int bd_attn_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg
                  bd_stream_t stream);
 
 /*
- * Forward pass (page "nemo_automodel.components.distributed.blockdiag_cp",
- * cp_blockdiag_sdpa: output [B, Hq, L, D] for the local rows).
+ * Forward pass in one call (page
+ * "nemo_automodel.components.distributed.blockdiag_cp", cp_blockdiag_sdpa:
+ * output [B, Hq, L, D] for the local rows, the mask "rebuilt from the
+ * document ids"; ids as doc_ids_from_cu_seqlens on the page
+ * "nemo_automodel.components.models.glm5_next.cp").
  *   q            bf16 [B, Hq, L, D]; query i sits at global position seq_start+i.
  *   k, v         bf16 [B, Hkv, S, D], the full key/value row.
  *   D            64 or 128 (else BD_ERR_UNSUPPORTED).
+ *   cu_seqlens,  each row's cumulative document boundaries, as for
+ *   row_ptr      bd_doc_ids_from_cu_seqlens (both device arrays; row_ptr is
+ *                required for every B).  The document of a position and its
+ *                bounds are found from them on the device; a row whose list
+ *                is invalid is treated as all padding and BD_ERR_INVALID_ARG
+ *                goes to *dev_status.
+ *   seq_start    0 <= seq_start, seq_start + L <= S.
  *   scale        softmax scale; a value <= 0 or not finite means D^-0.5
  *                ("None -> D**-0.5" on the page).
  *   enable_gqa   must be non-zero when Hq != Hkv (Hq a multiple of Hkv);
  *                query head h reads key/value head h / (Hq / Hkv).
- *   plan         from bd_attn_plan with the same sizes.
  *   out          bf16 [B, Hq, L, D] output.
  *   lse          fp32 [B, Hq, L] output: natural-log log-sum-exp of the
  *                scaled scores of each row (-inf for padding rows).
- *   out_lo       optional bf16 [B, Hq, L, D] output (NULL to skip): the
- *                rounding residual bf16(O - out) of the fp32 result O, so
- *                that out + out_lo carries O to about 16 significant bits.
- *                The backward uses it for Delta = <dout, O>; without it
- *                Delta is formed from the bf16 output alone.
- *   workspace    device scratch of bd_attn_fwd_workspace_size() bytes,
- *                256-byte aligned, owned by the caller; the call writes an
- *                fp16 copy of v there first.  The P V product runs with
- *                fp16 operands (the copy is exact for |x| in [2^-14, 65504];
- *                larger values become inf, so v must stay within the fp16
- *                range).  Too small: BD_ERR_WORKSPACE.
+ *   workspace    device scratch of bd_attn_workspace_size() bytes, 256-byte
+ *                aligned, owned by the caller.  The call keeps there the
+ *                attention plan (mask bounds and longest-first work lists),
+ *                an fp16 copy of v (the P V product runs with fp16 operands:
+ *                v must lie within the fp16 range, |x| <= 65504), and the
+ *                rounding residual of out, with a record of the shapes and
+ *                of out and lse.  Too small: BD_ERR_WORKSPACE.
+ * Validation on the host: B, Hq, Hkv, L, S >= 1, Hq % Hkv == 0, the interval
+ * inside the row, 16-byte aligned q, k, v, out, and B * ceil(L/128),
+ * B * ceil(S/128) <= 16384 (else BD_ERR_UNSUPPORTED).
  */
-size_t bd_attn_fwd_workspace_size(int B, int Hkv, int S, int D);
+size_t bd_attn_workspace_size(int B, int Hq, int Hkv, int L, int S, int D);
 int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L, int S,
-                int D, int seq_start, float scale, int enable_gqa, void* plan,
-                size_t plan_bytes, void* out, float* lse, void* out_lo, void* workspace,
+                int D, const int32_t* cu_seqlens, const int32_t* row_ptr, int seq_start,
+                float scale, int enable_gqa, void* out, float* lse, void* workspace,
                 size_t workspace_bytes, int32_t* dev_status, bd_stream_t stream);
 
 /*
- * Backward pass: gradients of sum(out * dout) (the autograd backward of the
- * forward above).  Same arguments as bd_attn_fwd plus
+ * Backward pass in one call: gradients of sum(out * dout) (the autograd
+ * backward of bd_attn_fwd).  Same arguments as bd_attn_fwd plus
  *   out, lse     the forward's outputs for these inputs.
- *   out_lo       the forward's residual output, or NULL (less precise Delta).
  *   dout         bf16 [B, Hq, L, D].
  *   dq           bf16 [B, Hq, L, D] output.
  *   dk, dv       bf16 [B, Hkv, S, D] outputs, summed over the query heads of
  *                each group; fully overwritten (rows no query attends are 0).
- *   workspace    device scratch of bd_attn_bwd_workspace_size() bytes,
- *                256-byte aligned (fp32 dq accumulator and per-row terms).
+ *   workspace    bd_attn_workspace_size() bytes.  The plan is rebuilt from
+ *                the boundaries.  Delta_i = <dO_i, O_i> takes O from out plus
+ *                the residual the forward kept in the workspace when the
+ *                workspace still records this out and lse with these shapes
+ *                (pass the workspace of the forward call, untouched in
+ *                between, for full precision); otherwise from out alone.
  * The dq accumulation uses floating-point atomics, so dq may differ in the
- * last bits between runs; dk and dv are deterministic.
- * All five products (K Q^T, V dO^T, P^T dO, dS^T Q, dS K) take bf16
- * operands with fp32 accumulation; P and dS = P (dP - Delta) are rounded to
- * bf16 for them.
+ * last bits between runs; dk and dv are deterministic.  All five products
+ * (K Q^T, V dO^T, P^T dO, dS^T Q, dS K) take bf16 operands with fp32
+ * accumulation; P and dS = P (dP - Delta) are rounded to bf16 for them.
  */
-size_t bd_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int S, int D);
-int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* out_lo,
-                const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S, int D,
-                int seq_start,
-                float scale, int enable_gqa, void* plan, size_t plan_bytes, void* dq,
-                void* dk, void* dv, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                bd_stream_t stream);
+int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                const void* dout, int B, int Hq, int Hkv, int L, int S, int D,
+                const int32_t* cu_seqlens, const int32_t* row_ptr, int seq_start, float scale,
+                int enable_gqa, void* dq, void* dk, void* dv, void* workspace,
+                size_t workspace_bytes, int32_t* dev_status, bd_stream_t stream);
+
+/*
+ * bd_attn_bwd in separately launchable stages (same arguments plus a bit
+ * mask), meant for timing one stage at a time.  Bit 1: the plan from the
+ * boundaries, per-row terms -lse log2 e and -Delta, and the zeroed fp32 dq
+ * accumulator (one launch).  Bit 2: the main kernel (dk, dv written; dq
+ * accumulated in the workspace).  Bit 4: dq = bf16(scale * accumulator).
+ * The stages must run in this order on the same workspace; bd_attn_bwd is
+ * stages = 7.
+ */
+int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* out,
+                       const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S,
+                       int D, const int32_t* cu_seqlens, const int32_t* row_ptr, int seq_start,
+                       float scale, int enable_gqa, void* dq, void* dk, void* dv,
+                       void* workspace, size_t workspace_bytes, int32_t* dev_status, int stages,
+                       bd_stream_t stream);
 
 /*
  * Forward and backward with attention dropout (page
@@ -260,34 +284,59 @@ int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, co
  * given the forward's dropout_p, seed and offset.
  */
 int bd_attn_fwd_dropout(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
-                        int L, int S, int D, int seq_start, float scale, int enable_gqa,
-                        void* plan, size_t plan_bytes, void* out, float* lse, void* out_lo,
-                        void* workspace, size_t workspace_bytes, double dropout_p,
-                        uint64_t seed, uint32_t offset, int32_t* dev_status,
-                        bd_stream_t stream);
+                        int L, int S, int D, const int32_t* cu_seqlens, const int32_t* row_ptr,
+                        int seq_start, float scale, int enable_gqa, void* out, float* lse,
+                        void* workspace, size_t workspace_bytes, double dropout_p, uint64_t seed,
+                        uint32_t offset, int32_t* dev_status, bd_stream_t stream);
 int bd_attn_bwd_dropout(const void* q, const void* k, const void* v, const void* out,
-                        const void* out_lo, const float* lse, const void* dout, int B, int Hq,
-                        int Hkv, int L, int S, int D, int seq_start, float scale, int enable_gqa,
-                        void* plan, size_t plan_bytes, void* dq, void* dk, void* dv,
+                        const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S,
+                        int D, const int32_t* cu_seqlens, const int32_t* row_ptr, int seq_start,
+                        float scale, int enable_gqa, void* dq, void* dk, void* dv,
                         void* workspace, size_t workspace_bytes, double dropout_p, uint64_t seed,
                         uint32_t offset, int32_t* dev_status, bd_stream_t stream);
 
 /*
- * The backward pass in separately launchable stages (same arguments as
- * bd_attn_bwd plus a bit mask).  Bit 1: per-row terms Delta_i = <dO_i, o_i>
- * and lse in log2 units, and zeroing of the fp32 dq accumulator (both in
- * `workspace`).  Bit 2: the main kernel (dk, dv written; dq accumulated into
- * the workspace).  Bit 4: dq = bf16(scale * accumulator).  The stages must
- * run in this order on the same workspace; bd_attn_bwd is stages = 7.  Meant
- * for timing one stage at a time.
+ * Lower-level forms on a plan from bd_attn_plan, for callers that hold
+ * document ids rather than boundaries (padding anywhere in a row, ids that
+ * repeat after a gap: the mask then follows the segments of the ids).  Same
+ * operation, arguments and results as the calls above, with
+ *   plan         from bd_attn_plan with the same B, Hq, Hkv, L, S, seq_start.
+ *   out_lo       forward: optional bf16 [B, Hq, L, D] output (NULL to skip),
+ *                the rounding residual bf16(O - out) of the fp32 result O, so
+ *                that out + out_lo carries O to about 16 significant bits;
+ *                backward: that residual, or NULL (Delta from out alone).
+ *   workspace    forward: bd_attn_fwd_planned_workspace_size() bytes (the
+ *                fp16 copy of v); backward:
+ *                bd_attn_bwd_planned_workspace_size() bytes (the fp32 dq
+ *                accumulator and per-row terms); 256-byte aligned.
+ * Dropout arguments as above.
  */
-int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* out,
-                       const void* out_lo, const float* lse, const void* dout, int B, int Hq,
-                       int Hkv, int L, int S,
-                       int D, int seq_start, float scale, int enable_gqa, void* plan,
-                       size_t plan_bytes, void* dq, void* dk, void* dv, void* workspace,
-                       size_t workspace_bytes, int32_t* dev_status, int stages,
-                       bd_stream_t stream);
+size_t bd_attn_fwd_planned_workspace_size(int B, int Hkv, int S, int D);
+int bd_attn_fwd_planned(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
+                        int L, int S, int D, int seq_start, float scale, int enable_gqa,
+                        void* plan, size_t plan_bytes, void* out, float* lse, void* out_lo,
+                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        bd_stream_t stream);
+int bd_attn_fwd_dropout_planned(const void* q, const void* k, const void* v, int B, int Hq,
+                                int Hkv, int L, int S, int D, int seq_start, float scale,
+                                int enable_gqa, void* plan, size_t plan_bytes, void* out,
+                                float* lse, void* out_lo, void* workspace, size_t workspace_bytes,
+                                double dropout_p, uint64_t seed, uint32_t offset,
+                                int32_t* dev_status, bd_stream_t stream);
+size_t bd_attn_bwd_planned_workspace_size(int B, int Hq, int Hkv, int L, int S, int D);
+int bd_attn_bwd_planned(const void* q, const void* k, const void* v, const void* out,
+                        const void* out_lo, const float* lse, const void* dout, int B, int Hq,
+                        int Hkv, int L, int S, int D, int seq_start, float scale, int enable_gqa,
+                        void* plan, size_t plan_bytes, void* dq, void* dk, void* dv,
+                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        bd_stream_t stream);
+int bd_attn_bwd_dropout_planned(const void* q, const void* k, const void* v, const void* out,
+                                const void* out_lo, const float* lse, const void* dout, int B,
+                                int Hq, int Hkv, int L, int S, int D, int seq_start, float scale,
+                                int enable_gqa, void* plan, size_t plan_bytes, void* dq,
+                                void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                                double dropout_p, uint64_t seed, uint32_t offset,
+                                int32_t* dev_status, bd_stream_t stream);
 
 /*
  * The backward pass without any caller-provided scratch, for callers that
@@ -297,10 +346,10 @@ int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* 
  * fail once memory is fragmented).  The pages describe no such variant; it
  * is an addition of this library.
  *
- * Same arguments and results as bd_attn_bwd, minus the workspace.  The
- * scratch is a fixed array of BD_NOALLOC_SCRATCH_BYTES (16 MiB) that the
+ * Same arguments and results as bd_attn_bwd_planned, minus the workspace.
+ * The scratch is a fixed array of BD_NOALLOC_SCRATCH_BYTES (16 MiB) that the
  * library image places on every GPU that loads it, held until the process
- * exits.  Problems whose bd_attn_bwd_workspace_size() exceeds that return
+ * exits.  Problems whose bd_attn_bwd_planned_workspace_size() exceeds that return
  * BD_ERR_WORKSPACE before anything is launched.  Nothing is allocated.
  *  - The first call on each device looks up the array's device address (with
  *    that device current) and caches it; make that first call before any
@@ -316,6 +365,25 @@ int bd_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
                         int Hkv, int L, int S, int D, int seq_start, float scale, int enable_gqa,
                         void* plan, size_t plan_bytes, void* dq, void* dk, void* dv,
                         int32_t* dev_status, bd_stream_t stream);
+
+/*
+ * Test hook for the bounded device-side waits (the pages have no counterpart;
+ * it exists to test this library's failure path).  Every wait of the
+ * forward and backward kernels gives up after 2 s, records BD_ERR_TIMEOUT in
+ * dev_status, lets the rest of the CTA stop, waits (bounded) for its own
+ * copies and tensor-core work in flight, frees its tensor memory and returns,
+ * so the context stays usable.  This call makes the next launch of one
+ * kernel from the calling host thread exercise that path on purpose: its
+ * producer publishes its first work unit but never loads that unit's first
+ * tile, and its waits give up after limit_us microseconds instead of 2 s.
+ *   which      1: the forward kernel (bd_attn_fwd*), 2: the backward main
+ *              kernel (bd_attn_bwd*, stage 2).
+ *   limit_us   1 .. 2000000.
+ * The request is used by that one launch and then dropped; its results are
+ * not valid (the status says BD_ERR_TIMEOUT).  Returns BD_ERR_INVALID_ARG for
+ * other arguments.
+ */
+int bd_test_arm_wait_timeout(int which, unsigned int limit_us);
 
 /*
  * Copy the device status word to *host_status after the work already queued

@@ -39,28 +39,39 @@ SIGNATURES = {
     "bd_kv_needed_range": (_c_int, [_vp, _vp, _vp] + [_c_int] * 4 + [_vp, _vp, _vp]),
     "bd_attn_plan_size": (_c_size, [_c_int] * 5),
     "bd_attn_plan": (_c_int, [_vp, _vp, _vp] + [_c_int] * 6 + [_vp, _c_size, _vp]),
-    "bd_attn_fwd_workspace_size": (_c_size, [_c_int] * 4),
-    "bd_attn_fwd": (_c_int, [_vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size,
-                                                               _vp, _vp, _vp, _vp, _c_size,
-                                                               _vp, _vp]),
-    "bd_attn_fwd_dropout": (_c_int, [_vp, _vp, _vp] + [_c_int] * 7 + [
+    "bd_attn_workspace_size": (_c_size, [_c_int] * 6),
+    "bd_attn_fwd": (_c_int, [_vp] * 3 + [_c_int] * 6 + [_vp, _vp, _c_int, _c_float, _c_int,
+                                                        _vp, _vp, _vp, _c_size, _vp, _vp]),
+    "bd_attn_bwd": (_c_int, [_vp] * 6 + [_c_int] * 6 + [_vp, _vp, _c_int, _c_float, _c_int,
+                                                        _vp, _vp, _vp, _vp, _c_size, _vp, _vp]),
+    "bd_attn_bwd_stages": (_c_int, [_vp] * 6 + [_c_int] * 6 + [
+        _vp, _vp, _c_int, _c_float, _c_int, _vp, _vp, _vp, _vp, _c_size, _vp, _c_int, _vp]),
+    "bd_attn_fwd_dropout": (_c_int, [_vp] * 3 + [_c_int] * 6 + [
+        _vp, _vp, _c_int, _c_float, _c_int, _vp, _vp, _vp, _c_size, _c_double, _c_u64, _c_u32,
+        _vp, _vp]),
+    "bd_attn_bwd_dropout": (_c_int, [_vp] * 6 + [_c_int] * 6 + [
+        _vp, _vp, _c_int, _c_float, _c_int, _vp, _vp, _vp, _vp, _c_size, _c_double, _c_u64,
+        _c_u32, _vp, _vp]),
+    "bd_attn_fwd_planned_workspace_size": (_c_size, [_c_int] * 4),
+    "bd_attn_fwd_planned": (_c_int, [_vp, _vp, _vp] + [_c_int] * 7 + [
+        _c_float, _c_int, _vp, _c_size, _vp, _vp, _vp, _vp, _c_size, _vp, _vp]),
+    "bd_attn_fwd_dropout_planned": (_c_int, [_vp, _vp, _vp] + [_c_int] * 7 + [
         _c_float, _c_int, _vp, _c_size, _vp, _vp, _vp, _vp, _c_size, _c_double, _c_u64, _c_u32,
         _vp, _vp]),
-    "bd_attn_bwd_workspace_size": (_c_size, [_c_int] * 6),
-    "bd_attn_bwd": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size, _vp,
-                                                         _vp, _vp, _vp, _c_size, _vp, _vp]),
-    "bd_attn_bwd_dropout": (_c_int, [_vp] * 7 + [_c_int] * 7 + [
+    "bd_attn_bwd_planned_workspace_size": (_c_size, [_c_int] * 6),
+    "bd_attn_bwd_planned": (_c_int, [_vp] * 7 + [_c_int] * 7 + [
+        _c_float, _c_int, _vp, _c_size, _vp, _vp, _vp, _vp, _c_size, _vp, _vp]),
+    "bd_attn_bwd_dropout_planned": (_c_int, [_vp] * 7 + [_c_int] * 7 + [
         _c_float, _c_int, _vp, _c_size, _vp, _vp, _vp, _vp, _c_size, _c_double, _c_u64, _c_u32,
         _vp, _vp]),
-    "bd_attn_bwd_stages": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size,
-                                                                _vp, _vp, _vp, _vp, _c_size, _vp,
-                                                                _c_int, _vp]),
     "bd_attn_bwd_noalloc": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_c_float, _c_int, _vp, _c_size,
                                                                  _vp, _vp, _vp, _vp, _vp]),
+    "bd_test_arm_wait_timeout": (_c_int, [_c_int, ctypes.c_uint]),
     "bd_get_device_status": (_c_int, [_vp, _vp, _vp]),
 }
 
-# Size of the fixed scratch array bd_attn_bwd_noalloc uses (BD_NOALLOC_SCRATCH_BYTES).
+# Size of the fixed scratch array bd_attn_bwd_noalloc uses (BD_NOALLOC_SCRATCH_BYTES in
+# include/bd_attn.h; a CPU test keeps the two equal).
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lib = None
@@ -191,106 +202,169 @@ def bd_attn_plan_size(B: int, Hq: int, Hkv: int, L: int, S: int) -> int:
 def bd_attn_plan(seg, seg_ids, nseg, B: int, Hq: int, Hkv: int, L: int, S: int, seq_start: int,
                  plan, stream=None) -> None:
     _check(lib().bd_attn_plan(_ptr(seg), _ptr(seg_ids), _ptr(nseg), B, Hq, Hkv, L, S, seq_start,
-                              _ptr(plan), plan.numel() * plan.element_size(), _stream(stream)),
+                              _ptr(plan), _nbytes(plan), _stream(stream)),
            "bd_attn_plan")
 
 
-def bd_attn_fwd_workspace_size(B: int, Hkv: int, S: int, D: int) -> int:
-    return int(lib().bd_attn_fwd_workspace_size(B, Hkv, S, D))
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
 
 
-def bd_attn_fwd(q, k, v, B: int, Hq: int, Hkv: int, L: int, S: int, D: int, seq_start: int,
-                scale: float, enable_gqa: bool, plan, out, lse, out_lo=None, workspace=None,
+def _want_all(pairs, dtype):
+    for t, n in pairs:
+        _want(t, dtype, n)
+
+
+# ---- single-call forms: cumulative boundaries and one workspace
+
+def bd_attn_workspace_size(B: int, Hq: int, Hkv: int, L: int, S: int, D: int) -> int:
+    return int(lib().bd_attn_workspace_size(B, Hq, Hkv, L, S, D))
+
+
+def bd_attn_fwd(q, k, v, B: int, Hq: int, Hkv: int, L: int, S: int, D: int, cu_seqlens, row_ptr,
+                seq_start: int, scale: float, enable_gqa: bool, out, lse, workspace,
                 dev_status=None, stream=None) -> None:
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
-        _want(t, torch.bfloat16, n)
-    if out_lo is not None:
-        _want(out_lo, torch.bfloat16, "out_lo")
+    _want_all(((q, "q"), (k, "k"), (v, "v"), (out, "out")), torch.bfloat16)
+    _want_all(((cu_seqlens, "cu_seqlens"), (row_ptr, "row_ptr")), torch.int32)
     _want(lse, torch.float32, "lse")
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib().bd_attn_fwd(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, L, S, D, seq_start,
-                             float(scale), int(bool(enable_gqa)), _ptr(plan),
-                             plan.numel() * plan.element_size(), _ptr(out), _ptr(lse),
-                             _ptr(out_lo), _ptr(workspace), ws_bytes, _ptr(dev_status),
-                             _stream(stream)), "bd_attn_fwd")
+    _check(lib().bd_attn_fwd(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, L, S, D, _ptr(cu_seqlens),
+                             _ptr(row_ptr), seq_start, float(scale), int(bool(enable_gqa)),
+                             _ptr(out), _ptr(lse), _ptr(workspace), _nbytes(workspace),
+                             _ptr(dev_status), _stream(stream)), "bd_attn_fwd")
 
 
-def bd_attn_fwd_dropout(q, k, v, B: int, Hq: int, Hkv: int, L: int, S: int, D: int,
-                        seq_start: int, scale: float, enable_gqa: bool, plan, out, lse,
-                        dropout_p: float, seed: int, offset: int = 0, out_lo=None,
-                        workspace=None, dev_status=None, stream=None) -> None:
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
-        _want(t, torch.bfloat16, n)
-    if out_lo is not None:
-        _want(out_lo, torch.bfloat16, "out_lo")
+def bd_attn_bwd(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: int, D: int,
+                cu_seqlens, row_ptr, seq_start: int, scale: float, enable_gqa: bool, dq, dk, dv,
+                workspace, dev_status=None, stream=None) -> None:
+    _want_all(((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"),
+               (dk, "dk"), (dv, "dv")), torch.bfloat16)
+    _want_all(((cu_seqlens, "cu_seqlens"), (row_ptr, "row_ptr")), torch.int32)
     _want(lse, torch.float32, "lse")
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib().bd_attn_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, L, S, D, seq_start,
-                                     float(scale), int(bool(enable_gqa)), _ptr(plan),
-                                     plan.numel() * plan.element_size(), _ptr(out), _ptr(lse),
-                                     _ptr(out_lo), _ptr(workspace), ws_bytes, float(dropout_p),
+    _check(lib().bd_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), B, Hq,
+                             Hkv, L, S, D, _ptr(cu_seqlens), _ptr(row_ptr), seq_start,
+                             float(scale), int(bool(enable_gqa)), _ptr(dq), _ptr(dk), _ptr(dv),
+                             _ptr(workspace), _nbytes(workspace), _ptr(dev_status),
+                             _stream(stream)), "bd_attn_bwd")
+
+
+def bd_attn_bwd_stages(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: int,
+                       D: int, cu_seqlens, row_ptr, seq_start: int, scale: float,
+                       enable_gqa: bool, dq, dk, dv, workspace, dev_status=None, stages: int = 7,
+                       stream=None) -> None:
+    _check(lib().bd_attn_bwd_stages(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                    B, Hq, Hkv, L, S, D, _ptr(cu_seqlens), _ptr(row_ptr),
+                                    seq_start, float(scale), int(bool(enable_gqa)), _ptr(dq),
+                                    _ptr(dk), _ptr(dv), _ptr(workspace), _nbytes(workspace),
+                                    _ptr(dev_status), int(stages), _stream(stream)),
+           "bd_attn_bwd_stages")
+
+
+def bd_attn_fwd_dropout(q, k, v, B: int, Hq: int, Hkv: int, L: int, S: int, D: int, cu_seqlens,
+                        row_ptr, seq_start: int, scale: float, enable_gqa: bool, out, lse,
+                        workspace, dropout_p: float, seed: int, offset: int = 0, dev_status=None,
+                        stream=None) -> None:
+    _want_all(((q, "q"), (k, "k"), (v, "v"), (out, "out")), torch.bfloat16)
+    _want_all(((cu_seqlens, "cu_seqlens"), (row_ptr, "row_ptr")), torch.int32)
+    _want(lse, torch.float32, "lse")
+    _check(lib().bd_attn_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, L, S, D,
+                                     _ptr(cu_seqlens), _ptr(row_ptr), seq_start, float(scale),
+                                     int(bool(enable_gqa)), _ptr(out), _ptr(lse),
+                                     _ptr(workspace), _nbytes(workspace), float(dropout_p),
                                      int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF,
                                      _ptr(dev_status), _stream(stream)), "bd_attn_fwd_dropout")
 
 
-def bd_attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, L: int, S: int, D: int) -> int:
-    return int(lib().bd_attn_bwd_workspace_size(B, Hq, Hkv, L, S, D))
-
-
-def bd_attn_bwd(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: int, D: int,
-                seq_start: int, scale: float, enable_gqa: bool, plan, dq, dk, dv, workspace,
-                out_lo=None, dev_status=None, stream=None) -> None:
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"),
-                 (dk, "dk"), (dv, "dv")):
-        _want(t, torch.bfloat16, n)
-    _want(lse, torch.float32, "lse")
-    _check(lib().bd_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo), _ptr(lse),
-                             _ptr(dout), B, Hq,
-                             Hkv, L, S, D, seq_start, float(scale), int(bool(enable_gqa)),
-                             _ptr(plan), plan.numel() * plan.element_size(), _ptr(dq), _ptr(dk),
-                             _ptr(dv), _ptr(workspace),
-                             workspace.numel() * workspace.element_size(), _ptr(dev_status),
-                             _stream(stream)), "bd_attn_bwd")
-
-
 def bd_attn_bwd_dropout(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: int,
-                        D: int, seq_start: int, scale: float, enable_gqa: bool, plan, dq, dk, dv,
-                        workspace, dropout_p: float, seed: int, offset: int = 0, out_lo=None,
-                        dev_status=None, stream=None) -> None:
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"),
-                 (dk, "dk"), (dv, "dv")):
-        _want(t, torch.bfloat16, n)
+                        D: int, cu_seqlens, row_ptr, seq_start: int, scale: float,
+                        enable_gqa: bool, dq, dk, dv, workspace, dropout_p: float, seed: int,
+                        offset: int = 0, dev_status=None, stream=None) -> None:
+    _want_all(((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"),
+               (dk, "dk"), (dv, "dv")), torch.bfloat16)
+    _want_all(((cu_seqlens, "cu_seqlens"), (row_ptr, "row_ptr")), torch.int32)
     _want(lse, torch.float32, "lse")
-    _check(lib().bd_attn_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo),
+    _check(lib().bd_attn_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                     _ptr(dout), B, Hq, Hkv, L, S, D, _ptr(cu_seqlens),
+                                     _ptr(row_ptr), seq_start, float(scale),
+                                     int(bool(enable_gqa)), _ptr(dq), _ptr(dk), _ptr(dv),
+                                     _ptr(workspace), _nbytes(workspace), float(dropout_p),
+                                     int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF,
+                                     _ptr(dev_status), _stream(stream)), "bd_attn_bwd_dropout")
+
+
+# ---- planned forms: a plan from bd_attn_plan, separate workspaces
+
+def bd_attn_fwd_planned_workspace_size(B: int, Hkv: int, S: int, D: int) -> int:
+    return int(lib().bd_attn_fwd_planned_workspace_size(B, Hkv, S, D))
+
+
+def bd_attn_fwd_planned(q, k, v, B: int, Hq: int, Hkv: int, L: int, S: int, D: int,
+                        seq_start: int, scale: float, enable_gqa: bool, plan, out, lse,
+                        out_lo=None, workspace=None, dev_status=None, stream=None) -> None:
+    _want_all(((q, "q"), (k, "k"), (v, "v"), (out, "out")), torch.bfloat16)
+    if out_lo is not None:
+        _want(out_lo, torch.bfloat16, "out_lo")
+    _want(lse, torch.float32, "lse")
+    _check(lib().bd_attn_fwd_planned(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, L, S, D, seq_start,
+                                     float(scale), int(bool(enable_gqa)), _ptr(plan),
+                                     _nbytes(plan), _ptr(out), _ptr(lse), _ptr(out_lo),
+                                     _ptr(workspace), _nbytes(workspace), _ptr(dev_status),
+                                     _stream(stream)), "bd_attn_fwd_planned")
+
+
+def bd_attn_fwd_dropout_planned(q, k, v, B: int, Hq: int, Hkv: int, L: int, S: int, D: int,
+                                seq_start: int, scale: float, enable_gqa: bool, plan, out, lse,
+                                dropout_p: float, seed: int, offset: int = 0, out_lo=None,
+                                workspace=None, dev_status=None, stream=None) -> None:
+    _want_all(((q, "q"), (k, "k"), (v, "v"), (out, "out")), torch.bfloat16)
+    if out_lo is not None:
+        _want(out_lo, torch.bfloat16, "out_lo")
+    _want(lse, torch.float32, "lse")
+    _check(lib().bd_attn_fwd_dropout_planned(
+        _ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, L, S, D, seq_start, float(scale),
+        int(bool(enable_gqa)), _ptr(plan), _nbytes(plan), _ptr(out), _ptr(lse), _ptr(out_lo),
+        _ptr(workspace), _nbytes(workspace), float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF,
+        int(offset) & 0xFFFFFFFF, _ptr(dev_status), _stream(stream)),
+        "bd_attn_fwd_dropout_planned")
+
+
+def bd_attn_bwd_planned_workspace_size(B: int, Hq: int, Hkv: int, L: int, S: int, D: int) -> int:
+    return int(lib().bd_attn_bwd_planned_workspace_size(B, Hq, Hkv, L, S, D))
+
+
+def bd_attn_bwd_planned(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: int,
+                        D: int, seq_start: int, scale: float, enable_gqa: bool, plan, dq, dk, dv,
+                        workspace, out_lo=None, dev_status=None, stream=None) -> None:
+    _want_all(((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"),
+               (dk, "dk"), (dv, "dv")), torch.bfloat16)
+    _want(lse, torch.float32, "lse")
+    _check(lib().bd_attn_bwd_planned(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo),
                                      _ptr(lse), _ptr(dout), B, Hq, Hkv, L, S, D, seq_start,
                                      float(scale), int(bool(enable_gqa)), _ptr(plan),
-                                     plan.numel() * plan.element_size(), _ptr(dq), _ptr(dk),
-                                     _ptr(dv), _ptr(workspace),
-                                     workspace.numel() * workspace.element_size(),
-                                     float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF,
-                                     int(offset) & 0xFFFFFFFF, _ptr(dev_status),
-                                     _stream(stream)), "bd_attn_bwd_dropout")
+                                     _nbytes(plan), _ptr(dq), _ptr(dk), _ptr(dv),
+                                     _ptr(workspace), _nbytes(workspace), _ptr(dev_status),
+                                     _stream(stream)), "bd_attn_bwd_planned")
 
 
-def bd_attn_bwd_stages(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: int,
-                       D: int, seq_start: int, scale: float, enable_gqa: bool, plan, dq, dk, dv,
-                       workspace, out_lo=None, dev_status=None, stages: int = 7,
-                       stream=None) -> None:
-    _check(lib().bd_attn_bwd_stages(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo),
-                                    _ptr(lse), _ptr(dout),
-                                    B, Hq, Hkv, L, S, D, seq_start, float(scale),
-                                    int(bool(enable_gqa)), _ptr(plan),
-                                    plan.numel() * plan.element_size(), _ptr(dq), _ptr(dk),
-                                    _ptr(dv), _ptr(workspace),
-                                    workspace.numel() * workspace.element_size(),
-                                    _ptr(dev_status), int(stages), _stream(stream)),
-           "bd_attn_bwd_stages")
+def bd_attn_bwd_dropout_planned(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int,
+                                S: int, D: int, seq_start: int, scale: float, enable_gqa: bool,
+                                plan, dq, dk, dv, workspace, dropout_p: float, seed: int,
+                                offset: int = 0, out_lo=None, dev_status=None,
+                                stream=None) -> None:
+    _want_all(((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"),
+               (dk, "dk"), (dv, "dv")), torch.bfloat16)
+    _want(lse, torch.float32, "lse")
+    _check(lib().bd_attn_bwd_dropout_planned(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo), _ptr(lse), _ptr(dout), B, Hq, Hkv,
+        L, S, D, seq_start, float(scale), int(bool(enable_gqa)), _ptr(plan), _nbytes(plan),
+        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), _nbytes(workspace), float(dropout_p),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF, _ptr(dev_status),
+        _stream(stream)), "bd_attn_bwd_dropout_planned")
 
 
 def bd_attn_bwd_noalloc(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: int,
                         D: int, seq_start: int, scale: float, enable_gqa: bool, plan, dq, dk, dv,
                         out_lo=None, dev_status=None, stream=None) -> None:
-    """bd_attn_bwd without a workspace argument: the library's own fixed scratch is used.
+    """bd_attn_bwd_planned without a workspace argument: the library's own fixed scratch is used.
 
     For callers that cannot allocate device memory.  Problems whose workspace
     exceeds NOALLOC_SCRATCH_BYTES raise ValueError; calls that overlap on the
@@ -303,9 +377,15 @@ def bd_attn_bwd_noalloc(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: i
     _check(lib().bd_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo),
                                      _ptr(lse), _ptr(dout), B, Hq, Hkv, L, S, D, seq_start,
                                      float(scale), int(bool(enable_gqa)), _ptr(plan),
-                                     plan.numel() * plan.element_size(), _ptr(dq), _ptr(dk),
+                                     _nbytes(plan), _ptr(dq), _ptr(dk),
                                      _ptr(dv), _ptr(dev_status), _stream(stream)),
            "bd_attn_bwd_noalloc")
+
+
+def bd_test_arm_wait_timeout(which: int, limit_us: int) -> None:
+    """Make the next launch of the forward (1) or backward main (2) kernel from this
+    thread withhold its first tile and give up its waits after limit_us (test hook)."""
+    _check(lib().bd_test_arm_wait_timeout(int(which), int(limit_us)), "bd_test_arm_wait_timeout")
 
 
 def bd_get_device_status(dev_status, stream=None) -> int:

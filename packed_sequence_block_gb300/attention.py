@@ -100,7 +100,7 @@ def attn_forward(q, k, v, plan, seq_start=0, scale=None, enable_gqa=False, resid
 
     The residual (bf16, same shape as out, or None when ``residual`` is
     False) lets the backward form Delta = <dout, O> from O at ~16 bits.
-    ``workspace`` (uint8, at least bd_attn_fwd_workspace_size bytes) is
+    ``workspace`` (uint8, at least bd_attn_fwd_planned_workspace_size bytes) is
     allocated here when not given.  ``dropout_p`` > 0 drops attention weights
     with the counter-based mask of (seed, offset); the backward must be given
     the same three values.
@@ -108,18 +108,20 @@ def attn_forward(q, k, v, plan, seq_start=0, scale=None, enable_gqa=False, resid
     B, Hq, L, D = q.shape
     Hkv, S = k.shape[1], k.shape[2]
     if workspace is None:
-        workspace = torch.empty(N.bd_attn_fwd_workspace_size(B, Hkv, S, D), dtype=torch.uint8,
-                                device=q.device)
+        workspace = torch.empty(N.bd_attn_fwd_planned_workspace_size(B, Hkv, S, D),
+                                dtype=torch.uint8, device=q.device)
     out = torch.empty_like(q)
     out_lo = torch.empty_like(q) if residual else None
     lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device)
     if dropout_p != 0.0:  # the library rejects p outside [0, 1)
-        N.bd_attn_fwd_dropout(q, k, v, B, Hq, Hkv, L, S, D, seq_start, _resolve_scale(scale, D),
-                              enable_gqa, plan, out, lse, dropout_p, seed, offset, out_lo,
-                              workspace, device_status_word(q.device))
+        N.bd_attn_fwd_dropout_planned(q, k, v, B, Hq, Hkv, L, S, D, seq_start,
+                                      _resolve_scale(scale, D), enable_gqa, plan, out, lse,
+                                      dropout_p, seed, offset, out_lo, workspace,
+                                      device_status_word(q.device))
     else:
-        N.bd_attn_fwd(q, k, v, B, Hq, Hkv, L, S, D, seq_start, _resolve_scale(scale, D),
-                      enable_gqa, plan, out, lse, out_lo, workspace, device_status_word(q.device))
+        N.bd_attn_fwd_planned(q, k, v, B, Hq, Hkv, L, S, D, seq_start, _resolve_scale(scale, D),
+                              enable_gqa, plan, out, lse, out_lo, workspace,
+                              device_status_word(q.device))
     return out, lse, out_lo
 
 
@@ -130,19 +132,74 @@ def attn_backward(q, k, v, out, lse, dout, plan, seq_start=0, scale=None, enable
     B, Hq, L, D = q.shape
     Hkv, S = k.shape[1], k.shape[2]
     if workspace is None:
-        workspace = torch.empty(N.bd_attn_bwd_workspace_size(B, Hq, Hkv, L, S, D),
+        workspace = torch.empty(N.bd_attn_bwd_planned_workspace_size(B, Hq, Hkv, L, S, D),
                                 dtype=torch.uint8, device=q.device)
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
     if dropout_p != 0.0:
-        N.bd_attn_bwd_dropout(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, seq_start,
-                              _resolve_scale(scale, D), enable_gqa, plan, dq, dk, dv, workspace,
-                              dropout_p, seed, offset, out_lo, device_status_word(q.device))
+        N.bd_attn_bwd_dropout_planned(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, seq_start,
+                                      _resolve_scale(scale, D), enable_gqa, plan, dq, dk, dv,
+                                      workspace, dropout_p, seed, offset, out_lo,
+                                      device_status_word(q.device))
     else:
-        N.bd_attn_bwd(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, seq_start,
-                      _resolve_scale(scale, D), enable_gqa, plan, dq, dk, dv, workspace, out_lo,
-                      device_status_word(q.device))
+        N.bd_attn_bwd_planned(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, seq_start,
+                              _resolve_scale(scale, D), enable_gqa, plan, dq, dk, dv, workspace,
+                              out_lo, device_status_word(q.device))
+    return dq, dk, dv
+
+
+def cu_csr(cu_seqlens, device):
+    """(flat boundaries, row_ptr) int32 device tensors for one row's boundaries or a list of
+    rows, the layout bd_attn_fwd / bd_attn_bwd take."""
+    flat, rp, _ = _csr(cu_seqlens, device)
+    return flat, rp
+
+
+def attn_forward_cu(q, k, v, cu_seqlens, row_ptr, seq_start=0, scale=None, enable_gqa=False,
+                    workspace=None, dropout_p: float = 0.0, seed: int = 0, offset: int = 0):
+    """out, lse and the workspace of the single-call forward (bd_attn_fwd, no autograd).
+
+    ``cu_seqlens`` / ``row_ptr`` are the int32 device tensors of ``cu_csr``.  The
+    workspace (bd_attn_workspace_size bytes, allocated here when not given)
+    carries the plan and the rounding residual of out to ``attn_backward_cu``.
+    """
+    B, Hq, L, D = q.shape
+    Hkv, S = k.shape[1], k.shape[2]
+    if workspace is None:
+        workspace = torch.empty(N.bd_attn_workspace_size(B, Hq, Hkv, L, S, D), dtype=torch.uint8,
+                                device=q.device)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device)
+    st = device_status_word(q.device)
+    if dropout_p != 0.0:
+        N.bd_attn_fwd_dropout(q, k, v, B, Hq, Hkv, L, S, D, cu_seqlens, row_ptr, seq_start,
+                              _resolve_scale(scale, D), enable_gqa, out, lse, workspace,
+                              dropout_p, seed, offset, st)
+    else:
+        N.bd_attn_fwd(q, k, v, B, Hq, Hkv, L, S, D, cu_seqlens, row_ptr, seq_start,
+                      _resolve_scale(scale, D), enable_gqa, out, lse, workspace, st)
+    return out, lse, workspace
+
+
+def attn_backward_cu(q, k, v, out, lse, dout, cu_seqlens, row_ptr, workspace, seq_start=0,
+                     scale=None, enable_gqa=False, dropout_p: float = 0.0, seed: int = 0,
+                     offset: int = 0):
+    """dq, dk, dv of the single-call backward (bd_attn_bwd, no autograd), on the
+    workspace the forward used."""
+    B, Hq, L, D = q.shape
+    Hkv, S = k.shape[1], k.shape[2]
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    st = device_status_word(q.device)
+    if dropout_p != 0.0:
+        N.bd_attn_bwd_dropout(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, cu_seqlens, row_ptr,
+                              seq_start, _resolve_scale(scale, D), enable_gqa, dq, dk, dv,
+                              workspace, dropout_p, seed, offset, st)
+    else:
+        N.bd_attn_bwd(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, cu_seqlens, row_ptr,
+                      seq_start, _resolve_scale(scale, D), enable_gqa, dq, dk, dv, workspace, st)
     return dq, dk, dv
 
 
@@ -245,7 +302,8 @@ def useful_pairs(cu_rows, seq_start: int, L: int) -> int:
 
 
 __all__ = [
-    "BlockdiagAttention", "attn_backward", "attn_forward", "blockdiag_attention",
+    "BlockdiagAttention", "attn_backward", "attn_backward_cu", "attn_forward", "attn_forward_cu",
+    "blockdiag_attention", "cu_csr",
     "check_device_status", "cp_blockdiag_sdpa", "device_status_word", "doc_ids_from_cu_seqlens",
     "make_plan", "segment_cu_seqlens", "useful_pairs",
 ]

@@ -16,8 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT = os.path.join(HERE, "libbd_attn.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["bd_abi.cu", "bd_index.cu", "bd_layout.cu", "bd_plan.cu", "bd_fwd.cu", "bd_bwd.cu",
-           "bd_noalloc.cu"]
+SOURCES = ["bd_abi.cu", "bd_index.cu", "bd_layout.cu", "bd_plan.cu", "bd_prep.cu", "bd_fwd.cu",
+           "bd_bwd.cu", "bd_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

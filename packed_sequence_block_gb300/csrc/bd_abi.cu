@@ -111,6 +111,21 @@ static bool make_tmap_16bit(CUtensorMap* map, const void* base, int planes, int 
   return r == CUDA_SUCCESS;
 }
 
+namespace {
+// One-shot wait-test requests of this host thread, per kernel (index 1: forward,
+// 2: backward main); 0 means none.
+thread_local uint32_t t_wait_test_ns[3] = {0, 0, 0};
+}  // namespace
+
+void arm_wait_test(int which, uint32_t limit_ns) { t_wait_test_ns[which] = limit_ns; }
+
+uint32_t take_wait_test(int which, int* withhold) {
+  const uint32_t t = t_wait_test_ns[which];
+  t_wait_test_ns[which] = 0;
+  *withhold = t != 0;
+  return t != 0 ? t : static_cast<uint32_t>(kWaitTimeoutNs);
+}
+
 bool make_tmap_dqacc(CUtensorMap* map, void* base, int planes, int rows, int D) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
   if (enc == nullptr) return false;
@@ -167,7 +182,7 @@ const char* bd_status_string(int status) {
   }
 }
 
-int bd_version(void) { return 100; }
+int bd_version(void) { return 200; }
 
 int bd_doc_ids_from_cu_seqlens(const int32_t* cu, const int32_t* row_ptr, int B, int S,
                                int32_t* doc_ids, int32_t* dev_status, bd_stream_t stream) {
@@ -256,9 +271,14 @@ int bd_attn_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg
              : BD_ERR_CUDA;
 }
 
-size_t bd_attn_fwd_workspace_size(int B, int Hkv, int S, int D) {
+size_t bd_attn_fwd_planned_workspace_size(int B, int Hkv, int S, int D) {
   if (B < 1 || Hkv < 1 || S < 1 || D < 1) return 0;
   return align256(2 * (size_t)B * Hkv * S * D);
+}
+
+size_t bd_attn_workspace_size(int B, int Hq, int Hkv, int L, int S, int D) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || S < 1 || D < 1) return 0;
+  return ws_layout(B, Hq, Hkv, L, S, D).total;
 }
 
 }  // extern "C"
@@ -266,77 +286,186 @@ size_t bd_attn_fwd_workspace_size(int B, int Hkv, int S, int D) {
 namespace bd {
 namespace {
 
-int fwd_impl(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L, int S,
-             int D, int seq_start, float scale, int enable_gqa, void* plan, size_t plan_bytes,
-             void* out, float* lse, void* out_lo, void* workspace, size_t workspace_bytes,
-             const DropoutArgs& drop, int32_t* dev_status, cudaStream_t stream) {
-  if (q == nullptr || k == nullptr || v == nullptr || plan == nullptr || out == nullptr ||
-      lse == nullptr || workspace == nullptr)
-    return BD_ERR_INVALID_ARG;
-  if (out_lo != nullptr && !aligned(out_lo, 16)) return BD_ERR_INVALID_ARG;
+// Argument checks shared by every attention entry point.
+int check_attn_args(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L,
+                    int S, int D, int seq_start, int enable_gqa) {
+  if (q == nullptr || k == nullptr || v == nullptr) return BD_ERR_INVALID_ARG;
   int st = check_dims(B, Hq, Hkv, L, S, D, seq_start, enable_gqa);
   if (st != BD_OK) return st;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
-      !aligned(lse, 4) || !aligned(plan, 256) || !aligned(workspace, 256))
-    return BD_ERR_INVALID_ARG;
-  st = check_plan_lists(B, Hq, Hkv, L, S);
-  if (st != BD_OK) return st;
-  if (plan_bytes < plan_layout(B, Hq, Hkv, L, S).total) return BD_ERR_WORKSPACE;
-  if (workspace_bytes < bd_attn_fwd_workspace_size(B, Hkv, S, D)) return BD_ERR_WORKSPACE;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return BD_ERR_INVALID_ARG;
+  return check_plan_lists(B, Hq, Hkv, L, S);
+}
+
+// The forward kernel on a built plan, v16 holding (or about to hold) the fp16 copy of v.
+int fwd_run(const void* q, const void* k, int B, int Hq, int Hkv, int L, int S, int D,
+            int seq_start, float scale, void* plan, void* v16, void* out, float* lse,
+            void* out_lo, const DropoutArgs& drop, int32_t* dev_status, int sms,
+            cudaStream_t stream, void* acc = nullptr, size_t acc_bytes = 0,
+            uint32_t* acc_flags = nullptr) {
   AttnDims d = resolve(B, Hq, Hkv, L, S, D, seq_start, scale);
   d.drop = drop;
-  // the P V product reads v through its fp16 copy in the workspace
   CUtensorMap tq, tk, tv, to, tol;
   if (!make_tmap_out(&to, out, B * Hq, L, D) ||
       !make_tmap_out(&tol, out_lo != nullptr ? out_lo : out, B * Hq, L, D))
     return BD_ERR_CUDA;
   if (!make_tmap_bf16(&tq, q, B * Hq, L, D) || !make_tmap_bf16(&tk, k, B * Hkv, S, D) ||
-      !make_tmap_f16(&tv, workspace, B * Hkv, S, D))
+      !make_tmap_f16(&tv, v16, B * Hkv, S, D))
     return BD_ERR_CUDA;
-  const int sms = num_sms_current();
-  if (sms <= 0) return BD_ERR_CUDA;
-  return launch_fwd(tq, tk, tv, to, tol, d, plan, v, workspace, out, out_lo, lse, dev_status, sms,
-                    stream) == cudaSuccess
+  return launch_fwd(tq, tk, tv, to, tol, d, plan, out, out_lo, lse, dev_status, sms, stream, acc,
+                    acc_bytes, acc_flags) == cudaSuccess
              ? BD_OK
              : BD_ERR_CUDA;
 }
 
-int bwd_impl(const void* q, const void* k, const void* v, const void* out, const void* out_lo,
-             const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S, int D,
-             int seq_start, float scale, int enable_gqa, void* plan, size_t plan_bytes, void* dq,
-             void* dk, void* dv, void* workspace, size_t workspace_bytes, const DropoutArgs& drop,
-             int32_t* dev_status, int stages, cudaStream_t stream) {
-  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || lse == nullptr ||
-      dout == nullptr || plan == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
+int fwd_planned_impl(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L,
+                     int S, int D, int seq_start, float scale, int enable_gqa, void* plan,
+                     size_t plan_bytes, void* out, float* lse, void* out_lo, void* workspace,
+                     size_t workspace_bytes, const DropoutArgs& drop, int32_t* dev_status,
+                     cudaStream_t stream) {
+  if (plan == nullptr || out == nullptr || lse == nullptr || workspace == nullptr)
+    return BD_ERR_INVALID_ARG;
+  if (out_lo != nullptr && !aligned(out_lo, 16)) return BD_ERR_INVALID_ARG;
+  int st = check_attn_args(q, k, v, B, Hq, Hkv, L, S, D, seq_start, enable_gqa);
+  if (st != BD_OK) return st;
+  if (!aligned(out, 16) || !aligned(lse, 4) || !aligned(plan, 256) || !aligned(workspace, 256))
+    return BD_ERR_INVALID_ARG;
+  if (plan_bytes < plan_layout(B, Hq, Hkv, L, S).total) return BD_ERR_WORKSPACE;
+  if (workspace_bytes < bd_attn_fwd_planned_workspace_size(B, Hkv, S, D)) return BD_ERR_WORKSPACE;
+  const int sms = num_sms_current();
+  if (sms <= 0) return BD_ERR_CUDA;
+  // the P V product reads v through its fp16 copy in the workspace
+  if (launch_v_to_f16(v, workspace, (long long)B * Hkv * S * D, sms, stream) != cudaSuccess)
+    return BD_ERR_CUDA;
+  return fwd_run(q, k, B, Hq, Hkv, L, S, D, seq_start, scale, plan, workspace, out, lse, out_lo,
+                 drop, dev_status, sms, stream);
+}
+
+WsTag ws_tag(int B, int Hq, int Hkv, int L, int S, int D, int seq_start, const void* out,
+             const float* lse, const int32_t* cu, const int32_t* row_ptr) {
+  WsTag t{};
+  t.cu = reinterpret_cast<uintptr_t>(cu);
+  t.row_ptr = reinterpret_cast<uintptr_t>(row_ptr);
+  t.flags = 0;
+  t.magic = kWsMagic;
+  t.B = B;
+  t.Hq = Hq;
+  t.Hkv = Hkv;
+  t.L = L;
+  t.S = S;
+  t.D = D;
+  t.seq_start = seq_start;
+  t.out = reinterpret_cast<uintptr_t>(out);
+  t.lse = reinterpret_cast<uintptr_t>(lse);
+  return t;
+}
+
+int fwd_cu_impl(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L,
+                int S, int D, const int32_t* cu, const int32_t* row_ptr, int seq_start,
+                float scale, int enable_gqa, void* out, float* lse, void* workspace,
+                size_t workspace_bytes, const DropoutArgs& drop, int32_t* dev_status,
+                cudaStream_t stream) {
+  if (cu == nullptr || row_ptr == nullptr || out == nullptr || lse == nullptr ||
       workspace == nullptr)
     return BD_ERR_INVALID_ARG;
-  if (stages <= 0 || stages > (kBwdPrepare | kBwdMain | kBwdFinish)) return BD_ERR_INVALID_ARG;
-  if (out_lo != nullptr && !aligned(out_lo, 16)) return BD_ERR_INVALID_ARG;
-  int st = check_dims(B, Hq, Hkv, L, S, D, seq_start, enable_gqa);
+  int st = check_attn_args(q, k, v, B, Hq, Hkv, L, S, D, seq_start, enable_gqa);
   if (st != BD_OK) return st;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
-      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
-      !aligned(lse, 4) || !aligned(plan, 256) || !aligned(workspace, 256))
-    return BD_ERR_INVALID_ARG;
-  st = check_plan_lists(B, Hq, Hkv, L, S);
-  if (st != BD_OK) return st;
-  if (plan_bytes < plan_layout(B, Hq, Hkv, L, S).total) return BD_ERR_WORKSPACE;
-  const BwdLayout wl = bwd_layout(B, Hq, Hkv, L, S, D);
+  if (!aligned(out, 16) || !aligned(lse, 4) || !aligned(workspace, 256)) return BD_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(B, Hq, Hkv, L, S, D);
   if (workspace_bytes < wl.total) return BD_ERR_WORKSPACE;
+  const int sms = num_sms_current();
+  if (sms <= 0) return BD_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  const PlanPtrs pp = plan_ptrs(ws + wl.plan_off, B, Hq, Hkv, L, S, seq_start);
+  WsTag* hdr = reinterpret_cast<WsTag*>(ws + wl.hdr);
+  if (launch_prep_fwd(cu, row_ptr, pp, ws_tag(B, Hq, Hkv, L, S, D, seq_start, out, lse, cu, row_ptr),
+                      hdr, v, ws + wl.v16, (long long)B * Hkv * S * D, dev_status, sms,
+                      stream) != cudaSuccess)
+    return BD_ERR_CUDA;
+  // the forward's idle warps zero the backward's dq accumulator in the same workspace
+  return fwd_run(q, k, B, Hq, Hkv, L, S, D, seq_start, scale, ws + wl.plan_off, ws + wl.v16, out,
+                 lse, ws + wl.out_lo, drop, dev_status, sms, stream,
+                 ws + wl.bwd_off + wl.bwd.dqacc, sizeof(float) * (size_t)B * Hq * L * D,
+                 &hdr->flags);
+}
+
+// The backward stages on a plan; `prep` set for the single-call form.
+int bwd_run(const void* q, const void* k, const void* v, const void* out, const void* out_lo,
+            const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S, int D,
+            int seq_start, float scale, void* plan, void* dq, void* dk, void* dv, void* bwd_ws,
+            const DropoutArgs& drop, int32_t* dev_status, int stages, const BwdPrep* prep,
+            cudaStream_t stream) {
   AttnDims d = resolve(B, Hq, Hkv, L, S, D, seq_start, scale);
   d.drop = drop;
+  const BwdLayout wl = bwd_layout(B, Hq, Hkv, L, S, D);
   CUtensorMap tq, tk, tv, tdo, tdq;
-  char* ws = static_cast<char*>(workspace);
+  char* ws = static_cast<char*>(bwd_ws);
   if (!make_tmap_bf16(&tq, q, B * Hq, L, D) || !make_tmap_bf16(&tk, k, B * Hkv, S, D) ||
       !make_tmap_bf16(&tv, v, B * Hkv, S, D) || !make_tmap_bf16(&tdo, dout, B * Hq, L, D) ||
       !make_tmap_dqacc(&tdq, ws + wl.dqacc, B * Hq, L, D))
     return BD_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return BD_ERR_CUDA;
-  return launch_bwd(tq, tk, tv, tdo, tdq, d, plan, out, out_lo, lse, dout, dq, dk, dv, workspace,
-                    dev_status, stages, sms, stream) == cudaSuccess
+  return launch_bwd(tq, tk, tv, tdo, tdq, d, plan, out, out_lo, lse, dout, dq, dk, dv, bwd_ws,
+                    dev_status, stages, sms, stream, prep) == cudaSuccess
              ? BD_OK
              : BD_ERR_CUDA;
+}
+
+int check_bwd_ptrs(const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                   void* dv, void* workspace) {
+  if (out == nullptr || lse == nullptr || dout == nullptr || dq == nullptr || dk == nullptr ||
+      dv == nullptr || workspace == nullptr)
+    return BD_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) ||
+      !aligned(dv, 16) || !aligned(lse, 4) || !aligned(workspace, 256))
+    return BD_ERR_INVALID_ARG;
+  return BD_OK;
+}
+
+int bwd_planned_impl(const void* q, const void* k, const void* v, const void* out,
+                     const void* out_lo, const float* lse, const void* dout, int B, int Hq,
+                     int Hkv, int L, int S, int D, int seq_start, float scale, int enable_gqa,
+                     void* plan, size_t plan_bytes, void* dq, void* dk, void* dv,
+                     void* workspace, size_t workspace_bytes, const DropoutArgs& drop,
+                     int32_t* dev_status, cudaStream_t stream) {
+  if (plan == nullptr) return BD_ERR_INVALID_ARG;
+  if (out_lo != nullptr && !aligned(out_lo, 16)) return BD_ERR_INVALID_ARG;
+  int st = check_attn_args(q, k, v, B, Hq, Hkv, L, S, D, seq_start, enable_gqa);
+  if (st != BD_OK) return st;
+  st = check_bwd_ptrs(out, lse, dout, dq, dk, dv, workspace);
+  if (st != BD_OK) return st;
+  if (!aligned(plan, 256)) return BD_ERR_INVALID_ARG;
+  if (plan_bytes < plan_layout(B, Hq, Hkv, L, S).total) return BD_ERR_WORKSPACE;
+  if (workspace_bytes < bwd_layout(B, Hq, Hkv, L, S, D).total) return BD_ERR_WORKSPACE;
+  return bwd_run(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale, plan, dq,
+                 dk, dv, workspace, drop, dev_status, kBwdPrepare | kBwdMain | kBwdFinish,
+                 nullptr, stream);
+}
+
+int bwd_cu_impl(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                const void* dout, int B, int Hq, int Hkv, int L, int S, int D,
+                const int32_t* cu, const int32_t* row_ptr, int seq_start, float scale,
+                int enable_gqa, void* dq, void* dk, void* dv, void* workspace,
+                size_t workspace_bytes, const DropoutArgs& drop, int32_t* dev_status, int stages,
+                cudaStream_t stream) {
+  if (cu == nullptr || row_ptr == nullptr) return BD_ERR_INVALID_ARG;
+  if (stages <= 0 || stages > (kBwdPrepare | kBwdMain | kBwdFinish)) return BD_ERR_INVALID_ARG;
+  int st = check_attn_args(q, k, v, B, Hq, Hkv, L, S, D, seq_start, enable_gqa);
+  if (st != BD_OK) return st;
+  st = check_bwd_ptrs(out, lse, dout, dq, dk, dv, workspace);
+  if (st != BD_OK) return st;
+  const WsLayout wl = ws_layout(B, Hq, Hkv, L, S, D);
+  if (workspace_bytes < wl.total) return BD_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  BwdPrep prep{};
+  prep.cu = cu;
+  prep.row_ptr = row_ptr;
+  prep.pp = plan_ptrs(ws + wl.plan_off, B, Hq, Hkv, L, S, seq_start);
+  prep.hdr = reinterpret_cast<WsTag*>(ws + wl.hdr);
+  prep.expect = ws_tag(B, Hq, Hkv, L, S, D, seq_start, out, lse, cu, row_ptr);
+  return bwd_run(q, k, v, out, ws + wl.out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
+                 ws + wl.plan_off, dq, dk, dv, ws + wl.bwd_off, drop, dev_status, stages, &prep,
+                 stream);
 }
 
 }  // namespace
@@ -345,66 +474,121 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
 extern "C" {
 
 int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L, int S,
-                int D, int seq_start, float scale, int enable_gqa, void* plan,
-                size_t plan_bytes, void* out, float* lse, void* out_lo, void* workspace,
+                int D, const int32_t* cu_seqlens, const int32_t* row_ptr, int seq_start,
+                float scale, int enable_gqa, void* out, float* lse, void* workspace,
                 size_t workspace_bytes, int32_t* dev_status, bd_stream_t stream) {
-  return fwd_impl(q, k, v, B, Hq, Hkv, L, S, D, seq_start, scale, enable_gqa, plan, plan_bytes,
-                  out, lse, out_lo, workspace, workspace_bytes, DropoutArgs{}, dev_status, stream);
+  return fwd_cu_impl(q, k, v, B, Hq, Hkv, L, S, D, cu_seqlens, row_ptr, seq_start, scale,
+                     enable_gqa, out, lse, workspace, workspace_bytes, DropoutArgs{}, dev_status,
+                     stream);
 }
 
-int bd_attn_fwd_dropout(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
-                        int L, int S, int D, int seq_start, float scale, int enable_gqa,
-                        void* plan, size_t plan_bytes, void* out, float* lse, void* out_lo,
-                        void* workspace, size_t workspace_bytes, double dropout_p,
-                        uint64_t seed, uint32_t offset, int32_t* dev_status,
-                        bd_stream_t stream) {
-  DropoutArgs drop;
-  const int st = make_dropout(dropout_p, seed, offset, &drop);
-  if (st != BD_OK) return st;
-  return fwd_impl(q, k, v, B, Hq, Hkv, L, S, D, seq_start, scale, enable_gqa, plan, plan_bytes,
-                  out, lse, out_lo, workspace, workspace_bytes, drop, dev_status, stream);
-}
-
-size_t bd_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int S, int D) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || S < 1 || D < 1) return 0;
-  return bwd_layout(B, Hq, Hkv, L, S, D).total;
+int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                const void* dout, int B, int Hq, int Hkv, int L, int S, int D,
+                const int32_t* cu_seqlens, const int32_t* row_ptr, int seq_start, float scale,
+                int enable_gqa, void* dq, void* dk, void* dv, void* workspace,
+                size_t workspace_bytes, int32_t* dev_status, bd_stream_t stream) {
+  return bwd_cu_impl(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, cu_seqlens, row_ptr,
+                     seq_start, scale, enable_gqa, dq, dk, dv, workspace, workspace_bytes,
+                     DropoutArgs{}, dev_status, kBwdPrepare | kBwdMain | kBwdFinish, stream);
 }
 
 int bd_attn_bwd_stages(const void* q, const void* k, const void* v, const void* out,
-                       const void* out_lo, const float* lse, const void* dout, int B, int Hq,
-                       int Hkv, int L, int S,
-                       int D, int seq_start, float scale, int enable_gqa, void* plan,
-                       size_t plan_bytes, void* dq, void* dk, void* dv, void* workspace,
-                       size_t workspace_bytes, int32_t* dev_status, int stages,
+                       const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S,
+                       int D, const int32_t* cu_seqlens, const int32_t* row_ptr, int seq_start,
+                       float scale, int enable_gqa, void* dq, void* dk, void* dv,
+                       void* workspace, size_t workspace_bytes, int32_t* dev_status, int stages,
                        bd_stream_t stream) {
-  return bwd_impl(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
-                  enable_gqa, plan, plan_bytes, dq, dk, dv, workspace, workspace_bytes,
-                  DropoutArgs{}, dev_status, stages, stream);
+  return bwd_cu_impl(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, cu_seqlens, row_ptr,
+                     seq_start, scale, enable_gqa, dq, dk, dv, workspace, workspace_bytes,
+                     DropoutArgs{}, dev_status, stages, stream);
 }
 
-int bd_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* out_lo,
-                const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S, int D,
-                int seq_start,
-                float scale, int enable_gqa, void* plan, size_t plan_bytes, void* dq,
-                void* dk, void* dv, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                bd_stream_t stream) {
-  return bd_attn_bwd_stages(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
-                            enable_gqa, plan, plan_bytes, dq, dk, dv, workspace, workspace_bytes,
-                            dev_status, kBwdPrepare | kBwdMain | kBwdFinish, stream);
-}
-
-int bd_attn_bwd_dropout(const void* q, const void* k, const void* v, const void* out,
-                        const void* out_lo, const float* lse, const void* dout, int B, int Hq,
-                        int Hkv, int L, int S, int D, int seq_start, float scale, int enable_gqa,
-                        void* plan, size_t plan_bytes, void* dq, void* dk, void* dv,
+int bd_attn_fwd_dropout(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
+                        int L, int S, int D, const int32_t* cu_seqlens, const int32_t* row_ptr,
+                        int seq_start, float scale, int enable_gqa, void* out, float* lse,
                         void* workspace, size_t workspace_bytes, double dropout_p, uint64_t seed,
                         uint32_t offset, int32_t* dev_status, bd_stream_t stream) {
   DropoutArgs drop;
   const int st = make_dropout(dropout_p, seed, offset, &drop);
   if (st != BD_OK) return st;
-  return bwd_impl(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
-                  enable_gqa, plan, plan_bytes, dq, dk, dv, workspace, workspace_bytes, drop,
-                  dev_status, kBwdPrepare | kBwdMain | kBwdFinish, stream);
+  return fwd_cu_impl(q, k, v, B, Hq, Hkv, L, S, D, cu_seqlens, row_ptr, seq_start, scale,
+                     enable_gqa, out, lse, workspace, workspace_bytes, drop, dev_status, stream);
+}
+
+int bd_attn_bwd_dropout(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S,
+                        int D, const int32_t* cu_seqlens, const int32_t* row_ptr, int seq_start,
+                        float scale, int enable_gqa, void* dq, void* dk, void* dv,
+                        void* workspace, size_t workspace_bytes, double dropout_p, uint64_t seed,
+                        uint32_t offset, int32_t* dev_status, bd_stream_t stream) {
+  DropoutArgs drop;
+  const int st = make_dropout(dropout_p, seed, offset, &drop);
+  if (st != BD_OK) return st;
+  return bwd_cu_impl(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, cu_seqlens, row_ptr,
+                     seq_start, scale, enable_gqa, dq, dk, dv, workspace, workspace_bytes, drop,
+                     dev_status, kBwdPrepare | kBwdMain | kBwdFinish, stream);
+}
+
+int bd_attn_fwd_planned(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
+                        int L, int S, int D, int seq_start, float scale, int enable_gqa,
+                        void* plan, size_t plan_bytes, void* out, float* lse, void* out_lo,
+                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        bd_stream_t stream) {
+  return fwd_planned_impl(q, k, v, B, Hq, Hkv, L, S, D, seq_start, scale, enable_gqa, plan,
+                          plan_bytes, out, lse, out_lo, workspace, workspace_bytes,
+                          DropoutArgs{}, dev_status, stream);
+}
+
+int bd_attn_fwd_dropout_planned(const void* q, const void* k, const void* v, int B, int Hq,
+                                int Hkv, int L, int S, int D, int seq_start, float scale,
+                                int enable_gqa, void* plan, size_t plan_bytes, void* out,
+                                float* lse, void* out_lo, void* workspace, size_t workspace_bytes,
+                                double dropout_p, uint64_t seed, uint32_t offset,
+                                int32_t* dev_status, bd_stream_t stream) {
+  DropoutArgs drop;
+  const int st = make_dropout(dropout_p, seed, offset, &drop);
+  if (st != BD_OK) return st;
+  return fwd_planned_impl(q, k, v, B, Hq, Hkv, L, S, D, seq_start, scale, enable_gqa, plan,
+                          plan_bytes, out, lse, out_lo, workspace, workspace_bytes, drop,
+                          dev_status, stream);
+}
+
+size_t bd_attn_bwd_planned_workspace_size(int B, int Hq, int Hkv, int L, int S, int D) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || S < 1 || D < 1) return 0;
+  return bwd_layout(B, Hq, Hkv, L, S, D).total;
+}
+
+int bd_attn_bwd_planned(const void* q, const void* k, const void* v, const void* out,
+                        const void* out_lo, const float* lse, const void* dout, int B, int Hq,
+                        int Hkv, int L, int S, int D, int seq_start, float scale, int enable_gqa,
+                        void* plan, size_t plan_bytes, void* dq, void* dk, void* dv,
+                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        bd_stream_t stream) {
+  return bwd_planned_impl(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
+                          enable_gqa, plan, plan_bytes, dq, dk, dv, workspace, workspace_bytes,
+                          DropoutArgs{}, dev_status, stream);
+}
+
+int bd_attn_bwd_dropout_planned(const void* q, const void* k, const void* v, const void* out,
+                                const void* out_lo, const float* lse, const void* dout, int B,
+                                int Hq, int Hkv, int L, int S, int D, int seq_start, float scale,
+                                int enable_gqa, void* plan, size_t plan_bytes, void* dq,
+                                void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                                double dropout_p, uint64_t seed, uint32_t offset,
+                                int32_t* dev_status, bd_stream_t stream) {
+  DropoutArgs drop;
+  const int st = make_dropout(dropout_p, seed, offset, &drop);
+  if (st != BD_OK) return st;
+  return bwd_planned_impl(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
+                          enable_gqa, plan, plan_bytes, dq, dk, dv, workspace, workspace_bytes,
+                          drop, dev_status, stream);
+}
+
+int bd_test_arm_wait_timeout(int which, unsigned int limit_us) {
+  if ((which != kWaitTestFwd && which != kWaitTestBwd) || limit_us < 1 || limit_us > 2000000u)
+    return BD_ERR_INVALID_ARG;
+  arm_wait_test(which, limit_us * 1000u);
+  return BD_OK;
 }
 
 int bd_get_device_status(const int32_t* dev_status, int32_t* host_status, bd_stream_t stream) {

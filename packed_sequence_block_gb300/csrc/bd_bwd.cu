@@ -17,7 +17,7 @@
 //             and adds it into the fp32 accumulator with TMA reductions;
 //             dK, dV leave once per unit.
 //  bwd_dq     dq = bf16(scale * accumulator)
-#include "bd_ptx.cuh"
+#include "bd_pre_dev.cuh"
 
 namespace bd {
 
@@ -26,7 +26,6 @@ namespace {
 // 20 warps: producer, MMA, dQ reduction issuer, one idle warp, two P/dS
 // warpgroups and two dQ reader warpgroups (64 columns of dQ each).
 constexpr int kThreads = 640;
-constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdCfg {
@@ -66,6 +65,10 @@ struct BwdParams {
   __nv_bfloat16* dv;
   int32_t* status;
   int* ctr;  // work counters in the plan: [next unit, finished CTAs]
+  int* aborts;  // CTAs of the launch that gave up a wait (in the plan)
+  uint32_t* acc_flags;  // optional: kAccZeroed is cleared (the accumulator now holds sums)
+  uint32_t wait_limit_ns;  // bound of every device-side wait
+  int withhold;            // test only: the producer withholds the first K/V load
   DropoutArgs drop;
 };
 
@@ -162,56 +165,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // ------------------------------------------------------------------ preprocess
 
 // One thread per 8 elements of a query row: -Delta, -lse in log2 units and the
-// zeroed dq accumulator.
+// zeroed dq accumulator (bwd_pre_rows in bd_pre_dev.cuh).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(
     const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ out_lo,
     const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse, int planes, int L,
     int Lq, float* __restrict__ nlse2o, float* __restrict__ ndeltao, float* __restrict__ dqacc) {
-  constexpr int TPR = D / 8;  // threads per row (a power of two dividing 32)
-  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (tid >= (long long)planes * Lq * TPR) return;  // a multiple of 32: whole warps leave
-  const long long rowg = tid / TPR;
-  const int part = static_cast<int>(tid % TPR);
-  const int plane = static_cast<int>(rowg / Lq);
-  const int i = static_cast<int>(rowg % Lq);
-  float acc = 0.f;
-  if (i < L) {
-    const size_t off = ((size_t)plane * L + i) * D + part * 8;
-    const uint4 o4 = *reinterpret_cast<const uint4*>(out + off);
-    const uint4 d4 = *reinterpret_cast<const uint4*>(dout + off);
-    const uint4 l4 = out_lo != nullptr ? *reinterpret_cast<const uint4*>(out_lo + off)
-                                       : make_uint4(0, 0, 0, 0);
-    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o4);
-    const __nv_bfloat162* l2v = reinterpret_cast<const __nv_bfloat162*>(&l4);
-    const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&d4);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 a = __bfloat1622float2(o2[j]);
-      const float2 r = __bfloat1622float2(l2v[j]);
-      const float2 b = __bfloat1622float2(d2[j]);
-      acc = fmaf(a.x + r.x, b.x, acc);
-      acc = fmaf(a.y + r.y, b.y, acc);
-    }
-    float4* z = reinterpret_cast<float4*>(dqacc + off);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  // every lane of the warp takes part in the shuffles (rows past L add 0)
-#pragma unroll
-  for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, TPR);
-  if (part == 0) {
-    float nl2 = -INFINITY, ndl = 0.f;
-    if (i < L) {
-      const float x = lse[(size_t)plane * L + i];
-      if (x != -INFINITY) {
-        nl2 = -(x * kLog2e);
-        ndl = -acc;
-      }
-    }
-    nlse2o[(size_t)plane * Lq + i] = nl2;
-    ndeltao[(size_t)plane * Lq + i] = ndl;
-  }
+  bwd_pre_rows<D>((long long)blockIdx.x * blockDim.x + threadIdx.x, out, out_lo, dout, lse,
+                  planes, L, Lq, nlse2o, ndeltao, dqacc);
 }
 
 template <int D>
@@ -282,15 +243,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* do_full = bars + 20;   // dO_i landed
   uint64_t* do_empty = bars + 21;  // dV_i done: the dO buffer may be refilled
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 22);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  WorkRing* ring = reinterpret_cast<WorkRing*>(bars + 23);
-  static_assert(23 * 8 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);  // + the wait limit
+  WorkRing* ring = reinterpret_cast<WorkRing*>(bars + 24);
+  static_assert(24 * 8 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
   static_assert(C::SMEM <= 232448, "shared memory over the per-block limit");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    *abort_flag = 0;
+    abort_flag[0] = 0;
+    abort_flag[1] = static_cast<int>(p.wait_limit_ns);
     if ((smem_u32(smem) & 1023u) != 0) {
       set_status(p.status, BD_ERR_CUDA);
       *abort_flag = 1;
@@ -340,6 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ring_publish(ring, kq++, p.ctr, p.n_units, abort_flag, p.status, w) || w < 0) break;
         const BUnit u = decode_bunit(p, w);
         if (u.n_it <= 0) continue;
+        // test of the bounded waits: the unit is published but its K/V never
+        // arrive, so the MMA thread's wait for them runs out
+        if (p.withhold) break;
         if (!mbar_wait(kv_empty, (kv_u & 1) ^ 1, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
         const int kvplane = u.b * p.Hkv + u.g;
@@ -818,7 +783,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  if (threadIdx.x == 0) ring_retire(p.ctr);
+  if (threadIdx.x == 0) {
+    if (ring_retire(p.ctr, p.aborts, *abort_flag != 0) != 0 && p.acc_flags != nullptr)
+      atomicAnd(p.acc_flags, ~kAccZeroed);
+  }
 }
 
 template <int D, bool kDrop>
@@ -829,7 +797,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const void* out, const void* out_lo, const float* lse,
                                 const void* dout, void* dq, int stages,
                                 int num_sms,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, const BwdPrep* prep) {
   using C = BwdCfg<D>;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -841,7 +809,12 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
     attr_set[dev] = true;
   }
   const int planes = p.B * p.Hq;
-  if (stages & kBwdPrepare) {
+  if ((stages & kBwdPrepare) && prep != nullptr) {
+    cudaError_t e = launch_prep_bwd(*prep, out, out_lo, dout, lse, D, planes, p.L, p.Lq,
+                                    const_cast<float*>(p.nlse2), const_cast<float*>(p.ndelta),
+                                    p.dqacc, p.status, stream);
+    if (e != cudaSuccess) return e;
+  } else if (stages & kBwdPrepare) {
     const long long threads = (long long)planes * p.Lq * (D / 8);
     bwd_pre_kernel<D><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(out_lo),
@@ -869,7 +842,7 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        void* plan, const void* out, const void* out_lo, const float* lse,
                        const void* dout, void* dq, void* dk,
                        void* dv, void* workspace, int32_t* status, int stages, int num_sms,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, const BwdPrep* prep) {
   const PlanLayout pl = plan_layout(d.B, d.Hq, d.Hkv, d.L, d.S);
   const BwdLayout wl = bwd_layout(d.B, d.Hq, d.Hkv, d.L, d.S, d.D);
   char* base = static_cast<char*>(plan);
@@ -898,19 +871,23 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.status = status;
   p.ctr = reinterpret_cast<int*>(base + pl.sched) + 2;
+  p.aborts = reinterpret_cast<int*>(base + pl.sched) + 5;
+  p.acc_flags = prep != nullptr ? &prep->hdr->flags : nullptr;
+  p.wait_limit_ns = (stages & kBwdMain) ? take_wait_test(kWaitTestBwd, &p.withhold)
+                                         : static_cast<uint32_t>(kWaitTimeoutNs);
   p.drop = d.drop;
   if (d.drop.on) {
     if (d.D == 64)
       return launch_bwd_t<64, true>(tq, tk, tv, tdo, tdq, p, out, out_lo, lse, dout, dq, stages,
-                                    num_sms, stream);
+                                    num_sms, stream, prep);
     return launch_bwd_t<128, true>(tq, tk, tv, tdo, tdq, p, out, out_lo, lse, dout, dq, stages,
-                                   num_sms, stream);
+                                   num_sms, stream, prep);
   }
   if (d.D == 64)
     return launch_bwd_t<64, false>(tq, tk, tv, tdo, tdq, p, out, out_lo, lse, dout, dq, stages,
-                                   num_sms, stream);
+                                   num_sms, stream, prep);
   return launch_bwd_t<128, false>(tq, tk, tv, tdo, tdq, p, out, out_lo, lse, dout, dq, stages,
-                                  num_sms, stream);
+                                  num_sms, stream, prep);
 }
 
 }  // namespace bd

@@ -60,6 +60,12 @@ struct FwdParams {
   float* lse;
   int32_t* status;
   int* ctr;  // work counters in the plan: [next unit, finished CTAs]
+  int* aborts;  // CTAs of the launch that gave up a wait (in the plan)
+  float4* acc;            // optional: zeroed by the idle warps (the backward's dq accumulator)
+  long long acc_n16;      // its size in 16-byte words
+  uint32_t* acc_flags;    // optional: gets kAccZeroed when every CTA finished cleanly
+  uint32_t wait_limit_ns;  // bound of every device-side wait
+  int withhold;            // test only: the producer withholds the first Q load
   DropoutArgs drop;
 };
 
@@ -148,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_full = p_full + 2;                    // [2]
   uint64_t* drain = o_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);  // + the wait limit
   WorkRing* ring = reinterpret_cast<WorkRing*>(smem + C::OFF_BAR + 256);
   static_assert(256 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
   static_assert(C::SMEM <= 232448, "shared memory over the per-block limit");
@@ -156,7 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    *abort_flag = 0;
+    abort_flag[0] = 0;
+    abort_flag[1] = static_cast<int>(p.wait_limit_ns);
     if ((smem_u32(smem) & 1023u) != 0) {  // swizzled tiles need 1024-byte alignment
       set_status(p.status, BD_ERR_CUDA);
       *abort_flag = 1;
@@ -205,6 +212,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ring_publish(ring, kq++, p.ctr, p.n_units, abort_flag, p.status, w) || w < 0) break;
         const Unit u = decode_unit(p, w);
         if (u.n <= 0) continue;
+        // test of the bounded waits: the unit is published but its Q never
+        // arrives, so the MMA thread's wait for it runs out
+        if (p.withhold) break;
         if (!mbar_wait(q_empty, (u_it & 1) ^ 1, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(q_full, 2 * C::QTILE);
         q_issued = true;
@@ -530,6 +540,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) bulk_wait_all();  // this warp's output stores are done
     __syncwarp();
+  } else if ((warp == 2 || warp == 3) && p.acc != nullptr) {
+    // ------------------------------------------------------------ zeroing
+    // The two warps without a role zero the backward's dq accumulator while
+    // the others compute, so that the backward need not make that pass.
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long i = (long long)blockIdx.x * 64 + (warp - 2) * 32 + lane; i < p.acc_n16;
+         i += (long long)gridDim.x * 64)
+      p.acc[i] = z;
+    __threadfence();
   }
 
   // ------------------------------------------------------------ teardown
@@ -539,7 +558,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  if (threadIdx.x == 0) ring_retire(p.ctr);
+  if (threadIdx.x == 0) {
+    // the last CTA records the zeroed accumulator when no CTA gave up (one
+    // that aborted at start skipped its share of the zeroing)
+    if (ring_retire(p.ctr, p.aborts, *abort_flag != 0) == 1 && p.acc_flags != nullptr)
+      atomicOr(p.acc_flags, kAccZeroed);
+  }
 }
 
 template <int D, bool kDrop>
@@ -574,19 +598,22 @@ __global__ void __launch_bounds__(256) v_to_f16_kernel(const uint4* __restrict__
   }
 }
 
+cudaError_t launch_v_to_f16(const void* v, void* v16, long long n, int num_sms,
+                            cudaStream_t stream) {
+  const long long n8 = n / 8;
+  const long long want = (n8 + 255) / 256;
+  const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
+  if (blocks <= 0) return cudaSuccess;
+  v_to_f16_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(v),
+                                              static_cast<uint4*>(v16), n8);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, const CUtensorMap& tol, const AttnDims& d, void* plan, const void* v, void* v16, void* out,
-                       void* out_lo, float* lse, int32_t* status, int num_sms,
-                       cudaStream_t stream) {
-  {
-    const long long n8 = (long long)d.B * d.Hkv * d.S * d.D / 8;
-    const long long want = (n8 + 255) / 256;
-    const int blocks = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
-    v_to_f16_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(v),
-                                                static_cast<uint4*>(v16), n8);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
+                       const CUtensorMap& to, const CUtensorMap& tol, const AttnDims& d,
+                       void* plan, void* out, void* out_lo, float* lse, int32_t* status,
+                       int num_sms, cudaStream_t stream, void* acc, size_t acc_bytes,
+                       uint32_t* acc_flags) {
   const PlanLayout pl = plan_layout(d.B, d.Hq, d.Hkv, d.L, d.S);
   char* base = static_cast<char*>(plan);
   FwdParams p{};
@@ -611,6 +638,11 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.lse = lse;
   p.status = status;
   p.ctr = reinterpret_cast<int*>(base + pl.sched);
+  p.aborts = p.ctr + 4;
+  p.acc = static_cast<float4*>(acc);
+  p.acc_n16 = static_cast<long long>(acc_bytes / 16);
+  p.acc_flags = acc != nullptr ? acc_flags : nullptr;
+  p.wait_limit_ns = take_wait_test(kWaitTestFwd, &p.withhold);
   p.drop = d.drop;
   if (d.drop.on) {
     if (d.D == 64) return launch_fwd_t<64, true>(tq, tk, tv, to, tol, p, num_sms, stream);

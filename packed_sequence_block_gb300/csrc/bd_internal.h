@@ -18,6 +18,16 @@ constexpr int kBN = 128;
 // Device-side waits give up after this long (a healthy wait lasts microseconds).
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 
+static_assert(kWaitTimeoutNs < (1ull << 32), "the wait limit travels as 32 bits");
+
+// Test hook for the bounded waits (bd_test_arm_wait_timeout): the next launch
+// of the chosen kernel from this host thread withholds its producer's first
+// arrival and uses a shorter wait limit.  take_wait_test() returns the
+// launch's limit in nanoseconds and whether to withhold, and disarms.
+constexpr int kWaitTestFwd = 1, kWaitTestBwd = 2;
+void arm_wait_test(int which, uint32_t limit_ns);
+uint32_t take_wait_test(int which, int* withhold);
+
 // Mask lower bound of a query row that attends nothing (padding / past L).
 constexpr int32_t kPadLo = 0x7fffffff;
 
@@ -100,6 +110,56 @@ struct DropoutArgs {
   uint32_t rk[20] = {};
 };
 
+// Workspace of the single-call entry points (bd_attn_fwd / bd_attn_bwd, which
+// take cumulative boundaries): a 256-byte header, the plan, the fp16 copy of
+// v, the forward's rounding residual of out, then the backward workspace.
+// Every part starts on a 256-byte boundary.
+struct WsLayout {
+  PlanLayout plan;
+  BwdLayout bwd;
+  size_t hdr, plan_off, v16, out_lo, bwd_off, total;
+};
+
+inline WsLayout ws_layout(int B, int Hq, int Hkv, int L, int S, int D) {
+  WsLayout w{};
+  w.plan = plan_layout(B, Hq, Hkv, L, S);
+  w.bwd = bwd_layout(B, Hq, Hkv, L, S, D);
+  size_t off = 0;
+  w.hdr = off;      off = 256;
+  w.plan_off = off; off = align256(off + w.plan.total);
+  w.v16 = off;      off = align256(off + 2 * (size_t)B * Hkv * S * D);
+  w.out_lo = off;   off = align256(off + 2 * (size_t)B * Hq * L * D);
+  w.bwd_off = off;  off = align256(off + w.bwd.total);
+  w.total = off;
+  return w;
+}
+
+// What the single-call forward records in the workspace header: the shapes,
+// the boundaries it planned from and the output it wrote.  The backward
+// reuses the plan and the residual of out kept in the workspace only when the
+// header names the same shapes, boundaries, out and lse; otherwise it
+// rebuilds the plan and forms Delta from the bf16 output alone.  `flags`
+// (not part of the match) has kAccZeroed set by the forward kernel once it
+// has zeroed the backward's dq accumulator, and cleared by the backward main
+// kernel, which leaves the accumulator holding sums.
+struct WsTag {
+  uint32_t magic;
+  int32_t B, Hq, Hkv, L, S, D, seq_start;
+  unsigned long long out, lse, cu, row_ptr;
+  uint32_t flags;
+};
+constexpr uint32_t kWsMagic = 0x42445732u;  // "BDW2"
+constexpr uint32_t kAccZeroed = 1u;
+
+// Where the plan builder writes (device pointers into a plan buffer).
+struct PlanPtrs {
+  int B, L, S, seq_start, NQB, QROWS, Lpad, NKT, Spad;
+  int32_t *qlo, *kend, *fwd_range, *bwd_range, *fwd_order, *bwd_order, *sched;
+};
+PlanPtrs plan_ptrs(void* plan, int B, int Hq, int Hkv, int L, int S, int seq_start);
+// Dynamic shared memory the one-CTA plan builder needs (sorting keys).
+size_t plan_cta_smem(const PlanPtrs& pp);
+
 struct AttnDims {
   int B, Hq, Hkv, L, S, D, seq_start;
   float scale;        // softmax scale (resolved, > 0)
@@ -140,21 +200,55 @@ bool make_tmap_f16(CUtensorMap* map, const void* base, int planes, int rows, int
 // box 32 x 128 x 1), the target of the backward's TMA reduce-adds.
 bool make_tmap_dqacc(CUtensorMap* map, void* base, int planes, int rows, int D);
 
-// Converts v to fp16 into v16 (the map tv describes v16), then runs the forward.
+// v (bf16) -> v16 (fp16), the P V operand of the forward.
+cudaError_t launch_v_to_f16(const void* v, void* v16, long long n, int num_sms,
+                            cudaStream_t stream);
+// The forward kernel alone (v16 already written; the map tv describes it).
+// `acc`, when not NULL, is a buffer of acc_bytes (a multiple of 16) that the
+// kernel's otherwise idle warps zero while it runs; `acc_flags` (or NULL)
+// then gets kAccZeroed once every CTA finished without an error.
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const CUtensorMap& tol,
-                       const AttnDims& d, void* plan, const void* v, void* v16, void* out,
+                       const AttnDims& d, void* plan, void* out,
                        void* out_lo, float* lse, int32_t* status, int num_sms,
-                       cudaStream_t stream);
+                       cudaStream_t stream, void* acc = nullptr, size_t acc_bytes = 0,
+                       uint32_t* acc_flags = nullptr);
+// One launch before the single-call forward: block 0 builds the plan from the
+// cumulative boundaries (validating them) and writes the workspace tag; the
+// other blocks convert v to fp16.
+cudaError_t launch_prep_fwd(const int32_t* cu, const int32_t* row_ptr, const PlanPtrs& pp,
+                            const WsTag& tag, WsTag* hdr, const void* v, void* v16,
+                            long long n_v, int32_t* status, int num_sms, cudaStream_t stream);
 // Backward stages (bit mask): per-row terms + accumulator zeroing, the main
 // dK/dV/dQ kernel, and the dq conversion.
 constexpr int kBwdPrepare = 1, kBwdMain = 2, kBwdFinish = 4;
+
+// For the single-call backward: stage 1 also builds the plan from the
+// cumulative boundaries (block 0 of the same launch), and takes the residual
+// of out from the workspace only when the header carries `expect`.
+struct BwdPrep {
+  const int32_t* cu;
+  const int32_t* row_ptr;
+  PlanPtrs pp;
+  WsTag* hdr;
+  WsTag expect;
+};
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const AttnDims& d,
                        void* plan, const void* out, const void* out_lo, const float* lse,
                        const void* dout, void* dq, void* dk,
                        void* dv, void* workspace, int32_t* status, int stages, int num_sms,
-                       cudaStream_t stream);
+                       cudaStream_t stream, const BwdPrep* prep = nullptr);
+
+// Stage 1 of the single-call backward (one launch): block 0 builds the plan
+// unless the workspace header shows the forward's plan for the same inputs;
+// the other blocks write -lse log2 e and -Delta per row and zero the dq
+// accumulator unless the header says the forward already did (the rows'
+// terms as bwd_pre_kernel writes them).
+cudaError_t launch_prep_bwd(const BwdPrep& prep, const void* out, const void* out_lo,
+                            const void* dout, const float* lse, int D, int planes, int L, int Lq,
+                            float* nlse2, float* ndelta, float* dqacc, int32_t* status,
+                            cudaStream_t stream);
 
 }  // namespace bd

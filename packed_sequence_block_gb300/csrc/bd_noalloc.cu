@@ -1,13 +1,13 @@
 // bd_attn_bwd_noalloc: the backward pass for callers that cannot allocate
 // device memory.
 //
-// bd_attn_bwd needs a caller-provided scratch buffer (the fp32 dq accumulator
+// bd_attn_bwd_planned needs a caller-provided scratch buffer (the fp32 dq accumulator
 // and per-row terms).  Some callers cannot provide one: code that runs inside
 // a host runtime which reserves all device memory up front and forbids
 // allocation afterwards (a cudaMalloc there can synchronise the device, stall
 // other work, or fail once memory is fragmented).  This entry point uses a
 // fixed scratch array that is part of the library image instead, so it
-// allocates nothing; it launches the same kernels as bd_attn_bwd.
+// allocates nothing; it launches the same kernels as bd_attn_bwd_planned.
 #include <mutex>
 
 #include "bd_internal.h"
@@ -55,16 +55,16 @@ int bd_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
                         void* plan, size_t plan_bytes, void* dq, void* dk, void* dv,
                         int32_t* dev_status, bd_stream_t stream) {
   if (B < 1 || Hq < 1 || L < 1 || D < 1) return BD_ERR_INVALID_ARG;
-  const size_t need = bd_attn_bwd_workspace_size(B, Hq, Hkv, L, S, D);
+  const size_t need = bd_attn_bwd_planned_workspace_size(B, Hq, Hkv, L, S, D);
   if (need == 0) return BD_ERR_INVALID_ARG;
   if (need > bd::kNoAllocScratchBytes) return BD_ERR_WORKSPACE;
-  // Arguments are checked by bd_attn_bwd below before anything is launched;
+  // Arguments are checked by bd_attn_bwd_planned below before anything is launched;
   // the scratch address is looked up first only because it is an argument.
   void* scratch = nullptr;
   if (bd::scratch_address(&scratch) != cudaSuccess) return BD_ERR_CUDA;
-  return bd_attn_bwd(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
-                     enable_gqa, plan, plan_bytes, dq, dk, dv, scratch, bd::kNoAllocScratchBytes,
-                     dev_status, stream);
+  return bd_attn_bwd_planned(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start,
+                             scale, enable_gqa, plan, plan_bytes, dq, dk, dv, scratch,
+                             bd::kNoAllocScratchBytes, dev_status, stream);
 }
 
 }  // extern "C"

@@ -9,19 +9,9 @@
 // by the query interval [p, end of p's segment).  The kernels below turn the
 // segment list into those bounds and into the tile ranges the attention
 // kernels iterate over, so that fully masked tiles are never loaded.
-#include "bd_ptx.cuh"
+#include "bd_plan_dev.cuh"
 
 namespace bd {
-
-// first k with seg[k] > x, minus one: the segment holding x (seg[0] = 0 <= x < seg[n])
-__device__ __forceinline__ int find_segment(const int32_t* __restrict__ seg, int n, int x) {
-  int lo = 1, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (seg[mid] > x) hi = mid; else lo = mid + 1;
-  }
-  return lo - 1;
-}
 
 // One warp per forward query block or backward key tile.  The warp of a
 // query block first writes the mask bound qlo of each of its rows, the warp
@@ -109,58 +99,6 @@ __global__ void __launch_bounds__(256) plan_tiles_kernel(
 // One CTA; bitonic sort of 64-bit keys in shared memory.
 constexpr int kSortThreads = 1024;
 
-// Key of entry i: cost descending, then index ascending (all keys distinct).
-__device__ __forceinline__ unsigned long long sort_key(const int32_t* __restrict__ range, int i) {
-  const int cost = max(0, range[2 * i + 1] - range[2 * i] + 1);
-  return (static_cast<unsigned long long>(0x7fffffffu - static_cast<unsigned>(cost)) << 32) |
-         static_cast<unsigned>(i);
-}
-
-// Lists of up to kRankSortMax entries: the position of an entry is the number
-// of smaller keys, one comparison pass per entry.
-constexpr int kRankSortMax = 2048;
-
-__device__ void sort_desc(const int32_t* __restrict__ range, int n, int32_t* __restrict__ order,
-                          unsigned long long* keys) {
-  if (n <= kRankSortMax) {
-    for (int i = threadIdx.x; i < n; i += blockDim.x) keys[i] = sort_key(range, i);
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const unsigned long long ki = keys[i];
-      int rank = 0;
-      for (int j = 0; j < n; ++j) rank += keys[j] < ki;
-      order[rank] = i;
-    }
-    __syncthreads();
-    return;
-  }
-  int np = 1;
-  while (np < n) np <<= 1;
-  for (int i = threadIdx.x; i < np; i += blockDim.x) {
-    keys[i] = i < n ? sort_key(range, i) : ~0ull;
-  }
-  __syncthreads();
-  for (int size = 2; size <= np; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < np; i += blockDim.x) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool up = (i & size) == 0;
-          const unsigned long long a = keys[i], c = keys[j];
-          if ((a > c) == up) {
-            keys[i] = c;
-            keys[j] = a;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
-  for (int i = threadIdx.x; i < n; i += blockDim.x)
-    order[i] = static_cast<int32_t>(keys[i] & 0xffffffffu);
-  __syncthreads();
-}
-
 __global__ void __launch_bounds__(kSortThreads) plan_sort_kernel(const int32_t* fwd_range, int nf,
                                                                  int32_t* fwd_order,
                                                                  const int32_t* bwd_range, int nb,
@@ -168,6 +106,37 @@ __global__ void __launch_bounds__(kSortThreads) plan_sort_kernel(const int32_t* 
   extern __shared__ unsigned long long keys[];
   sort_desc(fwd_range, nf, fwd_order, keys);
   sort_desc(bwd_range, nb, bwd_order, keys);
+}
+
+PlanPtrs plan_ptrs(void* plan, int B, int Hq, int Hkv, int L, int S, int seq_start) {
+  const PlanLayout pl = plan_layout(B, Hq, Hkv, L, S);
+  char* base = static_cast<char*>(plan);
+  PlanPtrs pp{};
+  pp.B = B;
+  pp.L = L;
+  pp.S = S;
+  pp.seq_start = seq_start;
+  pp.NQB = pl.NQB;
+  pp.QROWS = pl.QROWS;
+  pp.Lpad = pl.Lpad;
+  pp.NKT = pl.NKT;
+  pp.Spad = pl.Spad;
+  pp.qlo = reinterpret_cast<int32_t*>(base + pl.qlo);
+  pp.kend = reinterpret_cast<int32_t*>(base + pl.kend);
+  pp.fwd_range = reinterpret_cast<int32_t*>(base + pl.fwd_range);
+  pp.bwd_range = reinterpret_cast<int32_t*>(base + pl.bwd_range);
+  pp.fwd_order = reinterpret_cast<int32_t*>(base + pl.fwd_order);
+  pp.bwd_order = reinterpret_cast<int32_t*>(base + pl.bwd_order);
+  pp.sched = reinterpret_cast<int32_t*>(base + pl.sched);
+  return pp;
+}
+
+size_t plan_cta_smem(const PlanPtrs& pp) {
+  const int n = max(pp.B * pp.NQB, pp.B * pp.NKT);
+  int np = 1;
+  while (np < n) np <<= 1;
+  return sizeof(unsigned long long) * np + sizeof(uint32_t) * ((pp.B + 31) / 32) +
+         sizeof(int32_t) * kPlanCuCache;
 }
 
 cudaError_t launch_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg, int B,

@@ -1,0 +1,204 @@
+// Device helpers of the attention plan: binary searches over a row's
+// boundaries, the longest-first sort of the work lists, and the one-CTA plan
+// builder that works straight from cumulative document boundaries.
+//
+// The mask is the per-document causal rule of cp_blockdiag_sdpa (page
+// "nemo_automodel.components.distributed.blockdiag_cp"): the query at global
+// position t attends keys j <= t of its own segment, and a query in a padding
+// segment (id 0) attends nothing.  Ids from cumulative boundaries
+// (doc_ids_from_cu_seqlens, page "nemo_automodel.components.models.glm5_next
+// .cp") number the documents 1..n and give 0 past the last boundary, so the
+// segments of such a row are its non-empty documents, then the padding run:
+// the segment of position t < cu[n] is the document d with cu[d] <= t <
+// cu[d + 1].  The builder below finds d by the same search that assigns the
+// id and never stores the id array.
+#pragma once
+
+#include "bd_ptx.cuh"
+
+namespace bd {
+
+// first k with seg[k] > x, minus one: the segment holding x (seg[0] = 0 <= x < seg[n])
+__device__ __forceinline__ int find_segment(const int32_t* __restrict__ seg, int n, int x) {
+  int lo = 1, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (seg[mid] > x) hi = mid; else lo = mid + 1;
+  }
+  return lo - 1;
+}
+
+// Key of entry i: cost descending, then index ascending (all keys distinct).
+// The ranges may have been written earlier by the same block, so they are read
+// through plain (coherent) loads.
+__device__ __forceinline__ unsigned long long sort_key(const int32_t* range, int i) {
+  const int cost = max(0, range[2 * i + 1] - range[2 * i] + 1);
+  return (static_cast<unsigned long long>(0x7fffffffu - static_cast<unsigned>(cost)) << 32) |
+         static_cast<unsigned>(i);
+}
+
+// Lists of up to kRankSortMax entries: the position of an entry is the number
+// of smaller keys, one comparison pass per entry.
+constexpr int kRankSortMax = 2048;
+
+// Sort a work list by cost (range length), longest first, ties by index, into
+// order[0..n).  Every thread of the block calls it; `keys` holds the next
+// power of two >= n entries of shared memory.
+__device__ inline void sort_desc(const int32_t* range, int n, int32_t* __restrict__ order,
+                                 unsigned long long* keys) {
+  if (n <= kRankSortMax) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) keys[i] = sort_key(range, i);
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const unsigned long long ki = keys[i];
+      int rank = 0;
+      for (int j = 0; j < n; ++j) rank += keys[j] < ki;
+      order[rank] = i;
+    }
+    __syncthreads();
+    return;
+  }
+  int np = 1;
+  while (np < n) np <<= 1;
+  for (int i = threadIdx.x; i < np; i += blockDim.x) keys[i] = i < n ? sort_key(range, i) : ~0ull;
+  __syncthreads();
+  for (int size = 2; size <= np; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < np; i += blockDim.x) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool up = (i & size) == 0;
+          const unsigned long long a = keys[i], c = keys[j];
+          if ((a > c) == up) {
+            keys[i] = c;
+            keys[j] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    order[i] = static_cast<int32_t>(keys[i] & 0xffffffffu);
+  __syncthreads();
+}
+
+// Document index d of position x in a row with boundaries c[0..n] (valid, x < c[n]):
+// the first j in [1, n] with c[j] > x, minus one.  `c` may point to shared or
+// global memory.
+__device__ __forceinline__ int find_doc(const int32_t* c, int n, int x) {
+  int lo = 1, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (c[mid] > x) hi = mid; else lo = mid + 1;
+  }
+  return lo - 1;
+}
+
+// Boundary entries the plan builder copies into shared memory (all rows
+// together); longer lists are searched in global memory.
+constexpr int kPlanCuCache = 4096;
+
+// The whole plan of B rows in one CTA, from cumulative boundaries (rows as in
+// bd_doc_ids_from_cu_seqlens: row b's list is cu[row_ptr[b] .. row_ptr[b+1]-1]).
+// A row whose list does not start at 0, decreases, or ends past S is planned
+// as all padding and BD_ERR_INVALID_ARG goes to *status, as its ids would be
+// all 0.  Writes qlo, kend, both tile ranges, both longest-first orders and
+// zeroes the work counters.  Every thread of the block calls it; `keys` is
+// the sort's shared memory, `bad_rows` one bit per row (B <= 32 * bad_words),
+// `cu_cache` kPlanCuCache entries of shared memory.
+__device__ inline void build_plan_cta(const int32_t* __restrict__ cu,
+                                      const int32_t* __restrict__ row_ptr, const PlanPtrs& pp,
+                                      int32_t* status, unsigned long long* keys,
+                                      uint32_t* bad_rows, int bad_words, int32_t* cu_cache) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (int i = threadIdx.x; i < bad_words; i += blockDim.x) bad_rows[i] = 0;
+  if (threadIdx.x < 8) pp.sched[threadIdx.x] = 0;
+  // the searches below run in shared memory when every row's list fits
+  const int total = __ldg(row_ptr + pp.B);
+  const bool cached = total >= 0 && total <= kPlanCuCache;
+  if (cached)
+    for (int i = threadIdx.x; i < total; i += blockDim.x) cu_cache[i] = __ldg(cu + i);
+  const int32_t* cus = cached ? cu_cache : cu;
+  __syncthreads();
+  // validity of each row's list, one warp per row
+  for (int b = warp; b < pp.B; b += nwarps) {
+    const int base = __ldg(row_ptr + b);
+    const int n = __ldg(row_ptr + b + 1) - base - 1;
+    // a row must also lie inside the boundary array row_ptr[B] declares
+    int bad = n < 0 || base < 0 || base + n + 1 > total;
+    for (int j = lane; !bad && j <= n; j += 32) {
+      const int x = __ldg(cu + base + j);
+      if ((j == 0 && x != 0) || (j > 0 && x < __ldg(cu + base + j - 1)) || x > pp.S) bad = 1;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) {
+      atomicOr(&bad_rows[b >> 5], 1u << (b & 31));
+      set_status(status, BD_ERR_INVALID_ARG);
+    }
+  }
+  __syncthreads();
+  // one warp per forward query block or backward key tile
+  const int nf = pp.B * pp.NQB, nb = pp.B * pp.NKT;
+  for (int w = warp; w < nf + nb; w += nwarps) {
+    const bool fwd = w < nf;
+    const int u = fwd ? w : w - nf;
+    const int b = fwd ? u / pp.NQB : u / pp.NKT;
+    const int blk = fwd ? u % pp.NQB : u % pp.NKT;
+    const bool ok = ((bad_rows[b >> 5] >> (b & 31)) & 1u) == 0;
+    const int base = __ldg(row_ptr + b);
+    const int n = ok ? __ldg(row_ptr + b + 1) - base - 1 : 0;
+    const int32_t* c = cus + base;
+    const int last = ok ? c[n] : 0;  // positions >= last are padding
+    int mn = 0x7fffffff, mx = -1;
+    if (fwd) {
+      for (int r = lane; r < pp.QROWS; r += 32) {
+        const int i = blk * pp.QROWS + r;
+        const int t = pp.seq_start + i;
+        int32_t lo = kPadLo;
+        if (i < pp.L && t < last) lo = c[find_doc(c, n, t)];
+        pp.qlo[(size_t)b * pp.Lpad + i] = lo;
+        if (lo != kPadLo) {
+          mn = min(mn, lo);
+          mx = max(mx, t);
+        }
+      }
+    } else {
+      for (int r = lane; r < kBN; r += 32) {
+        const int p = blk * kBN + r;
+        int32_t e = p;
+        if (p < last) e = c[find_doc(c, n, p) + 1];
+        pp.kend[(size_t)b * pp.Spad + p] = e;
+        if (e > p) {
+          mn = min(mn, p);
+          mx = max(mx, e);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (lane == 0) {
+      if (fwd) {
+        const bool any = mx >= 0;
+        pp.fwd_range[2 * u] = any ? mn / kBN : 0;
+        pp.fwd_range[2 * u + 1] = any ? mx / kBN : -1;
+      } else {
+        int a = 0, e = 0;
+        if (mx >= 0) {
+          a = max(mn, pp.seq_start) - pp.seq_start;
+          e = min(mx, pp.seq_start + pp.L) - pp.seq_start;
+        }
+        pp.bwd_range[2 * u] = (a < e) ? a / kBM : 0;
+        pp.bwd_range[2 * u + 1] = (a < e) ? (e - 1) / kBM : -1;
+      }
+    }
+  }
+  __threadfence_block();
+  __syncthreads();
+  sort_desc(pp.fwd_range, nf, pp.fwd_order, keys);
+  sort_desc(pp.bwd_range, nb, pp.bwd_order, keys);
+}
+
+}  // namespace bd

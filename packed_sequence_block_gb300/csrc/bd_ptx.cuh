@@ -69,18 +69,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
-// after kWaitTimeoutNs (or as soon as another role of the CTA gave up, which
-// it signals through *abort): then records BD_ERR_TIMEOUT, raises *abort and
-// returns false.  Never spins without bound.
+// after the launch's wait limit (or as soon as another role of the CTA gave
+// up, which it signals through *abort): then records BD_ERR_TIMEOUT, raises
+// *abort and returns false.  Never spins without bound.  `abort` points at
+// two words of shared memory: the abort flag, then the limit in nanoseconds
+// (kWaitTimeoutNs unless the host shortened it for a test).
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort,
                                             int32_t* status) {
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = static_cast<uint32_t>(abort[1]);
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 256; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    if (globaltimer_ns() - t0 > limit) {
       *abort = 1;
       set_status(status, BD_ERR_TIMEOUT);
       return false;
@@ -497,13 +500,20 @@ __device__ __forceinline__ bool ring_take_warp(WorkRing* r, uint32_t k, volatile
 }
 
 // Called by one thread per CTA after the CTA's last fetch (behind __syncthreads).
-__device__ __forceinline__ void ring_retire(int* counters) {
+// `aborts` counts the CTAs of the launch that gave up a wait.  Returns 0 in
+// every CTA but the last to finish; the last one resets the counters and gets
+// 1 when no CTA gave up, 2 otherwise.
+__device__ __forceinline__ int ring_retire(int* counters, int* aborts, bool aborted) {
   __threadfence();
+  if (aborted) atomicAdd(aborts, 1);
   if (atomicAdd(&counters[1], 1) == static_cast<int>(gridDim.x) - 1) {
     __threadfence();
+    const int gave_up = atomicExch(aborts, 0);
     atomicExch(&counters[0], 0);
     atomicExch(&counters[1], 0);
+    return gave_up == 0 ? 1 : 2;
   }
+  return 0;
 }
 
 }  // namespace bd

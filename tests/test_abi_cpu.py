@@ -50,8 +50,15 @@ def test_sizes_are_host_computed(lib_):
     b = lib_.bd_attn_plan_size(2, 32, 8, 8192, 8192)
     assert a > 0 and b > a and a % 256 == 0
     assert lib_.bd_attn_plan_size(0, 1, 1, 1, 1) == 0
-    w = lib_.bd_attn_bwd_workspace_size(1, 32, 8, 8192, 8192, 128)
+    w = lib_.bd_attn_bwd_planned_workspace_size(1, 32, 8, 8192, 8192, 128)
     assert w >= 32 * 8192 * 128 * 4 + 32 * 8192 * 8
+    # the single-call workspace holds the plan, the fp16 v, the residual of out
+    # and the backward's accumulator and row terms
+    one = lib_.bd_attn_workspace_size(1, 32, 8, 8192, 8192, 128)
+    assert one % 256 == 0
+    assert one >= (a + lib_.bd_attn_fwd_planned_workspace_size(1, 8, 8192, 128) + w
+                   + 2 * 32 * 8192 * 128)
+    assert lib_.bd_attn_workspace_size(1, 32, 8, 8192, 8192, 0) == 0
 
 
 FAKE = 1 << 20  # a non-null, 256-aligned dummy address: never dereferenced on these paths
@@ -62,7 +69,7 @@ def _fwd(lib, **kw):
              scale=0.0, gqa=1, plan=FAKE, plan_bytes=1 << 30, out=FAKE, lse=FAKE, lo=None,
              ws=FAKE, ws_bytes=1 << 30, st=None, stream=None)
     a.update(kw)
-    return lib.bd_attn_fwd(a["q"], a["k"], a["v"], a["B"], a["Hq"], a["Hkv"], a["L"], a["S"],
+    return lib.bd_attn_fwd_planned(a["q"], a["k"], a["v"], a["B"], a["Hq"], a["Hkv"], a["L"], a["S"],
                          a["D"], a["seq_start"], a["scale"], a["gqa"], a["plan"], a["plan_bytes"],
                          a["out"], a["lse"], a["lo"], a["ws"], a["ws_bytes"], a["st"],
                          a["stream"])
@@ -90,7 +97,7 @@ def test_fwd_rejects_bad_arguments(lib_, kw, code):
 
 
 def test_bwd_and_plan_reject_bad_arguments(lib_):
-    f = lib_.bd_attn_bwd
+    f = lib_.bd_attn_bwd_planned
     args = [FAKE] * 7 + [1, 4, 2, 256, 256, 64, 0, 0.0, 1, FAKE, 1 << 30, FAKE, FAKE, FAKE,
                          FAKE, 1 << 30, None, None]
     bad = list(args)
@@ -133,20 +140,95 @@ def test_layout_entry_points_reject_bad_arguments_on_the_host(lib_):
 @pytest.mark.parametrize("p", [1.0, 1.5, -0.1, float("nan")])
 def test_dropout_entry_points_reject_bad_p_on_the_host(lib_, p):
     """dropout_p outside [0, 1) is refused before any shape check or launch."""
-    f = lib_.bd_attn_fwd_dropout
+    f = lib_.bd_attn_fwd_dropout_planned
     assert f(FAKE, FAKE, FAKE, 1, 4, 2, 256, 256, 64, 0, 0.0, 1, FAKE, 1 << 30, FAKE, FAKE, None,
              FAKE, 1 << 30, p, 7, 0, None, None) == 1
-    g = lib_.bd_attn_bwd_dropout
+    g = lib_.bd_attn_bwd_dropout_planned
     assert g(*([FAKE] * 7), 1, 4, 2, 256, 256, 64, 0, 0.0, 1, FAKE, 1 << 30, FAKE, FAKE, FAKE,
              FAKE, 1 << 30, p, 7, 0, None, None) == 1
+    f = lib_.bd_attn_fwd_dropout
+    assert f(*([FAKE] * 3), 1, 4, 2, 256, 256, 64, FAKE, FAKE, 0, 0.0, 1, FAKE, FAKE, FAKE,
+             1 << 30, p, 7, 0, None, None) == 1
+    g = lib_.bd_attn_bwd_dropout
+    assert g(*([FAKE] * 6), 1, 4, 2, 256, 256, 64, FAKE, FAKE, 0, 0.0, 1, FAKE, FAKE, FAKE, FAKE,
+             1 << 30, p, 7, 0, None, None) == 1
 
 
 def test_dropout_entry_points_check_shapes_like_the_plain_ones(lib_):
-    f = lib_.bd_attn_fwd_dropout
+    f = lib_.bd_attn_fwd_dropout_planned
     assert f(FAKE, FAKE, FAKE, 1, 4, 2, 256, 256, 96, 0, 0.0, 1, FAKE, 1 << 30, FAKE, FAKE, None,
              FAKE, 1 << 30, 0.1, 7, 0, None, None) == 2   # D = 96 unsupported
     assert f(FAKE, FAKE, FAKE, 1, 4, 2, 256, 256, 64, 0, 0.0, 1, FAKE, 1 << 30, FAKE, FAKE, None,
              FAKE, 16, 0.1, 7, 0, None, None) == 5        # workspace too small
-    g = lib_.bd_attn_bwd_dropout
+    g = lib_.bd_attn_bwd_dropout_planned
     assert g(*([FAKE] * 7), 1, 4, 2, 256, 256, 64, 0, 0.0, 1, FAKE, 1 << 30, FAKE, FAKE, FAKE,
              FAKE, 8, 0.1, 7, 0, None, None) == 5         # workspace too small
+
+
+def _fwd_cu(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, B=1, Hq=4, Hkv=2, L=256, S=256, D=64, cu=FAKE, rp=FAKE,
+             seq_start=0, scale=0.0, gqa=1, out=FAKE, lse=FAKE, ws=FAKE, ws_bytes=1 << 30,
+             st=None, stream=None)
+    a.update(kw)
+    return lib.bd_attn_fwd(a["q"], a["k"], a["v"], a["B"], a["Hq"], a["Hkv"], a["L"], a["S"],
+                           a["D"], a["cu"], a["rp"], a["seq_start"], a["scale"], a["gqa"],
+                           a["out"], a["lse"], a["ws"], a["ws_bytes"], a["st"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cu=None), 1),
+    (dict(rp=None), 1),
+    (dict(q=None), 1),
+    (dict(D=96), 2),
+    (dict(Hq=3, Hkv=2), 1),
+    (dict(gqa=0), 1),
+    (dict(seq_start=1), 1),
+    (dict(L=300), 1),
+    (dict(q=FAKE + 8), 1),
+    (dict(out=FAKE + 8), 1),
+    (dict(ws=None), 1),
+    (dict(ws=FAKE + 16), 1),
+    (dict(ws_bytes=16), 5),
+    (dict(B=1, L=1 << 22, S=1 << 22), 2),
+])
+def test_single_call_fwd_rejects_bad_arguments(lib_, kw, code):
+    assert _fwd_cu(lib_, **kw) == code
+
+
+def test_single_call_bwd_rejects_bad_arguments(lib_):
+    f = lib_.bd_attn_bwd
+    args = [FAKE] * 6 + [1, 4, 2, 256, 256, 64, FAKE, FAKE, 0, 0.0, 1, FAKE, FAKE, FAKE, FAKE,
+                         1 << 30, None, None]
+    bad = list(args)
+    bad[11] = 100  # D
+    assert f(*bad) == 2
+    bad = list(args)
+    bad[12] = None  # cu_seqlens
+    assert f(*bad) == 1
+    bad = list(args)
+    bad[21] = 8  # workspace too small
+    assert f(*bad) == 5
+    bad = list(args)
+    bad[19] = FAKE + 4  # misaligned dv
+    assert f(*bad) == 1
+    st = lib_.bd_attn_bwd_stages
+    sargs = args[:-1] + [0, None]
+    assert st(*sargs) == 1  # no stage
+    sargs = args[:-1] + [8, None]
+    assert st(*sargs) == 1  # unknown stage bit
+
+
+def test_noalloc_limit_matches_the_header():
+    from packed_sequence_block_gb300 import _native
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+BD_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "BD_NOALLOC_SCRATCH_BYTES not found in the header"
+    assert _native.NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_wait_test_hook_rejects_bad_arguments(lib_):
+    f = lib_.bd_test_arm_wait_timeout
+    assert f(0, 1000) == 1
+    assert f(3, 1000) == 1
+    assert f(1, 0) == 1
+    assert f(2, 2000001) == 1

@@ -1,6 +1,8 @@
 """bench.py reports the backward kernel's DRAM traffic from the committed ncu
-summary only while the kernel sources are the ones that were profiled."""
+figures (a JSON file beside the prose summary) only while the kernel sources
+are the ones that were profiled."""
 import hashlib
+import json
 import os
 import shutil
 import sys
@@ -10,14 +12,16 @@ sys.path.insert(0, ROOT)
 
 import bench  # noqa: E402
 
+FIG = "bd_bwd_kernel_lognormal8k.json"
 
-def _tree(tmp_path, body_lines, sources):
+
+def _tree(tmp_path, fig, sources):
     os.makedirs(tmp_path / "profiles")
     csrc = tmp_path / "packed_sequence_block_gb300" / "csrc"
     os.makedirs(csrc)
     for name, text in sources.items():
         (csrc / name).write_text(text)
-    (tmp_path / "profiles" / "bd_bwd_kernel_lognormal8k.md").write_text("\n".join(body_lines) + "\n")
+    (tmp_path / "profiles" / FIG).write_text(json.dumps(fig))
     return tmp_path
 
 
@@ -27,9 +31,9 @@ def _sha(text):
 
 def test_traffic_follows_the_profiled_sources(tmp_path, monkeypatch):
     src = {"bd_bwd.cu": "kernel v1\n", "bd_ptx.cuh": "helpers v1\n"}
-    root = _tree(tmp_path, ["    traffic_bytes_per_launch: 123456",
-                            f"    source_sha256: bd_bwd.cu {_sha(src['bd_bwd.cu'])}",
-                            f"    source_sha256: bd_ptx.cuh {_sha(src['bd_ptx.cuh'])}"], src)
+    fig = {"workload": "lognormal8k", "seed": 0, "traffic_bytes_per_launch": 123456,
+           "source_sha256": {n: _sha(t) for n, t in src.items()}}
+    root = _tree(tmp_path, fig, src)
     monkeypatch.setattr(bench, "ROOT", str(root))
     traffic, why = bench.profiled_traffic("lognormal8k", 0)
     assert traffic == 123456 and "ncu" in why
@@ -44,20 +48,20 @@ def test_traffic_follows_the_profiled_sources(tmp_path, monkeypatch):
 
 def test_traffic_needs_both_the_figure_and_the_hashes(tmp_path, monkeypatch):
     src = {"bd_bwd.cu": "kernel v1\n"}
-    root = _tree(tmp_path, ["    traffic_bytes_per_launch: 99"], src)
+    root = _tree(tmp_path, {"workload": "lognormal8k", "seed": 0,
+                            "traffic_bytes_per_launch": 99}, src)
     monkeypatch.setattr(bench, "ROOT", str(root))
     assert bench.profiled_traffic("lognormal8k", 0)[0] is None
     shutil.rmtree(root / "profiles")
     assert bench.profiled_traffic("lognormal8k", 0) == (None, "no capture")
 
 
-def test_committed_summary_parses():
-    """The committed summary carries a figure and hashes for files that exist."""
-    lines = open(os.path.join(ROOT, "profiles", "bd_bwd_kernel_lognormal8k.md")).read().splitlines()
-    figures = [ln for ln in lines if ln.strip().startswith("traffic_bytes_per_launch:")]
-    hashes = [ln.split(":", 1)[1].split() for ln in lines if ln.strip().startswith("source_sha256:")]
-    assert len(figures) == 1 and int(figures[0].split(":", 1)[1]) > 0
-    assert hashes
-    for name, digest in hashes:
+def test_committed_figures_parse():
+    """The committed figures carry a traffic number and hashes of files that exist."""
+    with open(os.path.join(ROOT, "profiles", FIG)) as f:
+        fig = json.load(f)
+    assert isinstance(fig["traffic_bytes_per_launch"], int) and fig["traffic_bytes_per_launch"] > 0
+    assert fig["source_sha256"]
+    for name, digest in fig["source_sha256"].items():
         assert os.path.exists(os.path.join(ROOT, "packed_sequence_block_gb300", "csrc", name))
         assert len(digest) == 64

@@ -146,10 +146,10 @@ def test_dropout_zero_is_the_plain_path(cuda_lib):
     a = A.attn_forward(q, k, v, plan, 0, None, True)
     from packed_sequence_block_gb300 import _native as N
     out, lse = torch.empty_like(q), torch.empty_like(a[1])
-    ws = torch.empty(N.bd_attn_fwd_workspace_size(wl.B, wl.Hkv, wl.S, wl.D), dtype=torch.uint8,
-                     device="cuda")
-    N.bd_attn_fwd_dropout(q, k, v, wl.B, wl.Hq, wl.Hkv, wl.L, wl.S, wl.D, 0, wl.D ** -0.5, True,
-                          plan, out, lse, 0.0, 123, 0, None, ws)
+    ws = torch.empty(N.bd_attn_fwd_planned_workspace_size(wl.B, wl.Hkv, wl.S, wl.D),
+                     dtype=torch.uint8, device="cuda")
+    N.bd_attn_fwd_dropout_planned(q, k, v, wl.B, wl.Hq, wl.Hkv, wl.L, wl.S, wl.D, 0,
+                                  wl.D ** -0.5, True, plan, out, lse, 0.0, 123, 0, None, ws)
     assert torch.equal(out, a[0]) and torch.equal(lse, a[1])
 
 
