@@ -359,12 +359,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sds = smem_u32(smem + C::OFF_DS);
       const uint32_t tDK = tmem, tDV = tmem + 128, tS = tmem + 256, tDP = tmem + 384;
       // D[128 keys, 128 queries] = A[keys, D] (K-major) * B[queries, D]^T (K-major)
+      // Each operand's descriptor is built once per product and stepped by a
+      // constant per instruction (sdesc_add), and every step but the first
+      // accumulates through a folded predicate: this thread's instruction
+      // count per tcgen05.mma stays low.
       auto issue_kmajor = [&](uint32_t d, uint32_t a, uint32_t b, uint32_t idesc) {
+        const uint64_t ad = make_sdesc_sw128(a, 16, 1024), bd = make_sdesc_sw128(b, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(d, make_sdesc_sw128(a + off, 16, 1024), make_sdesc_sw128(b + off, 16, 1024),
-                 idesc, kk > 0);
+          if (kk == 0)
+            mma_ss(d, ad, bd, idesc, 0);
+          else
+            mma_ss_acc(d, sdesc_add(ad, off), sdesc_add(bd, off), idesc);
         }
       };
       // D[keys, D] (+)= A[tmem, keys x 128 queries] * B[queries, D] (MN-major smem).
@@ -372,25 +379,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 128-column region and those for [64, 128) at [64, 96) (each P/dS
       // warpgroup packs into the first half of its own columns).
       auto issue_ts = [&](uint32_t d, uint32_t a_tmem, uint32_t b, bool acc, uint32_t idesc) {
+        const uint64_t bd = make_sdesc_sw128(b, 16384, 1024);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ts(d, a_tmem + ks * 8 + (ks >= 4 ? 32 : 0),
-                 make_sdesc_sw128(b + ks * 2048, 16384, 1024), idesc, (acc || ks > 0));
+        for (int ks = 0; ks < 8; ++ks) {
+          if (ks == 0)
+            mma_ts(d, a_tmem, bd, idesc, acc);
+          else
+            mma_ts_acc(d, a_tmem + ks * 8 + (ks >= 4 ? 32 : 0), sdesc_add(bd, ks * 2048), idesc);
+        }
       };
       // dK[keys, D] += dS^T[keys, queries] * Q[queries, D]: the dS tile (key rows,
       // queries contiguous) is the K-major A operand, Q the MN-major B operand
       auto issue_dk = [&](uint32_t b, bool acc) {
+        const uint64_t ad = make_sdesc_sw128(sds, 16, 1024), bd = make_sdesc_sw128(b, 16384, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tDK, make_sdesc_sw128(sds + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                 make_sdesc_sw128(b + kk * 2048, 16384, 1024), C::IDESC_DK, acc || kk > 0);
+        for (int kk = 0; kk < 8; ++kk) {
+          if (kk == 0)
+            mma_ss(tDK, ad, bd, C::IDESC_DK, acc);
+          else
+            mma_ss_acc(tDK, sdesc_add(ad, (kk >> 2) * 16384 + (kk & 3) * 32),
+                       sdesc_add(bd, kk * 2048), C::IDESC_DK);
+        }
       };
       // dQ[queries, D] = dS[queries, keys] (MN-major smem) * K[keys, D] (MN-major smem)
       auto issue_dq = [&]() {
+        const uint64_t ad = make_sdesc_sw128(sds, 16384, 1024);
+        const uint64_t bd = make_sdesc_sw128(sk, 16384, 1024);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ss(tDP, make_sdesc_sw128(sds + ks * 2048, 16384, 1024),
-                 make_sdesc_sw128(sk + ks * 2048, 16384, 1024), C::IDESC_DQ, ks > 0);
+        for (int ks = 0; ks < 8; ++ks) {
+          if (ks == 0)
+            mma_ss(tDP, ad, bd, C::IDESC_DQ, 0);
+          else
+            mma_ss_acc(tDP, sdesc_add(ad, ks * 2048), sdesc_add(bd, ks * 2048), C::IDESC_DQ);
+        }
       };
       uint32_t kv_u = 0, st_it = 0, it_g = 0, kq = 0;
       bool ok = true;

@@ -270,21 +270,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sq0 = smem_u32(smem + C::OFF_Q);
       const uint32_t sk0 = smem_u32(smem + C::OFF_K);
       const uint32_t sv0 = smem_u32(smem + C::OFF_V);
+      // each operand's descriptor is built once per product and stepped by
+      // a constant per instruction (sdesc_add), keeping this thread's
+      // instruction count per tcgen05.mma low
       auto issue_s = [&](int s, int st) {
-        const uint32_t qa = sq0 + s * C::QTILE, ka = sk0 + st * C::KTILE;
+        const uint64_t qd = make_sdesc_sw128(sq0 + s * C::QTILE, 16, 1024);
+        const uint64_t kd = make_sdesc_sw128(sk0 + st * C::KTILE, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + s * 128, make_sdesc_sw128(qa + off, 16, 1024),
-                 make_sdesc_sw128(ka + off, 16, 1024), C::IDESC_S, kk > 0);
+          if (kk == 0)
+            mma_ss(tmem + s * 128, qd, kd, C::IDESC_S, 0);
+          else
+            mma_ss_acc(tmem + s * 128, sdesc_add(qd, off), sdesc_add(kd, off), C::IDESC_S);
         }
       };
       auto issue_pv = [&](int s, int st, bool acc) {
-        const uint32_t va = sv0 + st * C::KTILE;
+        const uint64_t vd = make_sdesc_sw128(sv0 + st * C::KTILE, 16384, 1024);
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks) {
-          mma_ts(tmem + 256 + s * 128, tmem + s * 128 + ks * 8,
-                 make_sdesc_sw128(va + ks * 2048, 16384, 1024), C::IDESC_PV, (acc || ks > 0));
+          if (ks == 0)
+            mma_ts(tmem + 256 + s * 128, tmem + s * 128, vd, C::IDESC_PV, acc);
+          else
+            mma_ts_acc(tmem + 256 + s * 128, tmem + s * 128 + ks * 8, sdesc_add(vd, ks * 2048),
+                       C::IDESC_PV);
         }
       };
       uint32_t kv_it = 0, u_it = 0, t_it = 0, kq = 0;
