@@ -516,10 +516,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t stg = smem_u32(smem + C::OFF_STG) + (warp - 4) * 4096;
       const int i0 = i - lane;  // the warp's first row
       const int plane_o = u.b * p.Hq + h;
+      // the row's D columns in one TMEM read (the scores no longer hold
+      // registers), instead of one dependent read per chunk
+      uint32_t ov[D];
+      if constexpr (D == 128) {
+        tmem_ld128(tO, ov);
+      } else {
+        uint32_t (&o0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ov[0]);
+        uint32_t (&o1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ov[32]);
+        tmem_ld32x2(tO, tO + 32, o0, o1);
+      }
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tO + c * 32, v);
+        const uint32_t* v = ov + c * 32;
         uint32_t pk[16], pl[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {

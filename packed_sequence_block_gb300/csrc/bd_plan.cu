@@ -132,10 +132,13 @@ PlanPtrs plan_ptrs(void* plan, int B, int Hq, int Hkv, int L, int S, int seq_sta
 }
 
 size_t plan_cta_smem(const PlanPtrs& pp) {
-  const int n = max(pp.B * pp.NQB, pp.B * pp.NKT);
+  const int nf = pp.B * pp.NQB, nb = pp.B * pp.NKT;
   int np = 1;
-  while (np < n) np <<= 1;
-  return sizeof(unsigned long long) * np + sizeof(uint32_t) * ((pp.B + 31) / 32) +
+  while (np < max(nf, nb)) np <<= 1;
+  // the keys of both lists side by side (rank sort), or one list padded to a
+  // power of two (bitonic sort)
+  const int nkeys = (nf <= kRankSortMax && nb <= kRankSortMax) ? max(np, nf + nb) : np;
+  return sizeof(unsigned long long) * nkeys + sizeof(uint32_t) * ((pp.B + 31) / 32) +
          sizeof(int32_t) * kPlanCuCache;
 }
 

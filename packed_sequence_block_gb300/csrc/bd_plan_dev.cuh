@@ -96,7 +96,7 @@ __device__ __forceinline__ int find_doc(const int32_t* c, int n, int x) {
 }
 
 // Boundary entries the plan builder copies into shared memory (all rows
-// together); longer lists are searched in global memory.
+// together, then the row pointers); longer lists are read from global memory.
 constexpr int kPlanCuCache = 4096;
 
 // The whole plan of B rows in one CTA, from cumulative boundaries (rows as in
@@ -114,22 +114,27 @@ __device__ inline void build_plan_cta(const int32_t* __restrict__ cu,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   for (int i = threadIdx.x; i < bad_words; i += blockDim.x) bad_rows[i] = 0;
   if (threadIdx.x < 8) pp.sched[threadIdx.x] = 0;
-  // the searches below run in shared memory when every row's list fits
+  // Everything below reads the boundaries and row pointers from shared memory
+  // when they fit (the blocks running beside this one stream through L1, so
+  // global reads here would keep missing).
   const int total = __ldg(row_ptr + pp.B);
-  const bool cached = total >= 0 && total <= kPlanCuCache;
-  if (cached)
+  const bool cached = total >= 0 && total + pp.B + 1 <= kPlanCuCache;
+  if (cached) {
     for (int i = threadIdx.x; i < total; i += blockDim.x) cu_cache[i] = __ldg(cu + i);
+    for (int i = threadIdx.x; i <= pp.B; i += blockDim.x) cu_cache[total + i] = __ldg(row_ptr + i);
+  }
   const int32_t* cus = cached ? cu_cache : cu;
+  const int32_t* rps = cached ? cu_cache + total : row_ptr;
   __syncthreads();
   // validity of each row's list, one warp per row
   for (int b = warp; b < pp.B; b += nwarps) {
-    const int base = __ldg(row_ptr + b);
-    const int n = __ldg(row_ptr + b + 1) - base - 1;
+    const int base = rps[b];
+    const int n = rps[b + 1] - base - 1;
     // a row must also lie inside the boundary array row_ptr[B] declares
     int bad = n < 0 || base < 0 || base + n + 1 > total;
     for (int j = lane; !bad && j <= n; j += 32) {
-      const int x = __ldg(cu + base + j);
-      if ((j == 0 && x != 0) || (j > 0 && x < __ldg(cu + base + j - 1)) || x > pp.S) bad = 1;
+      const int x = cus[base + j];
+      if ((j == 0 && x != 0) || (j > 0 && x < cus[base + j - 1]) || x > pp.S) bad = 1;
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) {
       atomicOr(&bad_rows[b >> 5], 1u << (b & 31));
@@ -145,8 +150,8 @@ __device__ inline void build_plan_cta(const int32_t* __restrict__ cu,
     const int b = fwd ? u / pp.NQB : u / pp.NKT;
     const int blk = fwd ? u % pp.NQB : u % pp.NKT;
     const bool ok = ((bad_rows[b >> 5] >> (b & 31)) & 1u) == 0;
-    const int base = __ldg(row_ptr + b);
-    const int n = ok ? __ldg(row_ptr + b + 1) - base - 1 : 0;
+    const int base = rps[b];
+    const int n = ok ? rps[b + 1] - base - 1 : 0;
     const int32_t* c = cus + base;
     const int last = ok ? c[n] : 0;  // positions >= last are padding
     int mn = 0x7fffffff, mx = -1;
@@ -197,8 +202,26 @@ __device__ inline void build_plan_cta(const int32_t* __restrict__ cu,
   }
   __threadfence_block();
   __syncthreads();
-  sort_desc(pp.fwd_range, nf, pp.fwd_order, keys);
-  sort_desc(pp.bwd_range, nb, pp.bwd_order, keys);
+  if (nf <= kRankSortMax && nb <= kRankSortMax) {
+    // both lists at once: one pass of loads, one barrier, then the ranks
+    unsigned long long* kb = keys + nf;
+    for (int i = threadIdx.x; i < nf + nb; i += blockDim.x)
+      keys[i] = i < nf ? sort_key(pp.fwd_range, i) : sort_key(pp.bwd_range, i - nf);
+    __syncthreads();
+    for (int i = threadIdx.x; i < nf + nb; i += blockDim.x) {
+      const bool f = i < nf;
+      const unsigned long long* ks = f ? keys : kb;
+      const int n = f ? nf : nb, idx = f ? i : i - nf;
+      const unsigned long long ki = ks[idx];
+      int rank = 0;
+      for (int j = 0; j < n; ++j) rank += ks[j] < ki;
+      (f ? pp.fwd_order : pp.bwd_order)[rank] = idx;
+    }
+    __syncthreads();
+  } else {
+    sort_desc(pp.fwd_range, nf, pp.fwd_order, keys);
+    sort_desc(pp.bwd_range, nb, pp.bwd_order, keys);
+  }
 }
 
 }  // namespace bd

@@ -22,7 +22,9 @@ __device__ __forceinline__ void plan_block(const int32_t* cu, const int32_t* row
   int np = 1;
   while (np < max(nf, nb)) np <<= 1;
   const int bad_words = (pp.B + 31) / 32;
-  uint32_t* bad = reinterpret_cast<uint32_t*>(prep_smem + np);
+  // as plan_cta_smem lays it out: keys, row bits, boundary cache
+  const int nkeys = (nf <= kRankSortMax && nb <= kRankSortMax) ? max(np, nf + nb) : np;
+  uint32_t* bad = reinterpret_cast<uint32_t*>(prep_smem + nkeys);
   int32_t* cache = reinterpret_cast<int32_t*>(bad + bad_words);
   build_plan_cta(cu, row_ptr, pp, status, prep_smem, bad, bad_words, cache);
 }
