@@ -95,6 +95,22 @@ __device__ __forceinline__ int find_doc(const int32_t* c, int n, int x) {
   return lo - 1;
 }
 
+// The same document for an x at or past the position whose document was d
+// (d < 0: none yet): a few steps forward from d, else the search.  The steps
+// skip empty documents as the search does, so both give the one d with
+// c[d] <= x < c[d + 1].
+__device__ __forceinline__ int next_doc(const int32_t* c, int n, int x, int d) {
+  if (d >= 0) {
+#pragma unroll 1
+    for (int s = 0; s < 4; ++s) {
+      if (c[d + 1] > x) return d;
+      ++d;
+    }
+    if (c[d + 1] > x) return d;
+  }
+  return find_doc(c, n, x);
+}
+
 // Boundary entries the plan builder copies into shared memory (all rows
 // together, then the row pointers); longer lists are read from global memory.
 constexpr int kPlanCuCache = 4096;
@@ -156,11 +172,15 @@ __device__ inline void build_plan_cta(const int32_t* __restrict__ cu,
     const int last = ok ? c[n] : 0;  // positions >= last are padding
     int mn = 0x7fffffff, mx = -1;
     if (fwd) {
+      int d = -1;  // this lane's document so far (its rows increase)
       for (int r = lane; r < pp.QROWS; r += 32) {
         const int i = blk * pp.QROWS + r;
         const int t = pp.seq_start + i;
         int32_t lo = kPadLo;
-        if (i < pp.L && t < last) lo = c[find_doc(c, n, t)];
+        if (i < pp.L && t < last) {
+          d = next_doc(c, n, t, d);
+          lo = c[d];
+        }
         pp.qlo[(size_t)b * pp.Lpad + i] = lo;
         if (lo != kPadLo) {
           mn = min(mn, lo);
@@ -168,10 +188,14 @@ __device__ inline void build_plan_cta(const int32_t* __restrict__ cu,
         }
       }
     } else {
+      int d = -1;
       for (int r = lane; r < kBN; r += 32) {
         const int p = blk * kBN + r;
         int32_t e = p;
-        if (p < last) e = c[find_doc(c, n, p) + 1];
+        if (p < last) {
+          d = next_doc(c, n, p, d);
+          e = c[d + 1];
+        }
         pp.kend[(size_t)b * pp.Spad + p] = e;
         if (e > p) {
           mn = min(mn, p);
