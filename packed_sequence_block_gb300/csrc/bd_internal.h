@@ -46,7 +46,8 @@ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 //                              query block (hi < lo when empty)
 //   bwd_range int32 [B*NKT, 2] query-tile range [lo, hi] of each key tile
 //   fwd_order int32 [B*NQB]    query blocks sorted by cost, longest first
-//   bwd_order int32 [B*NKT]    key tiles sorted by cost, longest first
+//   bwd_order int32 [B*NKT]    key tiles by document: largest documents first, each
+//                              document's tiles together, longest first
 //   sched     int32 [8]        work counters: [0..1] forward, [2..3] backward
 //                              (next unit, finished CTAs); zeroed by the
 //                              planner, reset by the last CTA of each launch

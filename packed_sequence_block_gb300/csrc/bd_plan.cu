@@ -95,17 +95,20 @@ __global__ void __launch_bounds__(256) plan_tiles_kernel(
   }
 }
 
-// Sort both work lists by cost (range length), longest first, ties by index.
-// One CTA; bitonic sort of 64-bit keys in shared memory.
+// Sort the forward work list by cost (range length), longest first, and the
+// backward one by document (fill_bwd_keys); ties by index.  One CTA; 64-bit
+// keys in shared memory, then the run-head scan's ints.
 constexpr int kSortThreads = 1024;
 
 __global__ void __launch_bounds__(kSortThreads) plan_sort_kernel(const int32_t* fwd_range, int nf,
                                                                  int32_t* fwd_order,
                                                                  const int32_t* bwd_range, int nb,
-                                                                 int32_t* bwd_order) {
+                                                                 int nkt, int32_t* bwd_order,
+                                                                 int np) {
   extern __shared__ unsigned long long keys[];
+  int32_t* scratch = reinterpret_cast<int32_t*>(keys + np);
   sort_desc(fwd_range, nf, fwd_order, keys);
-  sort_desc(bwd_range, nb, bwd_order, keys);
+  sort_bwd(bwd_range, nb, nkt, bwd_order, keys, scratch);
 }
 
 PlanPtrs plan_ptrs(void* plan, int B, int Hq, int Hkv, int L, int S, int seq_start) {
@@ -162,18 +165,18 @@ cudaError_t launch_plan(const int32_t* seg, const int32_t* seg_ids, const int32_
   const int nf = B * pl.NQB, nb = B * pl.NKT;
   int np = 1;
   while (np < max(nf, nb)) np <<= 1;
-  const size_t smem = sizeof(unsigned long long) * np;
+  const size_t smem = sizeof(unsigned long long) * np + sizeof(int32_t) * kSortThreads;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (smem > 48 * 1024 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(plan_sort_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(sizeof(unsigned long long) * kMaxListLen));
+    cudaError_t e = cudaFuncSetAttribute(
+        plan_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        static_cast<int>(sizeof(unsigned long long) * kMaxListLen + sizeof(int32_t) * kSortThreads));
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  plan_sort_kernel<<<1, kSortThreads, smem, stream>>>(fr, nf, fo, br, nb, bo);
+  plan_sort_kernel<<<1, kSortThreads, smem, stream>>>(fr, nf, fo, br, nb, pl.NKT, bo, np);
   return cudaGetLastError();
 }
 

@@ -41,27 +41,23 @@ __device__ __forceinline__ unsigned long long sort_key(const int32_t* range, int
 // of smaller keys, one comparison pass per entry.
 constexpr int kRankSortMax = 2048;
 
-// Sort a work list by cost (range length), longest first, ties by index, into
-// order[0..n).  Every thread of the block calls it; `keys` holds the next
-// power of two >= n entries of shared memory.
-__device__ inline void sort_desc(const int32_t* range, int n, int32_t* __restrict__ order,
-                                 unsigned long long* keys) {
-  if (n <= kRankSortMax) {
-    for (int i = threadIdx.x; i < n; i += blockDim.x) keys[i] = sort_key(range, i);
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const unsigned long long ki = keys[i];
-      int rank = 0;
-      for (int j = 0; j < n; ++j) rank += keys[j] < ki;
-      order[rank] = i;
-    }
-    __syncthreads();
-    return;
+// order[0..n) = the entries by ascending key (keys unique, the entry's index
+// in their low 32 bits).  Every thread of the block calls it.
+__device__ inline void rank_order(const unsigned long long* keys, int n,
+                                  int32_t* __restrict__ order) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const unsigned long long ki = keys[i];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) rank += keys[j] < ki;
+    order[rank] = i;
   }
-  int np = 1;
-  while (np < n) np <<= 1;
-  for (int i = threadIdx.x; i < np; i += blockDim.x) keys[i] = i < n ? sort_key(range, i) : ~0ull;
   __syncthreads();
+}
+
+// The same for longer lists: bitonic sort of keys[0..np) in place (np the next
+// power of two >= n, entries past n hold ~0).
+__device__ inline void bitonic_order(unsigned long long* keys, int n, int np,
+                                     int32_t* __restrict__ order) {
   for (int size = 2; size <= np; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       for (int i = threadIdx.x; i < np; i += blockDim.x) {
@@ -81,6 +77,95 @@ __device__ inline void sort_desc(const int32_t* range, int n, int32_t* __restric
   for (int i = threadIdx.x; i < n; i += blockDim.x)
     order[i] = static_cast<int32_t>(keys[i] & 0xffffffffu);
   __syncthreads();
+}
+
+// A backward unit (key tile) opens a run unless it continues the previous
+// tile's: same row, both non-empty, same last query tile.  The tiles of one
+// document form one run (a tile shared by two documents joins the later one,
+// whose last query tile it reaches).
+__device__ __forceinline__ bool bwd_run_head(const int32_t* range, int i, int nkt) {
+  const int lo = range[2 * i], hi = range[2 * i + 1];
+  if (hi < lo || i % nkt == 0) return true;
+  const int plo = range[2 * i - 2], phi = range[2 * i - 1];
+  return phi < plo || phi != hi;
+}
+
+// Keys of the backward work list: documents by size, largest first (the size
+// is the cost of the run's first, longest tile), each document's tiles
+// together and longest first, empty tiles last; ties by index.  Units running
+// side by side then share their Q/dO tiles and dq accumulator rows in L2
+// (on a workload of 32-512-token documents the backward main kernel took
+// 604 us in this order against 780 us longest-first).  The run heads come
+// from a block-wide prefix maximum: each thread scans a contiguous chunk,
+// then shuffles within warps and one pass over the warps' maxima (`scratch`:
+// 64 ints of shared memory; blockDim.x a multiple of 32, at most 1024).
+// Every thread of the block calls it.
+__device__ inline void fill_bwd_keys(const int32_t* range, int n, int nkt,
+                                     unsigned long long* keys, int32_t* scratch) {
+  const int T = blockDim.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int c = (n + T - 1) / T;
+  const int b0 = min(n, t * c), b1 = min(n, b0 + c);
+  int v = -1;  // the last run head in this thread's chunk
+  for (int i = b0; i < b1; ++i)
+    if (bwd_run_head(range, i, nkt)) v = i;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v = max(v, u);
+  }
+  if (lane == 31) scratch[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (T >> 5) ? scratch[lane] : -1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w = max(w, u);
+    }
+    scratch[32 + lane] = w;
+  }
+  __syncthreads();
+  const int carry = warp > 0 ? scratch[32 + warp - 1] : -1;
+  const int before = __shfl_up_sync(0xffffffffu, max(v, carry), 1);
+  int head = lane > 0 ? before : carry;
+  for (int i = b0; i < b1; ++i) {
+    if (bwd_run_head(range, i, nkt)) head = i;
+    const int lo = range[2 * i], hi = range[2 * i + 1];
+    const int size = hi < lo ? 0 : min(range[2 * head + 1] - range[2 * head] + 1, 0xFFFFF);
+    keys[i] = (static_cast<unsigned long long>(0xFFFFF - size) << 40) | static_cast<unsigned>(i);
+  }
+  __syncthreads();
+}
+
+// Sort the forward work list by cost (range length), longest first, ties by
+// index, into order[0..n).  Every thread of the block calls it; `keys` holds
+// the next power of two >= n entries of shared memory.
+__device__ inline void sort_desc(const int32_t* range, int n, int32_t* __restrict__ order,
+                                 unsigned long long* keys) {
+  int np = 1;
+  while (np < n) np <<= 1;
+  const int m = n <= kRankSortMax ? n : np;
+  for (int i = threadIdx.x; i < m; i += blockDim.x) keys[i] = i < n ? sort_key(range, i) : ~0ull;
+  __syncthreads();
+  if (n <= kRankSortMax)
+    rank_order(keys, n, order);
+  else
+    bitonic_order(keys, n, np, order);
+}
+
+// The backward work list in the order of fill_bwd_keys.
+__device__ inline void sort_bwd(const int32_t* range, int n, int nkt, int32_t* __restrict__ order,
+                                unsigned long long* keys, int32_t* scratch) {
+  int np = 1;
+  while (np < n) np <<= 1;
+  fill_bwd_keys(range, n, nkt, keys, scratch);
+  if (n <= kRankSortMax) {
+    rank_order(keys, n, order);
+    return;
+  }
+  for (int i = n + threadIdx.x; i < np; i += blockDim.x) keys[i] = ~0ull;
+  __syncthreads();
+  bitonic_order(keys, n, np, order);
 }
 
 // Document index d of position x in a row with boundaries c[0..n] (valid, x < c[n]):
@@ -226,12 +311,12 @@ __device__ inline void build_plan_cta(const int32_t* __restrict__ cu,
   }
   __threadfence_block();
   __syncthreads();
+  // the boundary cache is free from here on: it holds the run-head scan
   if (nf <= kRankSortMax && nb <= kRankSortMax) {
-    // both lists at once: one pass of loads, one barrier, then the ranks
+    // both lists' keys side by side, then their ranks in one pass
     unsigned long long* kb = keys + nf;
-    for (int i = threadIdx.x; i < nf + nb; i += blockDim.x)
-      keys[i] = i < nf ? sort_key(pp.fwd_range, i) : sort_key(pp.bwd_range, i - nf);
-    __syncthreads();
+    for (int i = threadIdx.x; i < nf; i += blockDim.x) keys[i] = sort_key(pp.fwd_range, i);
+    fill_bwd_keys(pp.bwd_range, nb, pp.NKT, kb, cu_cache);
     for (int i = threadIdx.x; i < nf + nb; i += blockDim.x) {
       const bool f = i < nf;
       const unsigned long long* ks = f ? keys : kb;
@@ -244,7 +329,7 @@ __device__ inline void build_plan_cta(const int32_t* __restrict__ cu,
     __syncthreads();
   } else {
     sort_desc(pp.fwd_range, nf, pp.fwd_order, keys);
-    sort_desc(pp.bwd_range, nb, pp.bwd_order, keys);
+    sort_bwd(pp.bwd_range, nb, pp.NKT, pp.bwd_order, keys, cu_cache);
   }
 }
 

@@ -1,4 +1,4 @@
-"""GPU plan (tile classifier + longest-first lists) against a brute-force mask.
+"""GPU plan (tile classifier + ordered work lists) against a brute-force mask.
 
 The expected values come from the oracle's segments and the per-document causal
 rule evaluated pair by pair; the plan buffer layout is the library's internal
@@ -97,7 +97,48 @@ def test_plan_matches_brute_force(cuda_lib, case):
                 assert (lo, hi) == (min(qts), max(qts))
             else:
                 assert hi < lo
-    for order, rng_ in ((sec["fo"], fr), (sec["bo"], br)):
-        assert sorted(order.tolist()) == list(range(order.size))
-        cost = np.maximum(0, rng_[order, 1] - rng_[order, 0] + 1)
-        assert np.all(np.diff(cost) <= 0), "work list is not longest-first"
+    fo, bo = sec["fo"], sec["bo"]
+    assert sorted(fo.tolist()) == list(range(fo.size))
+    cost = np.maximum(0, fr[fo, 1] - fr[fo, 0] + 1)
+    assert np.all(np.diff(cost) <= 0), "forward work list is not longest-first"
+    assert bo.tolist() == _document_order(br, NKT), "backward work list is not by document"
+
+
+def _document_order(br, NKT):
+    """Backward order: each document's key tiles together (a run of tiles of one
+    row reaching the same last query tile), longest first within it; documents
+    by the cost of their first tile, largest first; empty tiles last; ties by
+    index."""
+    keys, head = [], -1
+    for i, (lo, hi) in enumerate(br.tolist()):
+        plo, phi = br[i - 1].tolist() if i else (0, -1)
+        if hi < lo or i % NKT == 0 or phi < plo or phi != hi:
+            head = i
+        size = 0 if hi < lo else int(br[head, 1] - br[head, 0] + 1)
+        keys.append((-size, i))
+    return [i for _, i in sorted(keys)]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_single_call_plan_equals_planned(cuda_lib, case):
+    """The single-call forward builds its plan from the boundaries inside its
+    workspace (after a 256-byte record); every section but the work counters
+    must equal the plan built from segments."""
+    cus, S, Hq, Hkv, L, s0 = CASES[case]
+    B = len(cus)
+    ids = np.stack([orc.doc_ids_from_cu_seqlens(c, S) for c in cus])
+    seg, sid, nseg = A.segment_cu_seqlens(torch.from_numpy(ids).cuda())
+    plan = A.make_plan(seg, sid, nseg, Hq, Hkv, L, s0)
+    g = torch.Generator().manual_seed(case)
+    D = 64
+    q = torch.randn((B, Hq, L, D), generator=g).to(torch.bfloat16).cuda()
+    k = torch.randn((B, Hkv, S, D), generator=g).to(torch.bfloat16).cuda()
+    v = torch.randn((B, Hkv, S, D), generator=g).to(torch.bfloat16).cuda()
+    cu, rp = A.cu_csr(cus, "cuda")
+    _, _, ws = A.attn_forward_cu(q, k, v, cu, rp, s0, None, Hq != Hkv)
+    A.check_device_status()
+    off, *_ = _layout(B, Hq, Hkv, L, S)
+    planned = plan.cpu().numpy().view(np.int32)
+    single = ws.cpu().numpy()[256:256 + plan.numel()].view(np.int32)
+    for name, (o, n) in off.items():
+        assert np.array_equal(single[o // 4:o // 4 + n], planned[o // 4:o // 4 + n]), name
