@@ -151,8 +151,10 @@ int bd_kv_needed_range(const int32_t* seg, const int32_t* seg_ids, const int32_t
 
 /*
  * Attention plan: per-row mask bounds, the non-empty tile ranges of every
- * query block (forward) and key tile (backward), and both work lists sorted
- * longest-first.  This is the "varlen metadata precompute" that the page
+ * query block (forward) and key tile (backward), and both work lists in the
+ * order the kernels take them (the forward's longest first; the backward's by
+ * document, largest first, each document's tiles together and longest first).
+ * This is the "varlen metadata precompute" that the page
  * "nemo_automodel.components.distributed.blockdiag_cp" names as an internal
  * detail.  Built on the device from the output of bd_segment_cu_seqlens,
  * with no host synchronisation.
@@ -164,7 +166,7 @@ int bd_kv_needed_range(const int32_t* seg, const int32_t* seg_ids, const int32_t
  *                       aligned, used by bd_attn_fwd_planned / bd_attn_bwd_planned, which must
  *                       be given the same B, Hq, Hkv, L, S, seq_start.  It also
  *                       holds the work counters those kernels take units from
- *                       (longest first) and leave at zero when they finish, so
+ *                       (in the lists' order) and leave at zero when they finish, so
  *                       one plan must not serve two launches that overlap in
  *                       time (use one plan per stream).
  * Returns BD_ERR_UNSUPPORTED when B * ceil(L/128) or B * ceil(S/128)
@@ -200,7 +202,7 @@ int bd_attn_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg
  *                scaled scores of each row (-inf for padding rows).
  *   workspace    device scratch of bd_attn_workspace_size() bytes, 256-byte
  *                aligned, owned by the caller.  The call keeps there the
- *                attention plan (mask bounds and longest-first work lists),
+ *                attention plan (mask bounds and ordered work lists),
  *                an fp16 copy of v (the P V product runs with fp16 operands:
  *                v must lie within the fp16 range, |x| <= 65504), and the
  *                rounding residual of out, with a record of the shapes and

@@ -1,5 +1,5 @@
-// Attention plan: mask bounds per row, non-empty tile ranges, longest-first
-// work lists.
+// Attention plan: mask bounds per row, non-empty tile ranges, ordered work
+// lists (the forward's longest first, the backward's by document).
 //
 // The mask is the per-document causal rule of cp_blockdiag_sdpa (page
 // "nemo_automodel.components.distributed.blockdiag_cp"): the query at global

@@ -1,5 +1,5 @@
 // Device helpers of the attention plan: binary searches over a row's
-// boundaries, the longest-first sort of the work lists, and the one-CTA plan
+// boundaries, the ordering of the work lists, and the one-CTA plan
 // builder that works straight from cumulative document boundaries.
 //
 // The mask is the per-document causal rule of cp_blockdiag_sdpa (page
@@ -204,7 +204,7 @@ constexpr int kPlanCuCache = 4096;
 // bd_doc_ids_from_cu_seqlens: row b's list is cu[row_ptr[b] .. row_ptr[b+1]-1]).
 // A row whose list does not start at 0, decreases, or ends past S is planned
 // as all padding and BD_ERR_INVALID_ARG goes to *status, as its ids would be
-// all 0.  Writes qlo, kend, both tile ranges, both longest-first orders and
+// all 0.  Writes qlo, kend, both tile ranges, both work-list orders and
 // zeroes the work counters.  Every thread of the block calls it; `keys` is
 // the sort's shared memory, `bad_rows` one bit per row (B <= 32 * bad_words),
 // `cu_cache` kPlanCuCache entries of shared memory.

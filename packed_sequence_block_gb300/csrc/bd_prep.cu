@@ -1,7 +1,7 @@
 // First launches of the single-call forward and backward (bd_attn_fwd and
 // bd_attn_bwd, which take cumulative document boundaries).  Each is one
 // launch whose block 0 builds the attention plan from the boundaries (the
-// mask bounds of every row and the longest-first work lists, see
+// mask bounds of every row and the ordered work lists, see
 // bd_plan_dev.cuh) while the other blocks do the pass over HBM that the call
 // needs anyway: the fp16 copy of v before the forward, the per-row terms
 // before the backward.
