@@ -3,10 +3,11 @@
 
 One step = the whole path on one synthetic packed batch, every call through
 the C ABI's single-call entry points: bd_attn_fwd (the plan -- mask bounds
-and longest-first tile lists -- from cu_seqlens, the fp16 copy of v, the
-forward kernel) then bd_attn_bwd (the plan again with the per-row terms, the
-main kernel, the dq conversion), for every query interval.  Default workload: 1 row x 8192 tokens, Hq=32, Hkv=8, D=128,
-lognormal(1024, 1.0) document lengths (seed 0).
+and ordered tile lists -- from cu_seqlens, the fp16 copy of v, the forward
+kernel) then bd_attn_bwd (the per-row terms with the forward's plan reused,
+the main kernel, the dq conversion), for every query interval.  Default
+workload: 1 row x 8192 tokens, Hq=32, Hkv=8, D=128, lognormal(1024, 1.0)
+document lengths (seed 0).
 
 Metric: useful TFLOP/s = 14 * D * (unmasked query/key pairs) * Hq per step
 (4*D forward + 10*D backward per pair and query head) over the step time;
