@@ -195,6 +195,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ d
 //
 // Per iteration i (query tile x head of the unit's group), TMEM columns:
 //   dK [0,128)  dV [128,256)  S^T -> P^T [256,384)  dP^T -> dQ [384,512)
+// (at D = 64 dQ has columns of its own, [64,128), beside dK)
 // Tensor-core order (one thread):
 //   dV += P^T_i dO_i | S^T_{i+1} | dK += dS^T_i Q_i | dQ_i = dS_i K | dP^T_{i+1}
 // so that the P/dS work overlaps MMAs: dS_i is formed while dV_i and S^T_{i+1}
@@ -358,6 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sdo0 = smem_u32(smem + C::OFF_DO);
       const uint32_t sds = smem_u32(smem + C::OFF_DS);
       const uint32_t tDK = tmem, tDV = tmem + 128, tS = tmem + 256, tDP = tmem + 384;
+      // At D = 64 dQ has columns of its own ([64, 128), beside dK), so dP^T_{i+1}
+      // need not wait for dQ_i to be read out; at D = 128 it shares dP^T's.
+      constexpr bool kOwnDQ = D == 64;
+      const uint32_t tDQ = kOwnDQ ? tmem + 64 : tDP;
       // D[128 keys, 128 queries] = A[keys, D] (K-major) * B[queries, D]^T (K-major)
       // Each operand's descriptor is built once per product and stepped by a
       // constant per instruction (sdesc_add), and every step but the first
@@ -408,9 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           if (ks == 0)
-            mma_ss(tDP, ad, bd, C::IDESC_DQ, 0);
+            mma_ss(tDQ, ad, bd, C::IDESC_DQ, 0);
           else
-            mma_ss_acc(tDP, sdesc_add(ad, ks * 2048), sdesc_add(bd, ks * 2048), C::IDESC_DQ);
+            mma_ss_acc(tDQ, sdesc_add(ad, ks * 2048), sdesc_add(bd, ks * 2048), C::IDESC_DQ);
         }
       };
       uint32_t kv_u = 0, st_it = 0, it_g = 0, kq = 0;
@@ -428,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         issue_kmajor(tS, sk, sq0 + st * C::TILE, C::IDESC_S);
         mma_commit(s_full);
-        if (it_g > 0) {  // the previous iteration's dQ must have left the dP columns
+        if (!kOwnDQ && it_g > 0) {  // the previous iteration's dQ must have left the dP columns
           ok = mbar_wait(dq_empty, (it_g - 1) & 1, abort_flag, p.status);
           if (!ok) break;
         }
@@ -459,11 +464,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_dk(sq0 + st * C::TILE, i > 0);
           mma_commit(st_empty + st);  // Q_i is no longer read after dK_i
+          if (kOwnDQ && it_g > 0) {  // the previous dQ must have been read out of its columns
+            ok = mbar_wait(dq_empty, (it_g - 1) & 1, abort_flag, p.status);
+            if (!ok) break;
+          }
           issue_dq();
           mma_commit(dq_full);
           if (more) {
-            ok = mbar_wait(dq_empty, it_g & 1, abort_flag, p.status);
-            if (!ok) break;
+            if (!kOwnDQ) {
+              ok = mbar_wait(dq_empty, it_g & 1, abort_flag, p.status);
+              if (!ok) break;
+            }
             ok = mbar_wait(do_full, (si + 1) & 1, abort_flag, p.status);
             if (!ok) break;
             tc_fence_after();
@@ -712,7 +723,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rg = (warp - 12) >> 2;
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;  // query row of the tile = TMEM lane
-    const uint32_t tQ = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + 384 + 64 * rg;
+    const uint32_t tQ =
+        tmem + (static_cast<uint32_t>(q4 * 32) << 16) + (D == 64 ? 64 : 384) + 64 * rg;
     const uint32_t srow = smem_u32(smem + C::OFF_STG) + r * 128;
     constexpr uint32_t kBoxes = D / 32;  // boxes per dQ tile
     const bool active = 64 * rg < D;
