@@ -204,9 +204,10 @@ int bd_attn_plan(const int32_t* seg, const int32_t* seg_ids, const int32_t* nseg
  *                aligned, owned by the caller.  The call keeps there the
  *                attention plan (mask bounds and ordered work lists),
  *                an fp16 copy of v (the P V product runs with fp16 operands:
- *                v must lie within the fp16 range, |x| <= 65504), and the
- *                rounding residual of out, with a record of the shapes and
- *                of out and lse.  Too small: BD_ERR_WORKSPACE.
+ *                v must lie within the fp16 range, |x| <= 65504), and an
+ *                fp16 copy of the result O for the backward, with a record
+ *                of the shapes and of out and lse.  Too small:
+ *                BD_ERR_WORKSPACE.
  * Validation on the host: B, Hq, Hkv, L, S >= 1, Hq % Hkv == 0, the interval
  * inside the row, 16-byte aligned q, k, v, out, and B * ceil(L/128),
  * B * ceil(S/128) <= 16384 (else BD_ERR_UNSUPPORTED).
@@ -226,11 +227,11 @@ int bd_attn_fwd(const void* q, const void* k, const void* v, int B, int Hq, int 
  *   dk, dv       bf16 [B, Hkv, S, D] outputs, summed over the query heads of
  *                each group; fully overwritten (rows no query attends are 0).
  *   workspace    bd_attn_workspace_size() bytes.  The plan is rebuilt from
- *                the boundaries.  Delta_i = <dO_i, O_i> takes O from out plus
- *                the residual the forward kept in the workspace when the
- *                workspace still records this out and lse with these shapes
- *                (pass the workspace of the forward call, untouched in
- *                between, for full precision); otherwise from out alone.
+ *                the boundaries.  Delta_i = <dO_i, O_i> takes O from the fp16
+ *                copy the forward kept in the workspace when the workspace
+ *                still records this out and lse with these shapes (pass the
+ *                workspace of the forward call, untouched in between, for
+ *                full precision); otherwise from the bf16 out.
  * The dq accumulation uses floating-point atomics, so dq may differ in the
  * last bits between runs; dk and dv are deterministic.  All five products
  * (K Q^T, V dO^T, P^T dO, dS^T Q, dS K) take bf16 operands with fp32
@@ -303,10 +304,12 @@ int bd_attn_bwd_dropout(const void* q, const void* k, const void* v, const void*
  * repeat after a gap: the mask then follows the segments of the ids).  Same
  * operation, arguments and results as the calls above, with
  *   plan         from bd_attn_plan with the same B, Hq, Hkv, L, S, seq_start.
- *   out_lo       forward: optional bf16 [B, Hq, L, D] output (NULL to skip),
- *                the rounding residual bf16(O - out) of the fp32 result O, so
- *                that out + out_lo carries O to about 16 significant bits;
- *                backward: that residual, or NULL (Delta from out alone).
+ *   out16        forward: optional fp16 [B, Hq, L, D] output (NULL to skip):
+ *                the fp32 result O rounded to fp16 (11 significant bits
+ *                against out's 8), without the dropout factor 1 / (1 - p),
+ *                so that its entries lie within the range of v; backward:
+ *                that output of the forward with the same dropout_p (Delta
+ *                from it, times 1 / (1 - p)), or NULL (Delta from out).
  *   workspace    forward: bd_attn_fwd_planned_workspace_size() bytes (the
  *                fp16 copy of v); backward:
  *                bd_attn_bwd_planned_workspace_size() bytes (the fp32 dq
@@ -316,24 +319,24 @@ int bd_attn_bwd_dropout(const void* q, const void* k, const void* v, const void*
 size_t bd_attn_fwd_planned_workspace_size(int B, int Hkv, int S, int D);
 int bd_attn_fwd_planned(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
                         int L, int S, int D, int seq_start, float scale, int enable_gqa,
-                        void* plan, size_t plan_bytes, void* out, float* lse, void* out_lo,
+                        void* plan, size_t plan_bytes, void* out, float* lse, void* out16,
                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
                         bd_stream_t stream);
 int bd_attn_fwd_dropout_planned(const void* q, const void* k, const void* v, int B, int Hq,
                                 int Hkv, int L, int S, int D, int seq_start, float scale,
                                 int enable_gqa, void* plan, size_t plan_bytes, void* out,
-                                float* lse, void* out_lo, void* workspace, size_t workspace_bytes,
+                                float* lse, void* out16, void* workspace, size_t workspace_bytes,
                                 double dropout_p, uint64_t seed, uint32_t offset,
                                 int32_t* dev_status, bd_stream_t stream);
 size_t bd_attn_bwd_planned_workspace_size(int B, int Hq, int Hkv, int L, int S, int D);
 int bd_attn_bwd_planned(const void* q, const void* k, const void* v, const void* out,
-                        const void* out_lo, const float* lse, const void* dout, int B, int Hq,
+                        const void* out16, const float* lse, const void* dout, int B, int Hq,
                         int Hkv, int L, int S, int D, int seq_start, float scale, int enable_gqa,
                         void* plan, size_t plan_bytes, void* dq, void* dk, void* dv,
                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
                         bd_stream_t stream);
 int bd_attn_bwd_dropout_planned(const void* q, const void* k, const void* v, const void* out,
-                                const void* out_lo, const float* lse, const void* dout, int B,
+                                const void* out16, const float* lse, const void* dout, int B,
                                 int Hq, int Hkv, int L, int S, int D, int seq_start, float scale,
                                 int enable_gqa, void* plan, size_t plan_bytes, void* dq,
                                 void* dk, void* dv, void* workspace, size_t workspace_bytes,
@@ -363,7 +366,7 @@ int bd_attn_bwd_dropout_planned(const void* q, const void* k, const void* v, con
  */
 #define BD_NOALLOC_SCRATCH_BYTES (16u << 20)
 int bd_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
-                        const void* out_lo, const float* lse, const void* dout, int B, int Hq,
+                        const void* out16, const float* lse, const void* dout, int B, int Hq,
                         int Hkv, int L, int S, int D, int seq_start, float scale, int enable_gqa,
                         void* plan, size_t plan_bytes, void* dq, void* dk, void* dv,
                         int32_t* dev_status, bd_stream_t stream);

@@ -299,29 +299,29 @@ def bd_attn_fwd_planned_workspace_size(B: int, Hkv: int, S: int, D: int) -> int:
 
 def bd_attn_fwd_planned(q, k, v, B: int, Hq: int, Hkv: int, L: int, S: int, D: int,
                         seq_start: int, scale: float, enable_gqa: bool, plan, out, lse,
-                        out_lo=None, workspace=None, dev_status=None, stream=None) -> None:
+                        out16=None, workspace=None, dev_status=None, stream=None) -> None:
     _want_all(((q, "q"), (k, "k"), (v, "v"), (out, "out")), torch.bfloat16)
-    if out_lo is not None:
-        _want(out_lo, torch.bfloat16, "out_lo")
+    if out16 is not None:
+        _want(out16, torch.float16, "out16")
     _want(lse, torch.float32, "lse")
     _check(lib().bd_attn_fwd_planned(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, L, S, D, seq_start,
                                      float(scale), int(bool(enable_gqa)), _ptr(plan),
-                                     _nbytes(plan), _ptr(out), _ptr(lse), _ptr(out_lo),
+                                     _nbytes(plan), _ptr(out), _ptr(lse), _ptr(out16),
                                      _ptr(workspace), _nbytes(workspace), _ptr(dev_status),
                                      _stream(stream)), "bd_attn_fwd_planned")
 
 
 def bd_attn_fwd_dropout_planned(q, k, v, B: int, Hq: int, Hkv: int, L: int, S: int, D: int,
                                 seq_start: int, scale: float, enable_gqa: bool, plan, out, lse,
-                                dropout_p: float, seed: int, offset: int = 0, out_lo=None,
+                                dropout_p: float, seed: int, offset: int = 0, out16=None,
                                 workspace=None, dev_status=None, stream=None) -> None:
     _want_all(((q, "q"), (k, "k"), (v, "v"), (out, "out")), torch.bfloat16)
-    if out_lo is not None:
-        _want(out_lo, torch.bfloat16, "out_lo")
+    if out16 is not None:
+        _want(out16, torch.float16, "out16")
     _want(lse, torch.float32, "lse")
     _check(lib().bd_attn_fwd_dropout_planned(
         _ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, L, S, D, seq_start, float(scale),
-        int(bool(enable_gqa)), _ptr(plan), _nbytes(plan), _ptr(out), _ptr(lse), _ptr(out_lo),
+        int(bool(enable_gqa)), _ptr(plan), _nbytes(plan), _ptr(out), _ptr(lse), _ptr(out16),
         _ptr(workspace), _nbytes(workspace), float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF,
         int(offset) & 0xFFFFFFFF, _ptr(dev_status), _stream(stream)),
         "bd_attn_fwd_dropout_planned")
@@ -333,11 +333,13 @@ def bd_attn_bwd_planned_workspace_size(B: int, Hq: int, Hkv: int, L: int, S: int
 
 def bd_attn_bwd_planned(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: int,
                         D: int, seq_start: int, scale: float, enable_gqa: bool, plan, dq, dk, dv,
-                        workspace, out_lo=None, dev_status=None, stream=None) -> None:
+                        workspace, out16=None, dev_status=None, stream=None) -> None:
     _want_all(((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"),
                (dk, "dk"), (dv, "dv")), torch.bfloat16)
     _want(lse, torch.float32, "lse")
-    _check(lib().bd_attn_bwd_planned(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo),
+    if out16 is not None:
+        _want(out16, torch.float16, "out16")
+    _check(lib().bd_attn_bwd_planned(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out16),
                                      _ptr(lse), _ptr(dout), B, Hq, Hkv, L, S, D, seq_start,
                                      float(scale), int(bool(enable_gqa)), _ptr(plan),
                                      _nbytes(plan), _ptr(dq), _ptr(dk), _ptr(dv),
@@ -348,13 +350,15 @@ def bd_attn_bwd_planned(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: i
 def bd_attn_bwd_dropout_planned(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int,
                                 S: int, D: int, seq_start: int, scale: float, enable_gqa: bool,
                                 plan, dq, dk, dv, workspace, dropout_p: float, seed: int,
-                                offset: int = 0, out_lo=None, dev_status=None,
+                                offset: int = 0, out16=None, dev_status=None,
                                 stream=None) -> None:
     _want_all(((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"),
                (dk, "dk"), (dv, "dv")), torch.bfloat16)
     _want(lse, torch.float32, "lse")
+    if out16 is not None:
+        _want(out16, torch.float16, "out16")
     _check(lib().bd_attn_bwd_dropout_planned(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo), _ptr(lse), _ptr(dout), B, Hq, Hkv,
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out16), _ptr(lse), _ptr(dout), B, Hq, Hkv,
         L, S, D, seq_start, float(scale), int(bool(enable_gqa)), _ptr(plan), _nbytes(plan),
         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), _nbytes(workspace), float(dropout_p),
         int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF, _ptr(dev_status),
@@ -363,7 +367,7 @@ def bd_attn_bwd_dropout_planned(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: i
 
 def bd_attn_bwd_noalloc(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: int, S: int,
                         D: int, seq_start: int, scale: float, enable_gqa: bool, plan, dq, dk, dv,
-                        out_lo=None, dev_status=None, stream=None) -> None:
+                        out16=None, dev_status=None, stream=None) -> None:
     """bd_attn_bwd_planned without a workspace argument: the library's own fixed scratch is used.
 
     For callers that cannot allocate device memory.  Problems whose workspace
@@ -374,7 +378,9 @@ def bd_attn_bwd_noalloc(q, k, v, out, lse, dout, B: int, Hq: int, Hkv: int, L: i
                  (dk, "dk"), (dv, "dv")):
         _want(t, torch.bfloat16, n)
     _want(lse, torch.float32, "lse")
-    _check(lib().bd_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo),
+    if out16 is not None:
+        _want(out16, torch.float16, "out16")
+    _check(lib().bd_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out16),
                                      _ptr(lse), _ptr(dout), B, Hq, Hkv, L, S, D, seq_start,
                                      float(scale), int(bool(enable_gqa)), _ptr(plan),
                                      _nbytes(plan), _ptr(dq), _ptr(dk),

@@ -94,12 +94,13 @@ def _resolve_scale(scale, D):
     return float(D) ** -0.5 if scale is None else float(scale)
 
 
-def attn_forward(q, k, v, plan, seq_start=0, scale=None, enable_gqa=False, residual=True,
+def attn_forward(q, k, v, plan, seq_start=0, scale=None, enable_gqa=False, keep_o16=True,
                  workspace=None, dropout_p: float = 0.0, seed: int = 0, offset: int = 0):
-    """out [B,Hq,L,D] bf16, lse [B,Hq,L] fp32 and the rounding residual of out (no autograd).
+    """out [B,Hq,L,D] bf16, lse [B,Hq,L] fp32 and an fp16 copy of O (no autograd).
 
-    The residual (bf16, same shape as out, or None when ``residual`` is
-    False) lets the backward form Delta = <dout, O> from O at ~16 bits.
+    The fp16 copy (same shape as out, without the dropout factor 1 / (1 - p);
+    None when ``keep_o16`` is False) lets the backward form Delta = <dout, O>
+    from O at 11 significant bits instead of out's 8.
     ``workspace`` (uint8, at least bd_attn_fwd_planned_workspace_size bytes) is
     allocated here when not given.  ``dropout_p`` > 0 drops attention weights
     with the counter-based mask of (seed, offset); the backward must be given
@@ -111,22 +112,22 @@ def attn_forward(q, k, v, plan, seq_start=0, scale=None, enable_gqa=False, resid
         workspace = torch.empty(N.bd_attn_fwd_planned_workspace_size(B, Hkv, S, D),
                                 dtype=torch.uint8, device=q.device)
     out = torch.empty_like(q)
-    out_lo = torch.empty_like(q) if residual else None
+    out16 = torch.empty_like(q, dtype=torch.float16) if keep_o16 else None
     lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device)
     if dropout_p != 0.0:  # the library rejects p outside [0, 1)
         N.bd_attn_fwd_dropout_planned(q, k, v, B, Hq, Hkv, L, S, D, seq_start,
                                       _resolve_scale(scale, D), enable_gqa, plan, out, lse,
-                                      dropout_p, seed, offset, out_lo, workspace,
+                                      dropout_p, seed, offset, out16, workspace,
                                       device_status_word(q.device))
     else:
         N.bd_attn_fwd_planned(q, k, v, B, Hq, Hkv, L, S, D, seq_start, _resolve_scale(scale, D),
-                              enable_gqa, plan, out, lse, out_lo, workspace,
+                              enable_gqa, plan, out, lse, out16, workspace,
                               device_status_word(q.device))
-    return out, lse, out_lo
+    return out, lse, out16
 
 
 def attn_backward(q, k, v, out, lse, dout, plan, seq_start=0, scale=None, enable_gqa=False,
-                  workspace=None, out_lo=None, dropout_p: float = 0.0, seed: int = 0,
+                  workspace=None, out16=None, dropout_p: float = 0.0, seed: int = 0,
                   offset: int = 0):
     """dq, dk, dv (bf16) for the forward above (no autograd)."""
     B, Hq, L, D = q.shape
@@ -140,12 +141,12 @@ def attn_backward(q, k, v, out, lse, dout, plan, seq_start=0, scale=None, enable
     if dropout_p != 0.0:
         N.bd_attn_bwd_dropout_planned(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, seq_start,
                                       _resolve_scale(scale, D), enable_gqa, plan, dq, dk, dv,
-                                      workspace, dropout_p, seed, offset, out_lo,
+                                      workspace, dropout_p, seed, offset, out16,
                                       device_status_word(q.device))
     else:
         N.bd_attn_bwd_planned(q, k, v, out, lse, dout, B, Hq, Hkv, L, S, D, seq_start,
                               _resolve_scale(scale, D), enable_gqa, plan, dq, dk, dv, workspace,
-                              out_lo, device_status_word(q.device))
+                              out16, device_status_word(q.device))
     return dq, dk, dv
 
 
@@ -162,7 +163,7 @@ def attn_forward_cu(q, k, v, cu_seqlens, row_ptr, seq_start=0, scale=None, enabl
 
     ``cu_seqlens`` / ``row_ptr`` are the int32 device tensors of ``cu_csr``.  The
     workspace (bd_attn_workspace_size bytes, allocated here when not given)
-    carries the plan and the rounding residual of out to ``attn_backward_cu``.
+    carries the plan and the fp16 copy of O to ``attn_backward_cu``.
     """
     B, Hq, L, D = q.shape
     Hkv, S = k.shape[1], k.shape[2]
@@ -210,19 +211,19 @@ class BlockdiagAttention(torch.autograd.Function):
     def forward(ctx, q, k, v, plan, seq_start, scale, enable_gqa, dropout_p=0.0, seed=0,
                 offset=0):
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
-        out, lse, out_lo = attn_forward(q, k, v, plan, seq_start, scale, enable_gqa,
+        out, lse, out16 = attn_forward(q, k, v, plan, seq_start, scale, enable_gqa,
                                         dropout_p=dropout_p, seed=seed, offset=offset)
-        ctx.save_for_backward(q, k, v, out, lse, plan, out_lo)
+        ctx.save_for_backward(q, k, v, out, lse, plan, out16)
         ctx.args = (seq_start, scale, enable_gqa, dropout_p, seed, offset)
         ctx.mark_non_differentiable(lse)
         return out, lse
 
     @staticmethod
     def backward(ctx, dout, _dlse):
-        q, k, v, out, lse, plan, out_lo = ctx.saved_tensors
+        q, k, v, out, lse, plan, out16 = ctx.saved_tensors
         seq_start, scale, enable_gqa, dropout_p, seed, offset = ctx.args
         dq, dk, dv = attn_backward(q, k, v, out, lse, dout.contiguous(), plan, seq_start, scale,
-                                   enable_gqa, out_lo=out_lo, dropout_p=dropout_p, seed=seed,
+                                   enable_gqa, out16=out16, dropout_p=dropout_p, seed=seed,
                                    offset=offset)
         return dq, dk, dv, None, None, None, None, None, None, None
 

@@ -145,7 +145,8 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int planes, int rows, in
   return make_tmap_16bit(map, base, planes, rows, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 }
 
-bool make_tmap_out(CUtensorMap* map, const void* base, int planes, int rows, int D) {
+bool make_tmap_out(CUtensorMap* map, const void* base, int planes, int rows, int D,
+                   CUtensorMapDataType type) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
   if (enc == nullptr) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
@@ -154,7 +155,7 @@ bool make_tmap_out(CUtensorMap* map, const void* base, int planes, int rows, int
                            static_cast<cuuint64_t>(rows) * D * 2};
   cuuint32_t box[3] = {32, 32, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+  CUresult r = enc(map, type, 3, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -299,19 +300,21 @@ int check_attn_args(const void* q, const void* k, const void* v, int B, int Hq, 
 // The forward kernel on a built plan, v16 holding (or about to hold) the fp16 copy of v.
 int fwd_run(const void* q, const void* k, int B, int Hq, int Hkv, int L, int S, int D,
             int seq_start, float scale, void* plan, void* v16, void* out, float* lse,
-            void* out_lo, const DropoutArgs& drop, int32_t* dev_status, int sms,
+            void* out16, const DropoutArgs& drop, int32_t* dev_status, int sms,
             cudaStream_t stream, void* acc = nullptr, size_t acc_bytes = 0,
             uint32_t* acc_flags = nullptr) {
   AttnDims d = resolve(B, Hq, Hkv, L, S, D, seq_start, scale);
   d.drop = drop;
-  CUtensorMap tq, tk, tv, to, tol;
-  if (!make_tmap_out(&to, out, B * Hq, L, D) ||
-      !make_tmap_out(&tol, out_lo != nullptr ? out_lo : out, B * Hq, L, D))
+  CUtensorMap tq, tk, tv, to, to16;
+  // (without out16 its map is never used; it then describes out)
+  if (!make_tmap_out(&to, out, B * Hq, L, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) ||
+      !make_tmap_out(&to16, out16 != nullptr ? out16 : out, B * Hq, L, D,
+                     CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
     return BD_ERR_CUDA;
   if (!make_tmap_bf16(&tq, q, B * Hq, L, D) || !make_tmap_bf16(&tk, k, B * Hkv, S, D) ||
       !make_tmap_f16(&tv, v16, B * Hkv, S, D))
     return BD_ERR_CUDA;
-  return launch_fwd(tq, tk, tv, to, tol, d, plan, out, out_lo, lse, dev_status, sms, stream, acc,
+  return launch_fwd(tq, tk, tv, to, to16, d, plan, out, out16, lse, dev_status, sms, stream, acc,
                     acc_bytes, acc_flags) == cudaSuccess
              ? BD_OK
              : BD_ERR_CUDA;
@@ -319,12 +322,12 @@ int fwd_run(const void* q, const void* k, int B, int Hq, int Hkv, int L, int S, 
 
 int fwd_planned_impl(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int L,
                      int S, int D, int seq_start, float scale, int enable_gqa, void* plan,
-                     size_t plan_bytes, void* out, float* lse, void* out_lo, void* workspace,
+                     size_t plan_bytes, void* out, float* lse, void* out16, void* workspace,
                      size_t workspace_bytes, const DropoutArgs& drop, int32_t* dev_status,
                      cudaStream_t stream) {
   if (plan == nullptr || out == nullptr || lse == nullptr || workspace == nullptr)
     return BD_ERR_INVALID_ARG;
-  if (out_lo != nullptr && !aligned(out_lo, 16)) return BD_ERR_INVALID_ARG;
+  if (out16 != nullptr && !aligned(out16, 16)) return BD_ERR_INVALID_ARG;
   int st = check_attn_args(q, k, v, B, Hq, Hkv, L, S, D, seq_start, enable_gqa);
   if (st != BD_OK) return st;
   if (!aligned(out, 16) || !aligned(lse, 4) || !aligned(plan, 256) || !aligned(workspace, 256))
@@ -336,7 +339,7 @@ int fwd_planned_impl(const void* q, const void* k, const void* v, int B, int Hq,
   // the P V product reads v through its fp16 copy in the workspace
   if (launch_v_to_f16(v, workspace, (long long)B * Hkv * S * D, sms, stream) != cudaSuccess)
     return BD_ERR_CUDA;
-  return fwd_run(q, k, B, Hq, Hkv, L, S, D, seq_start, scale, plan, workspace, out, lse, out_lo,
+  return fwd_run(q, k, B, Hq, Hkv, L, S, D, seq_start, scale, plan, workspace, out, lse, out16,
                  drop, dev_status, sms, stream);
 }
 
@@ -383,13 +386,13 @@ int fwd_cu_impl(const void* q, const void* k, const void* v, int B, int Hq, int 
     return BD_ERR_CUDA;
   // the forward's idle warps zero the backward's dq accumulator in the same workspace
   return fwd_run(q, k, B, Hq, Hkv, L, S, D, seq_start, scale, ws + wl.plan_off, ws + wl.v16, out,
-                 lse, ws + wl.out_lo, drop, dev_status, sms, stream,
+                 lse, ws + wl.out16, drop, dev_status, sms, stream,
                  ws + wl.bwd_off + wl.bwd.dqacc, sizeof(float) * (size_t)B * Hq * L * D,
                  &hdr->flags);
 }
 
 // The backward stages on a plan; `prep` set for the single-call form.
-int bwd_run(const void* q, const void* k, const void* v, const void* out, const void* out_lo,
+int bwd_run(const void* q, const void* k, const void* v, const void* out, const void* out16,
             const float* lse, const void* dout, int B, int Hq, int Hkv, int L, int S, int D,
             int seq_start, float scale, void* plan, void* dq, void* dk, void* dv, void* bwd_ws,
             const DropoutArgs& drop, int32_t* dev_status, int stages, const BwdPrep* prep,
@@ -405,7 +408,7 @@ int bwd_run(const void* q, const void* k, const void* v, const void* out, const 
     return BD_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return BD_ERR_CUDA;
-  return launch_bwd(tq, tk, tv, tdo, tdq, d, plan, out, out_lo, lse, dout, dq, dk, dv, bwd_ws,
+  return launch_bwd(tq, tk, tv, tdo, tdq, d, plan, out, out16, lse, dout, dq, dk, dv, bwd_ws,
                     dev_status, stages, sms, stream, prep) == cudaSuccess
              ? BD_OK
              : BD_ERR_CUDA;
@@ -423,13 +426,13 @@ int check_bwd_ptrs(const void* out, const float* lse, const void* dout, void* dq
 }
 
 int bwd_planned_impl(const void* q, const void* k, const void* v, const void* out,
-                     const void* out_lo, const float* lse, const void* dout, int B, int Hq,
+                     const void* out16, const float* lse, const void* dout, int B, int Hq,
                      int Hkv, int L, int S, int D, int seq_start, float scale, int enable_gqa,
                      void* plan, size_t plan_bytes, void* dq, void* dk, void* dv,
                      void* workspace, size_t workspace_bytes, const DropoutArgs& drop,
                      int32_t* dev_status, cudaStream_t stream) {
   if (plan == nullptr) return BD_ERR_INVALID_ARG;
-  if (out_lo != nullptr && !aligned(out_lo, 16)) return BD_ERR_INVALID_ARG;
+  if (out16 != nullptr && !aligned(out16, 16)) return BD_ERR_INVALID_ARG;
   int st = check_attn_args(q, k, v, B, Hq, Hkv, L, S, D, seq_start, enable_gqa);
   if (st != BD_OK) return st;
   st = check_bwd_ptrs(out, lse, dout, dq, dk, dv, workspace);
@@ -437,7 +440,7 @@ int bwd_planned_impl(const void* q, const void* k, const void* v, const void* ou
   if (!aligned(plan, 256)) return BD_ERR_INVALID_ARG;
   if (plan_bytes < plan_layout(B, Hq, Hkv, L, S).total) return BD_ERR_WORKSPACE;
   if (workspace_bytes < bwd_layout(B, Hq, Hkv, L, S, D).total) return BD_ERR_WORKSPACE;
-  return bwd_run(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale, plan, dq,
+  return bwd_run(q, k, v, out, out16, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale, plan, dq,
                  dk, dv, workspace, drop, dev_status, kBwdPrepare | kBwdMain | kBwdFinish,
                  nullptr, stream);
 }
@@ -463,7 +466,7 @@ int bwd_cu_impl(const void* q, const void* k, const void* v, const void* out, co
   prep.pp = plan_ptrs(ws + wl.plan_off, B, Hq, Hkv, L, S, seq_start);
   prep.hdr = reinterpret_cast<WsTag*>(ws + wl.hdr);
   prep.expect = ws_tag(B, Hq, Hkv, L, S, D, seq_start, out, lse, cu, row_ptr);
-  return bwd_run(q, k, v, out, ws + wl.out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
+  return bwd_run(q, k, v, out, ws + wl.out16, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
                  ws + wl.plan_off, dq, dk, dv, ws + wl.bwd_off, drop, dev_status, stages, &prep,
                  stream);
 }
@@ -531,25 +534,25 @@ int bd_attn_bwd_dropout(const void* q, const void* k, const void* v, const void*
 
 int bd_attn_fwd_planned(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
                         int L, int S, int D, int seq_start, float scale, int enable_gqa,
-                        void* plan, size_t plan_bytes, void* out, float* lse, void* out_lo,
+                        void* plan, size_t plan_bytes, void* out, float* lse, void* out16,
                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
                         bd_stream_t stream) {
   return fwd_planned_impl(q, k, v, B, Hq, Hkv, L, S, D, seq_start, scale, enable_gqa, plan,
-                          plan_bytes, out, lse, out_lo, workspace, workspace_bytes,
+                          plan_bytes, out, lse, out16, workspace, workspace_bytes,
                           DropoutArgs{}, dev_status, stream);
 }
 
 int bd_attn_fwd_dropout_planned(const void* q, const void* k, const void* v, int B, int Hq,
                                 int Hkv, int L, int S, int D, int seq_start, float scale,
                                 int enable_gqa, void* plan, size_t plan_bytes, void* out,
-                                float* lse, void* out_lo, void* workspace, size_t workspace_bytes,
+                                float* lse, void* out16, void* workspace, size_t workspace_bytes,
                                 double dropout_p, uint64_t seed, uint32_t offset,
                                 int32_t* dev_status, bd_stream_t stream) {
   DropoutArgs drop;
   const int st = make_dropout(dropout_p, seed, offset, &drop);
   if (st != BD_OK) return st;
   return fwd_planned_impl(q, k, v, B, Hq, Hkv, L, S, D, seq_start, scale, enable_gqa, plan,
-                          plan_bytes, out, lse, out_lo, workspace, workspace_bytes, drop,
+                          plan_bytes, out, lse, out16, workspace, workspace_bytes, drop,
                           dev_status, stream);
 }
 
@@ -559,18 +562,18 @@ size_t bd_attn_bwd_planned_workspace_size(int B, int Hq, int Hkv, int L, int S, 
 }
 
 int bd_attn_bwd_planned(const void* q, const void* k, const void* v, const void* out,
-                        const void* out_lo, const float* lse, const void* dout, int B, int Hq,
+                        const void* out16, const float* lse, const void* dout, int B, int Hq,
                         int Hkv, int L, int S, int D, int seq_start, float scale, int enable_gqa,
                         void* plan, size_t plan_bytes, void* dq, void* dk, void* dv,
                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
                         bd_stream_t stream) {
-  return bwd_planned_impl(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
+  return bwd_planned_impl(q, k, v, out, out16, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
                           enable_gqa, plan, plan_bytes, dq, dk, dv, workspace, workspace_bytes,
                           DropoutArgs{}, dev_status, stream);
 }
 
 int bd_attn_bwd_dropout_planned(const void* q, const void* k, const void* v, const void* out,
-                                const void* out_lo, const float* lse, const void* dout, int B,
+                                const void* out16, const float* lse, const void* dout, int B,
                                 int Hq, int Hkv, int L, int S, int D, int seq_start, float scale,
                                 int enable_gqa, void* plan, size_t plan_bytes, void* dq,
                                 void* dk, void* dv, void* workspace, size_t workspace_bytes,
@@ -579,7 +582,7 @@ int bd_attn_bwd_dropout_planned(const void* q, const void* k, const void* v, con
   DropoutArgs drop;
   const int st = make_dropout(dropout_p, seed, offset, &drop);
   if (st != BD_OK) return st;
-  return bwd_planned_impl(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
+  return bwd_planned_impl(q, k, v, out, out16, lse, dout, B, Hq, Hkv, L, S, D, seq_start, scale,
                           enable_gqa, plan, plan_bytes, dq, dk, dv, workspace, workspace_bytes,
                           drop, dev_status, stream);
 }

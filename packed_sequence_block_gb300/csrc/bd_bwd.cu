@@ -168,11 +168,11 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // zeroed dq accumulator (bwd_pre_rows in bd_pre_dev.cuh).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(
-    const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ out_lo,
+    const __nv_bfloat16* __restrict__ out, const __half* __restrict__ out16, float o16_scale,
     const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse, int planes, int L,
     int Lq, float* __restrict__ nlse2o, float* __restrict__ ndeltao, float* __restrict__ dqacc) {
-  bwd_pre_rows<D>((long long)blockIdx.x * blockDim.x + threadIdx.x, out, out_lo, dout, lse,
-                  planes, L, Lq, nlse2o, ndeltao, dqacc);
+  bwd_pre_rows<D>((long long)blockIdx.x * blockDim.x + threadIdx.x, out, out16, o16_scale, dout,
+                  lse, planes, L, Lq, nlse2o, ndeltao, dqacc);
 }
 
 template <int D>
@@ -827,7 +827,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const CUtensorMap& tdo,
                                 const CUtensorMap& tdq,
                                 const BwdParams& p,
-                                const void* out, const void* out_lo, const float* lse,
+                                const void* out, const void* out16, const float* lse,
                                 const void* dout, void* dq, int stages,
                                 int num_sms,
                                 cudaStream_t stream, const BwdPrep* prep) {
@@ -842,15 +842,17 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
     attr_set[dev] = true;
   }
   const int planes = p.B * p.Hq;
+  // out16 lacks the dropout scale that out carries
+  const float o16_scale = kDrop ? p.drop.rp : 1.f;
   if ((stages & kBwdPrepare) && prep != nullptr) {
-    cudaError_t e = launch_prep_bwd(*prep, out, out_lo, dout, lse, D, planes, p.L, p.Lq,
-                                    const_cast<float*>(p.nlse2), const_cast<float*>(p.ndelta),
-                                    p.dqacc, p.status, stream);
+    cudaError_t e = launch_prep_bwd(*prep, out, out16, o16_scale, dout, lse, D, planes, p.L,
+                                    p.Lq, const_cast<float*>(p.nlse2),
+                                    const_cast<float*>(p.ndelta), p.dqacc, p.status, stream);
     if (e != cudaSuccess) return e;
   } else if (stages & kBwdPrepare) {
-    const long long threads = (long long)planes * p.Lq * (D / 8);
+    const long long threads = (long long)planes * p.Lq * pre_threads_per_row<D>();
     bwd_pre_kernel<D><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(out_lo),
+        static_cast<const __nv_bfloat16*>(out), static_cast<const __half*>(out16), o16_scale,
         static_cast<const __nv_bfloat16*>(dout), lse, planes, p.L, p.Lq,
         const_cast<float*>(p.nlse2), const_cast<float*>(p.ndelta), p.dqacc);
     cudaError_t e = cudaGetLastError();
@@ -872,7 +874,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const AttnDims& d,
-                       void* plan, const void* out, const void* out_lo, const float* lse,
+                       void* plan, const void* out, const void* out16, const float* lse,
                        const void* dout, void* dq, void* dk,
                        void* dv, void* workspace, int32_t* status, int stages, int num_sms,
                        cudaStream_t stream, const BwdPrep* prep) {
@@ -911,15 +913,15 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.drop = d.drop;
   if (d.drop.on) {
     if (d.D == 64)
-      return launch_bwd_t<64, true>(tq, tk, tv, tdo, tdq, p, out, out_lo, lse, dout, dq, stages,
+      return launch_bwd_t<64, true>(tq, tk, tv, tdo, tdq, p, out, out16, lse, dout, dq, stages,
                                     num_sms, stream, prep);
-    return launch_bwd_t<128, true>(tq, tk, tv, tdo, tdq, p, out, out_lo, lse, dout, dq, stages,
+    return launch_bwd_t<128, true>(tq, tk, tv, tdo, tdq, p, out, out16, lse, dout, dq, stages,
                                    num_sms, stream, prep);
   }
   if (d.D == 64)
-    return launch_bwd_t<64, false>(tq, tk, tv, tdo, tdq, p, out, out_lo, lse, dout, dq, stages,
+    return launch_bwd_t<64, false>(tq, tk, tv, tdo, tdq, p, out, out16, lse, dout, dq, stages,
                                    num_sms, stream, prep);
-  return launch_bwd_t<128, false>(tq, tk, tv, tdo, tdq, p, out, out_lo, lse, dout, dq, stages,
+  return launch_bwd_t<128, false>(tq, tk, tv, tdo, tdq, p, out, out16, lse, dout, dq, stages,
                                   num_sms, stream, prep);
 }
 

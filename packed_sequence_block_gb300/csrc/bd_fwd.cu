@@ -38,7 +38,7 @@ struct FwdCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + 2 * QTILE;
   static constexpr int OFF_V = OFF_K + KSTAGES * KTILE;
-  // epilogue staging: per softmax warp 32 rows x 64 B of out, then of out_lo
+  // epilogue staging: per softmax warp 32 rows x 64 B of out, then of out16
   static constexpr int OFF_STG = OFF_V + VSTAGES * KTILE;
   static constexpr int OFF_BAR = OFF_STG + 8 * 4096;
   static constexpr int SMEM = OFF_BAR + 512;
@@ -56,7 +56,9 @@ struct FwdParams {
   const int32_t* fwd_range;
   const int32_t* fwd_order;
   __nv_bfloat16* out;
-  __nv_bfloat16* out_lo;  // optional: bf16(O - bf16(O)), the rounding residual of out
+  // optional: fp16 copy of O without the dropout scale 1 / (1 - p), i.e. the
+  // normalised P V (within the range of v), from which the backward forms Delta
+  __half* out16;
   float* lse;
   int32_t* status;
   int* ctr;  // work counters in the plan: [next unit, finished CTAs]
@@ -138,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v,
                   const __grid_constant__ CUtensorMap tmap_o,
-                  const __grid_constant__ CUtensorMap tmap_olo,
+                  const __grid_constant__ CUtensorMap tmap_o16,
                   const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -190,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
     prefetch_tmap(&tmap_o);
-    prefetch_tmap(&tmap_olo);
+    prefetch_tmap(&tmap_o16);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -380,8 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint4* dst = reinterpret_cast<uint4*>(p.out + row * D);
 #pragma unroll
           for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-          if (p.out_lo != nullptr) {
-            uint4* dl = reinterpret_cast<uint4*>(p.out_lo + row * D);
+          if (p.out16 != nullptr) {
+            uint4* dl = reinterpret_cast<uint4*>(p.out16 + row * D);
 #pragma unroll
             for (int c = 0; c < D / 8; ++c) dl[c] = make_uint4(0, 0, 0, 0);
           }
@@ -505,8 +507,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ++o_it;
       tc_fence_after();
-      // the kept weights enter P V unscaled; 1 / (1 - p) joins 1 / l here
-      const float inv = (l > 0.f) ? (kDrop ? p.drop.rp : 1.f) / l : 0.f;
+      // the kept weights enter P V unscaled; 1 / (1 - p) joins 1 / l for out
+      // (out16 keeps the normalised P V, whose entries lie within v's range)
+      const float inv16 = (l > 0.f) ? 1.f / l : 0.f;
+      const float inv = kDrop ? inv16 * p.drop.rp : inv16;
       // Each 32-column chunk of this warp's 32 rows goes through its staging
       // area in the TMA box layout (64-byte rows, 16-byte pieces swizzled by
       // row pair, which also keeps the writes free of bank conflicts), and
@@ -532,10 +536,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16], pl[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float a = __uint_as_float(v[2 * e]) * inv, b = __uint_as_float(v[2 * e + 1]) * inv;
-          pk[e] = pack_bf16x2(a, b);
-          pl[e] = pack_bf16x2(a - __uint_as_float(pk[e] << 16),
-                              b - __uint_as_float(pk[e] & 0xffff0000u));
+          const float a = __uint_as_float(v[2 * e]), b = __uint_as_float(v[2 * e + 1]);
+          pk[e] = pack_bf16x2(a * inv, b * inv);
+          pl[e] = pack_f16x2(a * inv16, b * inv16);
         }
         if (lane == 0) bulk_wait_read_all();  // the TMA has read the previous chunk
         __syncwarp();
@@ -549,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           tma_store_3d(&tmap_o, stg, c * 32, i0, plane_o);
-          if (p.out_lo != nullptr) tma_store_3d(&tmap_olo, stg + 2048, c * 32, i0, plane_o);
+          if (p.out16 != nullptr) tma_store_3d(&tmap_o16, stg + 2048, c * 32, i0, plane_o);
           bulk_commit_group();
         }
       }
@@ -587,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool kDrop>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const CUtensorMap& to,
-                                const CUtensorMap& tol, const FwdParams& p, int num_sms,
+                                const CUtensorMap& to16, const FwdParams& p, int num_sms,
                                 cudaStream_t stream) {
   using C = FwdCfg<D>;
   static bool attr_set[64] = {};
@@ -601,7 +604,7 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
   }
   const int grid = p.n_units < num_sms ? p.n_units : num_sms;
   if (grid <= 0) return cudaSuccess;
-  bd_fwd_kernel<D, kDrop><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, tol, p);
+  bd_fwd_kernel<D, kDrop><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, to, to16, p);
   return cudaGetLastError();
 }
 
@@ -628,8 +631,8 @@ cudaError_t launch_v_to_f16(const void* v, void* v16, long long n, int num_sms,
 }
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, const CUtensorMap& tol, const AttnDims& d,
-                       void* plan, void* out, void* out_lo, float* lse, int32_t* status,
+                       const CUtensorMap& to, const CUtensorMap& to16, const AttnDims& d,
+                       void* plan, void* out, void* out16, float* lse, int32_t* status,
                        int num_sms, cudaStream_t stream, void* acc, size_t acc_bytes,
                        uint32_t* acc_flags) {
   const PlanLayout pl = plan_layout(d.B, d.Hq, d.Hkv, d.L, d.S);
@@ -652,7 +655,7 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.fwd_range = reinterpret_cast<const int32_t*>(base + pl.fwd_range);
   p.fwd_order = reinterpret_cast<const int32_t*>(base + pl.fwd_order);
   p.out = static_cast<__nv_bfloat16*>(out);
-  p.out_lo = static_cast<__nv_bfloat16*>(out_lo);
+  p.out16 = static_cast<__half*>(out16);
   p.lse = lse;
   p.status = status;
   p.ctr = reinterpret_cast<int*>(base + pl.sched);
@@ -663,11 +666,11 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   p.wait_limit_ns = take_wait_test(kWaitTestFwd, &p.withhold);
   p.drop = d.drop;
   if (d.drop.on) {
-    if (d.D == 64) return launch_fwd_t<64, true>(tq, tk, tv, to, tol, p, num_sms, stream);
-    return launch_fwd_t<128, true>(tq, tk, tv, to, tol, p, num_sms, stream);
+    if (d.D == 64) return launch_fwd_t<64, true>(tq, tk, tv, to, to16, p, num_sms, stream);
+    return launch_fwd_t<128, true>(tq, tk, tv, to, to16, p, num_sms, stream);
   }
-  if (d.D == 64) return launch_fwd_t<64, false>(tq, tk, tv, to, tol, p, num_sms, stream);
-  return launch_fwd_t<128, false>(tq, tk, tv, to, tol, p, num_sms, stream);
+  if (d.D == 64) return launch_fwd_t<64, false>(tq, tk, tv, to, to16, p, num_sms, stream);
+  return launch_fwd_t<128, false>(tq, tk, tv, to, to16, p, num_sms, stream);
 }
 
 }  // namespace bd

@@ -113,12 +113,12 @@ struct DropoutArgs {
 
 // Workspace of the single-call entry points (bd_attn_fwd / bd_attn_bwd, which
 // take cumulative boundaries): a 256-byte header, the plan, the fp16 copy of
-// v, the forward's rounding residual of out, then the backward workspace.
+// v, the forward's fp16 copy of O (out16), then the backward workspace.
 // Every part starts on a 256-byte boundary.
 struct WsLayout {
   PlanLayout plan;
   BwdLayout bwd;
-  size_t hdr, plan_off, v16, out_lo, bwd_off, total;
+  size_t hdr, plan_off, v16, out16, bwd_off, total;
 };
 
 inline WsLayout ws_layout(int B, int Hq, int Hkv, int L, int S, int D) {
@@ -129,7 +129,7 @@ inline WsLayout ws_layout(int B, int Hq, int Hkv, int L, int S, int D) {
   w.hdr = off;      off = 256;
   w.plan_off = off; off = align256(off + w.plan.total);
   w.v16 = off;      off = align256(off + 2 * (size_t)B * Hkv * S * D);
-  w.out_lo = off;   off = align256(off + 2 * (size_t)B * Hq * L * D);
+  w.out16 = off;   off = align256(off + 2 * (size_t)B * Hq * L * D);
   w.bwd_off = off;  off = align256(off + w.bwd.total);
   w.total = off;
   return w;
@@ -137,7 +137,7 @@ inline WsLayout ws_layout(int B, int Hq, int Hkv, int L, int S, int D) {
 
 // What the single-call forward records in the workspace header: the shapes,
 // the boundaries it planned from and the output it wrote.  The backward
-// reuses the plan and the residual of out kept in the workspace only when the
+// reuses the plan and the fp16 O kept in the workspace only when the
 // header names the same shapes, boundaries, out and lse; otherwise it
 // rebuilds the plan and forms Delta from the bf16 output alone.  `flags`
 // (not part of the match) has kAccZeroed set by the forward kernel once it
@@ -149,7 +149,7 @@ struct WsTag {
   unsigned long long out, lse, cu, row_ptr;
   uint32_t flags;
 };
-constexpr uint32_t kWsMagic = 0x42445732u;  // "BDW2"
+constexpr uint32_t kWsMagic = 0x42445733u;  // "BDW3"
 constexpr uint32_t kAccZeroed = 1u;
 
 // Where the plan builder writes (device pointers into a plan buffer).
@@ -193,8 +193,10 @@ cudaError_t launch_plan(const int32_t* seg, const int32_t* seg_ids, const int32_
 // Tensor maps for q/k/v-like tensors [planes, rows, D] (bf16, 128-byte swizzle,
 // box 64 x 128 x 1).  Returns false when the driver rejects the map.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int planes, int rows, int D);
-// bf16 [planes, rows, D] written by TMA stores of 32 x 32 boxes (64-byte swizzle).
-bool make_tmap_out(CUtensorMap* map, const void* base, int planes, int rows, int D);
+// 16-bit [planes, rows, D] (out: bf16, out16: fp16) written by TMA stores of
+// 32 x 32 boxes (64-byte swizzle).
+bool make_tmap_out(CUtensorMap* map, const void* base, int planes, int rows, int D,
+                   CUtensorMapDataType type);
 // The same for fp16 data.
 bool make_tmap_f16(CUtensorMap* map, const void* base, int planes, int rows, int D);
 // Tensor map for the fp32 dq accumulator [planes, rows, D] (128-byte swizzle,
@@ -209,9 +211,9 @@ cudaError_t launch_v_to_f16(const void* v, void* v16, long long n, int num_sms,
 // kernel's otherwise idle warps zero while it runs; `acc_flags` (or NULL)
 // then gets kAccZeroed once every CTA finished without an error.
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, const CUtensorMap& tol,
+                       const CUtensorMap& to, const CUtensorMap& to16,
                        const AttnDims& d, void* plan, void* out,
-                       void* out_lo, float* lse, int32_t* status, int num_sms,
+                       void* out16, float* lse, int32_t* status, int num_sms,
                        cudaStream_t stream, void* acc = nullptr, size_t acc_bytes = 0,
                        uint32_t* acc_flags = nullptr);
 // One launch before the single-call forward: block 0 builds the plan from the
@@ -225,8 +227,8 @@ cudaError_t launch_prep_fwd(const int32_t* cu, const int32_t* row_ptr, const Pla
 constexpr int kBwdPrepare = 1, kBwdMain = 2, kBwdFinish = 4;
 
 // For the single-call backward: stage 1 also builds the plan from the
-// cumulative boundaries (block 0 of the same launch), and takes the residual
-// of out from the workspace only when the header carries `expect`.
+// cumulative boundaries (block 0 of the same launch), and takes the fp16 O
+// from the workspace only when the header carries `expect`.
 struct BwdPrep {
   const int32_t* cu;
   const int32_t* row_ptr;
@@ -237,7 +239,7 @@ struct BwdPrep {
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const AttnDims& d,
-                       void* plan, const void* out, const void* out_lo, const float* lse,
+                       void* plan, const void* out, const void* out16, const float* lse,
                        const void* dout, void* dq, void* dk,
                        void* dv, void* workspace, int32_t* status, int stages, int num_sms,
                        cudaStream_t stream, const BwdPrep* prep = nullptr);
@@ -247,9 +249,9 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 // the other blocks write -lse log2 e and -Delta per row and zero the dq
 // accumulator unless the header says the forward already did (the rows'
 // terms as bwd_pre_kernel writes them).
-cudaError_t launch_prep_bwd(const BwdPrep& prep, const void* out, const void* out_lo,
-                            const void* dout, const float* lse, int D, int planes, int L, int Lq,
-                            float* nlse2, float* ndelta, float* dqacc, int32_t* status,
-                            cudaStream_t stream);
+cudaError_t launch_prep_bwd(const BwdPrep& prep, const void* out, const void* out16,
+                            float o16_scale, const void* dout, const float* lse, int D,
+                            int planes, int L, int Lq, float* nlse2, float* ndelta, float* dqacc,
+                            int32_t* status, cudaStream_t stream);
 
 }  // namespace bd

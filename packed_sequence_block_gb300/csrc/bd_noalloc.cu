@@ -50,7 +50,7 @@ cudaError_t scratch_address(void** out) {
 extern "C" {
 
 int bd_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
-                        const void* out_lo, const float* lse, const void* dout, int B, int Hq,
+                        const void* out16, const float* lse, const void* dout, int B, int Hq,
                         int Hkv, int L, int S, int D, int seq_start, float scale, int enable_gqa,
                         void* plan, size_t plan_bytes, void* dq, void* dk, void* dv,
                         int32_t* dev_status, bd_stream_t stream) {
@@ -62,7 +62,7 @@ int bd_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
   // the scratch address is looked up first only because it is an argument.
   void* scratch = nullptr;
   if (bd::scratch_address(&scratch) != cudaSuccess) return BD_ERR_CUDA;
-  return bd_attn_bwd_planned(q, k, v, out, out_lo, lse, dout, B, Hq, Hkv, L, S, D, seq_start,
+  return bd_attn_bwd_planned(q, k, v, out, out16, lse, dout, B, Hq, Hkv, L, S, D, seq_start,
                              scale, enable_gqa, plan, plan_bytes, dq, dk, dv, scratch,
                              bd::kNoAllocScratchBytes, dev_status, stream);
 }

@@ -57,10 +57,10 @@ template <int D>
 __global__ void __launch_bounds__(kPrepBwdThreads) prep_bwd_kernel(
     const int32_t* __restrict__ cu, const int32_t* __restrict__ row_ptr, const PlanPtrs pp,
     const WsTag* hdr, const WsTag expect, const __nv_bfloat16* __restrict__ out,
-    const __nv_bfloat16* __restrict__ out_lo, const __nv_bfloat16* __restrict__ dout,
+    const __half* __restrict__ out16, float o16_scale, const __nv_bfloat16* __restrict__ dout,
     const float* __restrict__ lse, int planes, int L, int Lq, float* __restrict__ nlse2o,
     float* __restrict__ ndeltao, float* __restrict__ dqacc, int32_t* status) {
-  // the plan, the residual of out and the zeroed accumulator the forward left
+  // the plan, the fp16 O and the zeroed accumulator the forward left
   // in the workspace belong to these inputs only if its header says so
   const bool same = same_tag(hdr, expect);
   if (blockIdx.x == 0) {
@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kPrepBwdThreads) prep_bwd_kernel(
   }
   const bool zero = !(same && (hdr->flags & kAccZeroed) != 0);
   bwd_pre_rows<D>((long long)(blockIdx.x - 1) * blockDim.x + threadIdx.x, out,
-                  same ? out_lo : nullptr, dout, lse, planes, L, Lq, nlse2o, ndeltao,
+                  same ? out16 : nullptr, o16_scale, dout, lse, planes, L, Lq, nlse2o, ndeltao,
                   zero ? dqacc : nullptr);
 }
 
@@ -105,31 +105,32 @@ cudaError_t launch_prep_fwd(const int32_t* cu, const int32_t* row_ptr, const Pla
   return cudaGetLastError();
 }
 
-cudaError_t launch_prep_bwd(const BwdPrep& prep, const void* out, const void* out_lo,
-                            const void* dout, const float* lse, int D, int planes, int L, int Lq,
-                            float* nlse2, float* ndelta, float* dqacc, int32_t* status,
-                            cudaStream_t stream) {
+cudaError_t launch_prep_bwd(const BwdPrep& prep, const void* out, const void* out16,
+                            float o16_scale, const void* dout, const float* lse, int D,
+                            int planes, int L, int Lq, float* nlse2, float* ndelta, float* dqacc,
+                            int32_t* status, cudaStream_t stream) {
   static int attr64[64] = {}, attr128[64] = {};
   const size_t smem = plan_cta_smem(prep.pp);
-  const long long threads = (long long)planes * Lq * (D / 8);
+  const long long threads =
+      (long long)planes * Lq * (D == 64 ? pre_threads_per_row<64>() : pre_threads_per_row<128>());
   const unsigned blocks =
       1 + static_cast<unsigned>((threads + kPrepBwdThreads - 1) / kPrepBwdThreads);
   const auto* o = static_cast<const __nv_bfloat16*>(out);
-  const auto* ol = static_cast<const __nv_bfloat16*>(out_lo);
+  const auto* ol = static_cast<const __half*>(out16);
   const auto* d = static_cast<const __nv_bfloat16*>(dout);
   cudaError_t e;
   if (D == 64) {
     e = set_smem(reinterpret_cast<const void*>(prep_bwd_kernel<64>), smem, attr64);
     if (e != cudaSuccess) return e;
     prep_bwd_kernel<64><<<blocks, kPrepBwdThreads, smem, stream>>>(
-        prep.cu, prep.row_ptr, prep.pp, prep.hdr, prep.expect, o, ol, d, lse, planes, L, Lq,
-        nlse2, ndelta, dqacc, status);
+        prep.cu, prep.row_ptr, prep.pp, prep.hdr, prep.expect, o, ol, o16_scale, d, lse, planes,
+        L, Lq, nlse2, ndelta, dqacc, status);
   } else {
     e = set_smem(reinterpret_cast<const void*>(prep_bwd_kernel<128>), smem, attr128);
     if (e != cudaSuccess) return e;
     prep_bwd_kernel<128><<<blocks, kPrepBwdThreads, smem, stream>>>(
-        prep.cu, prep.row_ptr, prep.pp, prep.hdr, prep.expect, o, ol, d, lse, planes, L, Lq,
-        nlse2, ndelta, dqacc, status);
+        prep.cu, prep.row_ptr, prep.pp, prep.hdr, prep.expect, o, ol, o16_scale, d, lse, planes,
+        L, Lq, nlse2, ndelta, dqacc, status);
   }
   return cudaGetLastError();
 }

@@ -57,10 +57,10 @@ def gpu_forward_backward(q, k, v, do, doc_ids, seq_start=0, scale=None, enable_g
     p, seed, offset = dropout if dropout is not None else (0.0, 0, 0)
     seg, sid, nseg = A.segment_cu_seqlens(doc_ids)
     plan = A.make_plan(seg, sid, nseg, q.shape[1], k.shape[1], q.shape[2], seq_start)
-    out, lse, out_lo = A.attn_forward(q, k, v, plan, seq_start, scale, enable_gqa,
+    out, lse, out16 = A.attn_forward(q, k, v, plan, seq_start, scale, enable_gqa,
                                       dropout_p=p, seed=seed, offset=offset)
     dq, dk, dv = A.attn_backward(q, k, v, out, lse, do, plan, seq_start, scale, enable_gqa,
-                                 out_lo=out_lo, dropout_p=p, seed=seed, offset=offset)
+                                 out16=out16, dropout_p=p, seed=seed, offset=offset)
     A.check_device_status(q.device)
     return out, lse, dq, dk, dv
 

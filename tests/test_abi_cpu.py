@@ -52,7 +52,7 @@ def test_sizes_are_host_computed(lib_):
     assert lib_.bd_attn_plan_size(0, 1, 1, 1, 1) == 0
     w = lib_.bd_attn_bwd_planned_workspace_size(1, 32, 8, 8192, 8192, 128)
     assert w >= 32 * 8192 * 128 * 4 + 32 * 8192 * 8
-    # the single-call workspace holds the plan, the fp16 v, the residual of out
+    # the single-call workspace holds the plan, the fp16 v, the fp16 copy of O
     # and the backward's accumulator and row terms
     one = lib_.bd_attn_workspace_size(1, 32, 8, 8192, 8192, 128)
     assert one % 256 == 0
@@ -110,7 +110,7 @@ def test_bwd_and_plan_reject_bad_arguments(lib_):
     bad[20] = FAKE + 4  # misaligned dv
     assert f(*bad) == 1
     bad = list(args)
-    bad[4] = FAKE + 2  # misaligned out_lo
+    bad[4] = FAKE + 2  # misaligned out16
     assert f(*bad) == 1
     p = lib_.bd_attn_plan
     assert p(FAKE, FAKE, FAKE, 1, 4, 2, 256, 256, 0, FAKE, 8, None) == 5

@@ -80,7 +80,7 @@ def _planned(G, q, k, v, do, ids_np, s0, drop):
     N.bd_segment_cu_seqlens(ids, B, S, seg, sid, nseg)
     plan = G(None, torch.uint8, N.bd_attn_plan_size(B, Hq, Hkv, L, S))
     N.bd_attn_plan(seg, sid, nseg, B, Hq, Hkv, L, S, s0, plan)
-    out, out_lo = G((B, Hq, L, D), torch.bfloat16), G((B, Hq, L, D), torch.bfloat16)
+    out, out16 = G((B, Hq, L, D), torch.bfloat16), G((B, Hq, L, D), torch.float16)
     lse = G((B, Hq, L), torch.float32)
     fws = G(None, torch.uint8, N.bd_attn_fwd_planned_workspace_size(B, Hkv, S, D))
     dq, dk, dv = (G((B, Hq, L, D), torch.bfloat16), G((B, Hkv, S, D), torch.bfloat16),
@@ -88,22 +88,22 @@ def _planned(G, q, k, v, do, ids_np, s0, drop):
     bws = G(None, torch.uint8, N.bd_attn_bwd_planned_workspace_size(B, Hq, Hkv, L, S, D))
     scale = D ** -0.5
     if drop is None:
-        N.bd_attn_fwd_planned(q, k, v, B, Hq, Hkv, L, S, D, s0, scale, gqa, plan, out, lse, out_lo,
+        N.bd_attn_fwd_planned(q, k, v, B, Hq, Hkv, L, S, D, s0, scale, gqa, plan, out, lse, out16,
                               fws, st)
         N.bd_attn_bwd_planned(q, k, v, out, lse, do, B, Hq, Hkv, L, S, D, s0, scale, gqa, plan,
-                              dq, dk, dv, bws, out_lo, st)
+                              dq, dk, dv, bws, out16, st)
     else:
         N.bd_attn_fwd_dropout_planned(q, k, v, B, Hq, Hkv, L, S, D, s0, scale, gqa, plan, out,
-                                      lse, *drop, out_lo, fws, st)
+                                      lse, *drop, out16, fws, st)
         N.bd_attn_bwd_dropout_planned(q, k, v, out, lse, do, B, Hq, Hkv, L, S, D, s0, scale, gqa,
-                                      plan, dq, dk, dv, bws, *drop, out_lo, st)
+                                      plan, dq, dk, dv, bws, *drop, out16, st)
     res = (out, lse, dq, dk, dv)
     if drop is None and N.bd_attn_bwd_planned_workspace_size(B, Hq, Hkv, L, S, D) <= \
             N.NOALLOC_SCRATCH_BYTES:
         dq2, dk2, dv2 = (G((B, Hq, L, D), torch.bfloat16), G((B, Hkv, S, D), torch.bfloat16),
                          G((B, Hkv, S, D), torch.bfloat16))
         N.bd_attn_bwd_noalloc(q, k, v, out, lse, do, B, Hq, Hkv, L, S, D, s0, scale, gqa, plan,
-                              dq2, dk2, dv2, out_lo, st)
+                              dq2, dk2, dv2, out16, st)
         res = res + (dq2, dk2, dv2)
     return res
 

@@ -81,8 +81,8 @@ def test_forward_wait_runs_out_then_the_plan_still_works(cuda_lib, name):
     A.check_device_status()
     N.bd_test_arm_wait_timeout(1, LIMIT_US)
     _expect_timeout(lambda: A.attn_forward(q, k, v, plan, 0, None, gqa))
-    out, lse, out_lo = A.attn_forward(q, k, v, plan, 0, None, gqa)
-    dq, dk, dv = A.attn_backward(q, k, v, out, lse, do, plan, 0, None, gqa, out_lo=out_lo)
+    out, lse, out16 = A.attn_forward(q, k, v, plan, 0, None, gqa)
+    dq, dk, dv = A.attn_backward(q, k, v, out, lse, do, plan, 0, None, gqa, out16=out16)
     A.check_device_status()
     _compare((out, lse, dq, dk, dv), _oracle(q, k, v, do, ids), f"{name} after forward timeout")
 
@@ -93,12 +93,12 @@ def test_backward_wait_runs_out_then_the_plan_still_works(cuda_lib, name):
     gqa = q.shape[1] != k.shape[1]
     seg, sid, nseg = A.segment_cu_seqlens(torch.from_numpy(ids).cuda())
     plan = A.make_plan(seg, sid, nseg, q.shape[1], k.shape[1], q.shape[2], 0)
-    out, lse, out_lo = A.attn_forward(q, k, v, plan, 0, None, gqa)
+    out, lse, out16 = A.attn_forward(q, k, v, plan, 0, None, gqa)
     A.check_device_status()
     N.bd_test_arm_wait_timeout(2, LIMIT_US)
     _expect_timeout(lambda: A.attn_backward(q, k, v, out, lse, do, plan, 0, None, gqa,
-                                            out_lo=out_lo))
-    dq, dk, dv = A.attn_backward(q, k, v, out, lse, do, plan, 0, None, gqa, out_lo=out_lo)
+                                            out16=out16))
+    dq, dk, dv = A.attn_backward(q, k, v, out, lse, do, plan, 0, None, gqa, out16=out16)
     A.check_device_status()
     _compare((out, lse, dq, dk, dv), _oracle(q, k, v, do, ids), f"{name} after backward timeout")
 

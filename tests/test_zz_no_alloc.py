@@ -50,13 +50,13 @@ def _noalloc_against_workspace_path(case, calls=2):
     q, k, v, do, plan, ids = _problem(B, S, Hq, Hkv, D, cu_rows, seed)
     gqa = Hq != Hkv
     assert N.bd_attn_bwd_planned_workspace_size(B, Hq, Hkv, S, S, D) <= N.NOALLOC_SCRATCH_BYTES
-    out, lse, out_lo = A.attn_forward(q, k, v, plan, 0, None, gqa)
-    ref = A.attn_backward(q, k, v, out, lse, do, plan, 0, None, gqa, out_lo=out_lo)
+    out, lse, out16 = A.attn_forward(q, k, v, plan, 0, None, gqa)
+    ref = A.attn_backward(q, k, v, out, lse, do, plan, 0, None, gqa, out16=out16)
     A.check_device_status()
     for call in range(calls):
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         N.bd_attn_bwd_noalloc(q, k, v, out, lse, do, B, Hq, Hkv, S, S, D, 0, D ** -0.5, gqa,
-                              plan, dq, dk, dv, out_lo=out_lo,
+                              plan, dq, dk, dv, out16=out16,
                               dev_status=A.device_status_word())
         A.check_device_status()
         assert_close(f"S={S} call {call} dq", to64(dq), to64(ref[0]))
