@@ -180,38 +180,49 @@ __device__ __forceinline__ int find_doc(const int32_t* c, int n, int x) {
   return lo - 1;
 }
 
-// The same document for an x at or past the position whose document was d
-// (d < 0: none yet): a few steps forward from d, else the search.  The steps
-// skip empty documents as the search does, so both give the one d with
-// c[d] <= x < c[d + 1].
-__device__ __forceinline__ int next_doc(const int32_t* c, int n, int x, int d) {
-  if (d >= 0) {
-#pragma unroll 1
-    for (int s = 0; s < 4; ++s) {
-      if (c[d + 1] > x) return d;
-      ++d;
-    }
-    if (c[d + 1] > x) return d;
-  }
-  return find_doc(c, n, x);
-}
-
 // Boundary entries the plan builder copies into shared memory (all rows
 // together, then the row pointers); longer lists are read from global memory.
 constexpr int kPlanCuCache = 4096;
+
+// Row b's boundary list c[0..n] inside the array of `total` entries, or n = -1
+// when the row pointers put it outside (the row then has no documents).
+__device__ __forceinline__ const int32_t* row_list(const int32_t* cus, const int32_t* rps,
+                                                   int total, int b, int& n) {
+  const int base = rps[b];
+  n = rps[b + 1] - base - 1;
+  if (n < 0 || base < 0 || base + n + 1 > total) n = -1;
+  return cus + (n >= 0 ? base : 0);
+}
+
+// The plan's per-position entries of a row with boundaries c[0..n] (n = 0:
+// no documents): qlo of local query x, the start of its document (kPadLo for
+// padding), and kend of key x, the end of its document (x itself for
+// padding).  Searches stay inside c[0..n] whatever the list holds.
+__device__ __forceinline__ int32_t qlo_entry(const int32_t* c, int n, const PlanPtrs& pp, int x) {
+  const int last = n > 0 ? c[n] : 0;  // positions >= last are padding
+  const int t = pp.seq_start + x;
+  return (x < pp.L && t < last) ? c[find_doc(c, n, t)] : kPadLo;
+}
+__device__ __forceinline__ int32_t kend_entry(const int32_t* c, int n, int x) {
+  const int last = n > 0 ? c[n] : 0;
+  return x < last ? c[find_doc(c, n, x) + 1] : x;
+}
 
 // The whole plan of B rows in one CTA, from cumulative boundaries (rows as in
 // bd_doc_ids_from_cu_seqlens: row b's list is cu[row_ptr[b] .. row_ptr[b+1]-1]).
 // A row whose list does not start at 0, decreases, or ends past S is planned
 // as all padding and BD_ERR_INVALID_ARG goes to *status, as its ids would be
-// all 0.  Writes qlo, kend, both tile ranges, both work-list orders and
-// zeroes the work counters.  Every thread of the block calls it; `keys` is
-// the sort's shared memory, `bad_rows` one bit per row (B <= 32 * bad_words),
-// `cu_cache` kPlanCuCache entries of shared memory.
+// all 0.  Writes both tile ranges, both work-list orders, zeroes the work
+// counters and, with write_rows, qlo and kend; without it other blocks write
+// those with qlo_entry / kend_entry (a bad row's entries are then unspecified:
+// its tiles are all empty, so no kernel reads them).  Every thread of the block
+// calls it; `keys` is the sort's shared memory, `bad_rows` one bit per row
+// (B <= 32 * bad_words), `cu_cache` kPlanCuCache entries of shared memory.
 __device__ inline void build_plan_cta(const int32_t* __restrict__ cu,
                                       const int32_t* __restrict__ row_ptr, const PlanPtrs& pp,
                                       int32_t* status, unsigned long long* keys,
-                                      uint32_t* bad_rows, int bad_words, int32_t* cu_cache) {
+                                      uint32_t* bad_rows, int bad_words, int32_t* cu_cache,
+                                      bool write_rows) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   for (int i = threadIdx.x; i < bad_words; i += blockDim.x) bad_rows[i] = 0;
   if (threadIdx.x < 8) pp.sched[threadIdx.x] = 0;
@@ -243,70 +254,51 @@ __device__ inline void build_plan_cta(const int32_t* __restrict__ cu,
     }
   }
   __syncthreads();
-  // one warp per forward query block or backward key tile
+  // Tile ranges, one thread per forward query block or backward key tile, from
+  // the first and last positions of the tile that a document holds: document
+  // starts and ends grow with the position, so the block's first valid query
+  // has the smallest start and the tile's last valid key the largest end.
   const int nf = pp.B * pp.NQB, nb = pp.B * pp.NKT;
-  for (int w = warp; w < nf + nb; w += nwarps) {
+  for (int w = threadIdx.x; w < nf + nb; w += blockDim.x) {
     const bool fwd = w < nf;
     const int u = fwd ? w : w - nf;
     const int b = fwd ? u / pp.NQB : u / pp.NKT;
     const int blk = fwd ? u % pp.NQB : u % pp.NKT;
     const bool ok = ((bad_rows[b >> 5] >> (b & 31)) & 1u) == 0;
-    const int base = rps[b];
-    const int n = ok ? rps[b + 1] - base - 1 : 0;
-    const int32_t* c = cus + base;
-    const int last = ok ? c[n] : 0;  // positions >= last are padding
-    int mn = 0x7fffffff, mx = -1;
+    int n;
+    const int32_t* c = row_list(cus, rps, total, b, n);
+    if (!ok || n < 1) n = 0;
+    const int last = n > 0 ? c[n] : 0;  // positions >= last are padding
     if (fwd) {
-      int d = -1;  // this lane's document so far (its rows increase)
-      for (int r = lane; r < pp.QROWS; r += 32) {
-        const int i = blk * pp.QROWS + r;
-        const int t = pp.seq_start + i;
-        int32_t lo = kPadLo;
-        if (i < pp.L && t < last) {
-          d = next_doc(c, n, t, d);
-          lo = c[d];
-        }
-        pp.qlo[(size_t)b * pp.Lpad + i] = lo;
-        if (lo != kPadLo) {
-          mn = min(mn, lo);
-          mx = max(mx, t);
-        }
+      const int i0 = blk * pp.QROWS, t0 = pp.seq_start + i0;
+      int lo = 0, hi = -1;
+      if (i0 < pp.L && t0 < last) {
+        lo = c[find_doc(c, n, t0)] / kBN;
+        hi = min(pp.seq_start + min(pp.L, i0 + pp.QROWS) - 1, last - 1) / kBN;
       }
+      pp.fwd_range[2 * u] = lo;
+      pp.fwd_range[2 * u + 1] = hi;
     } else {
-      int d = -1;
-      for (int r = lane; r < kBN; r += 32) {
-        const int p = blk * kBN + r;
-        int32_t e = p;
-        if (p < last) {
-          d = next_doc(c, n, p, d);
-          e = c[d + 1];
-        }
-        pp.kend[(size_t)b * pp.Spad + p] = e;
-        if (e > p) {
-          mn = min(mn, p);
-          mx = max(mx, e);
-        }
+      const int p0 = blk * kBN;
+      int a = 0, e = 0;
+      if (p0 < last) {
+        const int mx = c[find_doc(c, n, min(p0 + kBN, last) - 1) + 1];
+        a = max(p0, pp.seq_start) - pp.seq_start;
+        e = min(mx, pp.seq_start + pp.L) - pp.seq_start;
       }
+      pp.bwd_range[2 * u] = (a < e) ? a / kBM : 0;
+      pp.bwd_range[2 * u + 1] = (a < e) ? (e - 1) / kBM : -1;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    if (lane == 0) {
-      if (fwd) {
-        const bool any = mx >= 0;
-        pp.fwd_range[2 * u] = any ? mn / kBN : 0;
-        pp.fwd_range[2 * u + 1] = any ? mx / kBN : -1;
-      } else {
-        int a = 0, e = 0;
-        if (mx >= 0) {
-          a = max(mn, pp.seq_start) - pp.seq_start;
-          e = min(mx, pp.seq_start + pp.L) - pp.seq_start;
-        }
-        pp.bwd_range[2 * u] = (a < e) ? a / kBM : 0;
-        pp.bwd_range[2 * u + 1] = (a < e) ? (e - 1) / kBM : -1;
-      }
+  }
+  if (write_rows) {
+    for (int b = 0; b < pp.B; ++b) {
+      int n;
+      const int32_t* c = row_list(cus, rps, total, b, n);
+      if (((bad_rows[b >> 5] >> (b & 31)) & 1u) != 0 || n < 1) n = 0;
+      for (int x = threadIdx.x; x < pp.Lpad; x += blockDim.x)
+        pp.qlo[(size_t)b * pp.Lpad + x] = qlo_entry(c, n, pp, x);
+      for (int x = threadIdx.x; x < pp.Spad; x += blockDim.x)
+        pp.kend[(size_t)b * pp.Spad + x] = kend_entry(c, n, x);
     }
   }
   __threadfence_block();

@@ -3,8 +3,8 @@
 // launch whose block 0 builds the attention plan from the boundaries (the
 // mask bounds of every row and the ordered work lists, see
 // bd_plan_dev.cuh) while the other blocks do the pass over HBM that the call
-// needs anyway: the fp16 copy of v before the forward, the per-row terms
-// before the backward.
+// needs anyway: the fp16 copy of v and the plan's per-position mask bounds
+// before the forward, the per-row terms before the backward.
 #include "bd_plan_dev.cuh"
 #include "bd_pre_dev.cuh"
 
@@ -16,7 +16,7 @@ constexpr int kPrepFwdThreads = 1024;
 constexpr int kPrepBwdThreads = 256;
 
 __device__ __forceinline__ void plan_block(const int32_t* cu, const int32_t* row_ptr,
-                                           const PlanPtrs& pp, int32_t* status) {
+                                           const PlanPtrs& pp, int32_t* status, bool write_rows) {
   extern __shared__ unsigned long long prep_smem[];
   const int nf = pp.B * pp.NQB, nb = pp.B * pp.NKT;
   int np = 1;
@@ -26,7 +26,7 @@ __device__ __forceinline__ void plan_block(const int32_t* cu, const int32_t* row
   const int nkeys = (nf <= kRankSortMax && nb <= kRankSortMax) ? max(np, nf + nb) : np;
   uint32_t* bad = reinterpret_cast<uint32_t*>(prep_smem + nkeys);
   int32_t* cache = reinterpret_cast<int32_t*>(bad + bad_words);
-  build_plan_cta(cu, row_ptr, pp, status, prep_smem, bad, bad_words, cache);
+  build_plan_cta(cu, row_ptr, pp, status, prep_smem, bad, bad_words, cache, write_rows);
 }
 
 // The header records the forward of these inputs (flags aside).
@@ -41,9 +41,29 @@ __global__ void __launch_bounds__(kPrepFwdThreads) prep_fwd_kernel(
     const WsTag tag, WsTag* hdr, const uint4* __restrict__ v, uint4* __restrict__ v16,
     long long n8, int32_t* status) {
   if (blockIdx.x == 0) {
-    plan_block(cu, row_ptr, pp, status);
+    plan_block(cu, row_ptr, pp, status, false);
     if (threadIdx.x == 0) *hdr = tag;  // flags 0: the forward kernel sets kAccZeroed
     return;
+  }
+  // the plan's per-position entries (block 0 has the tile ranges and lists):
+  // qlo of every row, then kend of every row (fewer than 2^31 entries: the
+  // plan's lists are at most kMaxListLen tiles)
+  {
+    const int total = __ldg(row_ptr + pp.B);
+    const int nq = pp.B * pp.Lpad, ne = nq + pp.B * pp.Spad;
+    for (int e = (blockIdx.x - 1) * blockDim.x + threadIdx.x; e < ne;
+         e += (gridDim.x - 1) * blockDim.x) {
+      const bool key = e >= nq;
+      const int k = key ? e - nq : e;
+      const int b = key ? k / pp.Spad : k / pp.Lpad;
+      int n;
+      const int32_t* c = row_list(cu, row_ptr, total, b, n);
+      if (n < 1) n = 0;
+      if (key)
+        pp.kend[k] = kend_entry(c, n, k - b * pp.Spad);
+      else
+        pp.qlo[k] = qlo_entry(c, n, pp, k - b * pp.Lpad);
+    }
   }
   for (long long i = (long long)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < n8;
        i += (long long)(gridDim.x - 1) * blockDim.x) {
@@ -64,7 +84,7 @@ __global__ void __launch_bounds__(kPrepBwdThreads) prep_bwd_kernel(
   // in the workspace belong to these inputs only if its header says so
   const bool same = same_tag(hdr, expect);
   if (blockIdx.x == 0) {
-    if (!same) plan_block(cu, row_ptr, pp, status);
+    if (!same) plan_block(cu, row_ptr, pp, status, true);
     return;
   }
   const bool zero = !(same && (hdr->flags & kAccZeroed) != 0);
