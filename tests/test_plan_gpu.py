@@ -49,6 +49,13 @@ CASES = [
     ([[0, 130, 900, 1500, 1900]], 2048, 6, 2, 700, 555),            # G = 3, interval
     ([[0, 64, 64, 400, 1024]], 1024, 4, 4, 256, 768),               # interval at the tail
     ([[0]], 512, 2, 1, 512, 0),                                     # all padding
+    # the per-tile range searches at their edges: boundaries on tile edges,
+    # empty documents on a tile edge with the interval starting mid-document
+    # and padding after it, an interval wholly in padding, one-token documents
+    ([[0, 128, 256, 384, 512]], 512, 2, 2, 512, 0),
+    ([[0, 128, 128, 128, 300, 1000]], 1024, 4, 2, 600, 200),
+    ([[0, 100]], 1024, 2, 1, 500, 300),
+    ([[0, 1, 2, 3, 640], [0, 639, 640]], 640, 3, 3, 640, 0),
 ]
 
 
