@@ -58,6 +58,10 @@ CASES = [
     ([[0, 1, 2, 3, 640], [0, 639, 640]], 640, 3, 3, 640, 0),
     # a long document: the forward list goes longest first
     ([[0, 1900, 2048]], 2048, 2, 2, 2048, 0),
+    # at the order rule's threshold: a query block reaching 8 key tiles keeps
+    # position order, one reaching 9 goes longest first
+    ([[0, 1024, 1100]], 1100, 2, 2, 1100, 0),
+    ([[0, 1025, 1100]], 1100, 2, 2, 1100, 0),
 ]
 
 
