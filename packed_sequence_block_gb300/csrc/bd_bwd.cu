@@ -243,10 +243,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* stg_read = bars + 16;  // [4]
   uint64_t* do_full = bars + 20;   // dO_i landed
   uint64_t* do_empty = bars + 21;  // dV_i done: the dO buffer may be refilled
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 22);
+  // ds_half (D = 64): the first 32 queries of each P/dS group's dS_i are in
+  // shared memory (the dK k-steps over those queries can start)
+  uint64_t* ds_half = bars + 22;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 23);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);  // + the wait limit
-  WorkRing* ring = reinterpret_cast<WorkRing*>(bars + 24);
-  static_assert(24 * 8 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
+  WorkRing* ring = reinterpret_cast<WorkRing*>(bars + 25);
+  static_assert(25 * 8 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
   static_assert(C::SMEM <= 232448, "shared memory over the per-block limit");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -268,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dp_full, 1);
     mbar_init(p_full, 256);
     mbar_init(ds_full, 256);
+    mbar_init(ds_half, 256);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 2 * D);  // the reader threads that hold dQ columns
     mbar_init(dkdv_full, 1);
@@ -394,16 +398,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       // dK[keys, D] += dS^T[keys, queries] * Q[queries, D]: the dS tile (key rows,
-      // queries contiguous) is the K-major A operand, Q the MN-major B operand
-      auto issue_dk = [&](uint32_t b, bool acc) {
+      // queries contiguous) is the K-major A operand, Q the MN-major B operand.
+      // Issued in two halves: part 0 takes the k-steps over queries [0, 32) and
+      // [64, 96) (the first 32 queries of each P/dS group, ready at ds_half at
+      // D = 64), part 1 the rest; the first instruction of part 0 sets or
+      // accumulates.  At D = 64, where the P/dS warps and this thread bound
+      // the period together, starting part 0 early took causal64k's backward
+      // from 82.7 to 81.7 ms; at D = 128 it cost short documents ~1%, so there
+      // all eight k-steps go in order once the whole of dS is in.
+      // part < 0: all eight k-steps in order.
+      auto issue_dk = [&](uint32_t b, bool acc, int part) {
         const uint64_t ad = make_sdesc_sw128(sds, 16, 1024), bd = make_sdesc_sw128(b, 16384, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          if (kk == 0)
-            mma_ss(tDK, ad, bd, C::IDESC_DK, acc);
+        for (int j = 0; j < (part < 0 ? 8 : 4); ++j) {
+          // 0..7, or 0,1,4,5 (part 0) or 2,3,6,7 (part 1)
+          const int kk = part < 0 ? j : (j >> 1) * 4 + part * 2 + (j & 1);
+          const uint64_t a = sdesc_add(ad, (kk >> 2) * 16384 + (kk & 3) * 32);
+          if (part <= 0 && j == 0)
+            mma_ss(tDK, a, bd, C::IDESC_DK, acc);
           else
-            mma_ss_acc(tDK, sdesc_add(ad, (kk >> 2) * 16384 + (kk & 3) * 32),
-                       sdesc_add(bd, kk * 2048), C::IDESC_DK);
+            mma_ss_acc(tDK, a, sdesc_add(bd, kk * 2048), C::IDESC_DK);
         }
       };
       // dQ[queries, D] = dS[queries, keys] (MN-major smem) * K[keys, D] (MN-major smem)
@@ -459,10 +473,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_kmajor(tS, sk, sq0 + sn * C::TILE, C::IDESC_S);
             mma_commit(s_full);
           }
+          if constexpr (D == 64) {
+            ok = mbar_wait(ds_half, it_g & 1, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_dk(sq0 + st * C::TILE, i > 0, 0);
+          }
           ok = mbar_wait(ds_full, it_g & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
-          issue_dk(sq0 + st * C::TILE, i > 0);
+          if constexpr (D == 64)
+            issue_dk(sq0 + st * C::TILE, true, 1);
+          else
+            issue_dk(sq0 + st * C::TILE, i > 0, -1);
           mma_commit(st_empty + st);  // Q_i is no longer read after dK_i
           if (kOwnDQ && it_g > 0) {  // the previous dQ must have been read out of its columns
             ok = mbar_wait(dq_empty, (it_g - 1) & 1, abort_flag, p.status);
@@ -654,6 +677,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int cq = c * 4 + gq;  // 16-byte chunk index along this group's queries
             const uint32_t addr = sds_row + ((cq ^ (r & 7)) << 4);
             st_shared_v4(addr, dk[4 * gq], dk[4 * gq + 1], dk[4 * gq + 2], dk[4 * gq + 3]);
+          }
+          if (D == 64 && c == 0) {  // half of dK_i can start on these 32 queries
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(ds_half);
           }
         }
         fence_async_smem();
