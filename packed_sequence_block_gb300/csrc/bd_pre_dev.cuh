@@ -49,15 +49,17 @@ __device__ __forceinline__ void bwd_pre_rows(long long tid, const __nv_bfloat16*
   float acc = 0.f;
   if (i < L) {
     const size_t row = ((size_t)plane * L + i) * D;
-    // piece j of this thread: elements [(j TPR + part) 8, + 8) of the row
+    // piece j of this thread: elements [(j TPR + part) 8, + 8) of the row.
+    // O is read only here (evict-first load); dO stays in L2 for the main
+    // kernel that reads it next.
     uint4 d4[NP], o4[NP];
     const bool hp = out16 != nullptr;
 #pragma unroll
     for (int j = 0; j < NP; ++j) {
       const size_t off = row + (size_t)(j * TPR + part) * 8;
       d4[j] = *reinterpret_cast<const uint4*>(dout + off);
-      o4[j] = hp ? *reinterpret_cast<const uint4*>(out16 + off)
-                 : *reinterpret_cast<const uint4*>(out + off);
+      o4[j] = hp ? __ldcs(reinterpret_cast<const uint4*>(out16 + off))
+                 : __ldcs(reinterpret_cast<const uint4*>(out + off));
     }
 #pragma unroll
     for (int j = 0; j < NP; ++j) {
