@@ -57,12 +57,16 @@ def parse_args():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="steps of the end-to-end timing (default: --steps)")
     ap.add_argument("--dropout-p", type=float, default=0.1,
                     help="also time the step with attention dropout at this p (0: skip)")
     ap.add_argument("--soak", type=float, default=SOAK_S,
                     help="seconds of step replays before the timed steps, under the clock sampler")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.e2e_steps is None:
+        args.e2e_steps = args.steps
+    return args
 
 
 def useful_pairs(wl):
