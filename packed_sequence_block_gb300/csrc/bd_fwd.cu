@@ -116,6 +116,67 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int w) {
   return u;
 }
 
+// The decoded unit of each work-ring slot, written by the producer before it
+// publishes the slot, so that the consumers read it from shared memory
+// instead of repeating the dependent global loads of decode_unit.
+struct UnitSlots {
+  int4 a[kRing];  // b, h0, h1, qt0
+  int4 b[kRing];  // qt1, kt_lo, n, g
+};
+
+// Producer: fetch this CTA's k-th unit, decode it into its slot and publish
+// it (w = -1: no more work).
+__device__ __forceinline__ bool publish_unit(WorkRing* r, UnitSlots* us, uint32_t k,
+                                             const FwdParams& p, volatile int* abort, int& w,
+                                             Unit& u) {
+  const int slot = k % kRing;
+  if (!mbar_wait(&r->empty[slot], ((k / kRing) & 1) ^ 1, abort, p.status)) return false;
+  w = atomicAdd(&p.ctr[0], 1);
+  if (w >= p.n_units) w = -1;
+  if (w >= 0) {
+    u = decode_unit(p, w);
+    // plain stores: the arrive below (an asm statement with a memory clobber)
+    // keeps them before it, and it releases them to the slot's consumers
+    us->a[slot] = make_int4(u.b, u.h0, u.h1, u.qt0);
+    us->b[slot] = make_int4(u.qt1, u.kt_lo, u.n, u.g);
+  }
+  *reinterpret_cast<volatile int*>(&r->idx[slot]) = w;
+  mbar_arrive(&r->full[slot]);
+  return true;
+}
+
+__device__ __forceinline__ Unit slot_unit(const UnitSlots* us, int slot) {
+  const int4 a = us->a[slot];  // after the slot's full wait (acquire)
+  const int4 b = us->b[slot];
+  Unit u;
+  u.b = a.x; u.h0 = a.y; u.h1 = a.z; u.qt0 = a.w;
+  u.qt1 = b.x; u.kt_lo = b.y; u.n = b.z; u.g = b.w;
+  return u;
+}
+
+// Consumers: take slot k's unit (one thread, or a whole warp whose lane 0
+// releases the slot).
+__device__ __forceinline__ bool take_unit(WorkRing* r, const UnitSlots* us, uint32_t k,
+                                          volatile int* abort, int32_t* status, int& w, Unit& u) {
+  const int slot = k % kRing;
+  if (!mbar_wait(&r->full[slot], (k / kRing) & 1, abort, status)) return false;
+  w = *reinterpret_cast<volatile int*>(&r->idx[slot]);
+  if (w >= 0) u = slot_unit(us, slot);
+  mbar_arrive(&r->empty[slot]);
+  return true;
+}
+__device__ __forceinline__ bool take_unit_warp(WorkRing* r, const UnitSlots* us, uint32_t k,
+                                               volatile int* abort, int32_t* status, int& w,
+                                               Unit& u) {
+  const int slot = k % kRing;
+  if (!mbar_wait_warp(&r->full[slot], (k / kRing) & 1, abort, status)) return false;
+  w = *reinterpret_cast<volatile int*>(&r->idx[slot]);
+  if (w >= 0) u = slot_unit(us, slot);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&r->empty[slot]);
+  return true;
+}
+
 // Bounded wait used at teardown for copies/MMAs already in flight: ignores
 // the abort flag (the operation completes on its own) but never spins forever.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
@@ -158,7 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);  // + the wait limit
   WorkRing* ring = reinterpret_cast<WorkRing*>(smem + C::OFF_BAR + 256);
-  static_assert(256 + sizeof(WorkRing) <= C::SMEM - C::OFF_BAR, "barrier area too small");
+  UnitSlots* uslots = reinterpret_cast<UnitSlots*>(smem + C::OFF_BAR + 384);
+  static_assert(256 + sizeof(WorkRing) <= 384, "ring past the unit slots");
+  static_assert(384 + sizeof(UnitSlots) <= C::SMEM - C::OFF_BAR, "barrier area too small");
   static_assert(C::SMEM <= 232448, "shared memory over the per-block limit");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -211,8 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool q_issued = false;
       for (;;) {
         int w;
-        if (!ring_publish(ring, kq++, p.ctr, p.n_units, abort_flag, p.status, w) || w < 0) break;
-        const Unit u = decode_unit(p, w);
+        Unit u;
+        if (!publish_unit(ring, uslots, kq++, p, abort_flag, w, u) || w < 0) break;
         if (u.n <= 0) continue;
         // test of the bounded waits: the unit is published but its Q never
         // arrives, so the MMA thread's wait for it runs out
@@ -302,8 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok) {
         int w;
-        if (!ring_take(ring, kq++, abort_flag, p.status, w) || w < 0) break;
-        const Unit u = decode_unit(p, w);
+        Unit u;
+        if (!take_unit(ring, uslots, kq++, abort_flag, p.status, w, u) || w < 0) break;
         if (u.n <= 0) continue;
         ok = mbar_wait(q_full, u_it & 1, abort_flag, p.status);
         if (!ok) break;
@@ -364,10 +427,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + wg * 128;
     const uint32_t tO = tmem + lane_off + 256 + wg * 128;
     uint32_t t_it = 0, o_it = 0, kq = 0;
-    for (;;) {
-      int w;
-      if (!ring_take_warp(ring, kq++, abort_flag, p.status, w) || w < 0) break;
-      const Unit u = decode_unit(p, w);
+    // The next unit is taken from the ring ahead of time (at the current
+    // unit's epilogue, when the producer has published it: it only waits for
+    // stages that this unit's P tiles have already released), and the load of
+    // this row's mask bound is issued then, so that neither lies between one
+    // unit's epilogue and the next unit's first tile (~2,900 cycles a unit
+    // when they did).
+    int nw = -1;
+    Unit nu{};
+    int32_t nlo = kPadLo;
+    auto take_next = [&]() -> bool {
+      if (!take_unit_warp(ring, uslots, kq++, abort_flag, p.status, nw, nu)) return false;
+      if (nw >= 0) {
+        const int ni = (wg ? nu.qt1 : nu.qt0) * kBM + r;
+        nlo = ni < p.L ? p.qlo[(size_t)nu.b * p.Lpad + ni] : kPadLo;
+      }
+      return true;
+    };
+    bool have = take_next();
+    while (have && nw >= 0) {
+      const Unit u = nu;
       const int h = wg ? u.h1 : u.h0;
       const int qt = wg ? u.qt1 : u.qt0;
       const int i = qt * kBM + r;  // local query row
@@ -375,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = p.seq_start + i;
       const uint32_t tpos = static_cast<uint32_t>(t);  // dropout counter word 1
       const uint32_t plane = static_cast<uint32_t>(u.b * p.Hq + h);
-      const int32_t lo = in_range ? p.qlo[(size_t)u.b * p.Lpad + i] : kPadLo;
+      const int32_t lo = nlo;
       const size_t row = static_cast<size_t>(u.b * p.Hq + h) * p.L + i;
       if (u.n <= 0) {
         if (in_range) {
@@ -389,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           p.lse[row] = -INFINITY;
         }
+        have = take_next();
         continue;
       }
       float m_used = -INFINITY, l = 0.f;
@@ -502,7 +582,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++t_it;
       }
       if (!ok) break;
-      // epilogue: O / l -> bf16, LSE
+      // epilogue: O / l -> bf16, LSE (the next unit taken first)
+      have = take_next();
+      if (!have) break;
       ok = mbar_wait_warp(o_full + wg, o_it & 1, abort_flag, p.status);
       if (!ok) break;
       ++o_it;
