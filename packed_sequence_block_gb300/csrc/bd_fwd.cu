@@ -165,9 +165,9 @@ __device__ __forceinline__ bool take_unit(WorkRing* r, const UnitSlots* us, uint
   mbar_arrive(&r->empty[slot]);
   return true;
 }
-__device__ __forceinline__ bool take_unit_warp(WorkRing* r, const UnitSlots* us, uint32_t k,
-                                               volatile int* abort, int32_t* status, int& w,
-                                               Unit& u) {
+__device__ __forceinline__ bool take_release_unit_warp(WorkRing* r, const UnitSlots* us,
+                                                       uint32_t k, volatile int* abort,
+                                                       int32_t* status, int& w, Unit& u) {
   const int slot = k % kRing;
   if (!mbar_wait_warp(&r->full[slot], (k / kRing) & 1, abort, status)) return false;
   w = *reinterpret_cast<volatile int*>(&r->idx[slot]);
@@ -175,6 +175,22 @@ __device__ __forceinline__ bool take_unit_warp(WorkRing* r, const UnitSlots* us,
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(&r->empty[slot]);
   return true;
+}
+// A second warp form leaves the slot taken: the warp reads the unit again
+// when it starts it (holding no registers meanwhile) and then releases it.
+__device__ __forceinline__ bool take_unit_warp(WorkRing* r, uint32_t k, volatile int* abort,
+                                               int32_t* status, int& w) {
+  const int slot = k % kRing;
+  if (!mbar_wait_warp(&r->full[slot], (k / kRing) & 1, abort, status)) return false;
+  w = *reinterpret_cast<volatile int*>(&r->idx[slot]);
+  return true;
+}
+__device__ __forceinline__ Unit release_unit_warp(WorkRing* r, const UnitSlots* us, uint32_t k) {
+  const int slot = k % kRing;
+  const Unit u = slot_unit(us, slot);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&r->empty[slot]);
+  return u;
 }
 
 // Bounded wait used at teardown for copies/MMAs already in flight: ignores
@@ -433,20 +449,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     // this row's mask bound is issued then, so that neither lies between one
     // unit's epilogue and the next unit's first tile (~2,900 cycles a unit
     // when they did).
+    // At D = 128 the slot stays taken until the unit starts (no registers
+    // held across the epilogue); at D = 64 the unit is read and the slot
+    // released at once (the other form measured 2.6% slower there).
     int nw = -1;
     Unit nu{};
     int32_t nlo = kPadLo;
     auto take_next = [&]() -> bool {
-      if (!take_unit_warp(ring, uslots, kq++, abort_flag, p.status, nw, nu)) return false;
-      if (nw >= 0) {
-        const int ni = (wg ? nu.qt1 : nu.qt0) * kBM + r;
-        nlo = ni < p.L ? p.qlo[(size_t)nu.b * p.Lpad + ni] : kPadLo;
+      if constexpr (D == 128) {
+        if (!take_unit_warp(ring, kq, abort_flag, p.status, nw)) return false;
+        if (nw >= 0) {
+          const int4 a = uslots->a[kq % kRing], b = uslots->b[kq % kRing];  // b,..,..,qt0 | qt1
+          const int ni = (wg ? b.x : a.w) * kBM + r;
+          nlo = ni < p.L ? p.qlo[(size_t)a.x * p.Lpad + ni] : kPadLo;
+        } else {
+          release_unit_warp(ring, uslots, kq);
+        }
+        ++kq;
+      } else {
+        if (!take_release_unit_warp(ring, uslots, kq++, abort_flag, p.status, nw, nu)) return false;
+        if (nw >= 0) {
+          const int ni = (wg ? nu.qt1 : nu.qt0) * kBM + r;
+          nlo = ni < p.L ? p.qlo[(size_t)nu.b * p.Lpad + ni] : kPadLo;
+        }
       }
       return true;
     };
     bool have = take_next();
     while (have && nw >= 0) {
-      const Unit u = nu;
+      Unit u = nu;
+      if constexpr (D == 128) u = release_unit_warp(ring, uslots, kq - 1);
       const int h = wg ? u.h1 : u.h0;
       const int qt = wg ? u.qt1 : u.qt0;
       const int i = qt * kBM + r;  // local query row
@@ -591,6 +623,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // the kept weights enter P V unscaled; 1 / (1 - p) joins 1 / l for out
       // (out16 keeps the normalised P V, whose entries lie within v's range)
+      // LSE before the O chunks at D = 128 (m_used and l then leave the
+      // registers before the row's 128 O values arrive); after them at D = 64
+      if (D == 128 && in_range) p.lse[row] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
       const float inv16 = (l > 0.f) ? 1.f / l : 0.f;
       const float inv = kDrop ? inv16 * p.drop.rp : inv16;
       // Each 32-column chunk of this warp's 32 rows goes through its staging
@@ -638,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_commit_group();
         }
       }
-      if (in_range) p.lse[row] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      if (D == 64 && in_range) p.lse[row] = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
       tc_fence_before();
     }
     if (lane == 0) bulk_wait_all();  // this warp's output stores are done
